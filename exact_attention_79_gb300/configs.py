@@ -1,0 +1,64 @@
+"""The five attention workloads the library is validated and measured on.
+
+Each entry names its shape, dtype, masking and scale; the FLOP counts follow
+the usual convention for attention: 4 B Hq N^2 d for the forward (two GEMMs of
+2 N^2 d each per head), halved when causal, and 2.5x that for the backward.
+"""
+import math
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str          # "fp32" or "bf16": the element type of q, k, v, o (and grads)
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool
+    backward: bool      # whether the workload includes the backward pass
+    q_mult: float = 1.0  # Q is multiplied by this before rounding (logit stress run)
+    sampled_rows: int = 0  # >0: check only this many seeded query/key rows per head
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops_fwd(self) -> float:
+        f = 4.0 * self.B * self.Hq * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    @property
+    def flops_bwd(self) -> float:
+        return 2.5 * self.flops_fwd
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name, "dtype": self.dtype, "B": self.B, "Hq": self.Hq,
+            "Hkv": self.Hkv, "N": self.N, "d": self.d, "causal": self.causal,
+            "scale": self.scale, "backward": self.backward,
+        }
+
+
+WORKLOADS = {
+    # fp32 single head, the smallest check: N=128, d=64, non-causal
+    "fp32_h1_n128_d64": Workload("fp32_h1_n128_d64", "fp32", 1, 1, 1, 128, 64, False, False),
+    # bf16 forward, 4x16 heads, N=2048, d=64, non-causal, and the same with Q x 4
+    "bf16_b4_h16_n2048_d64": Workload("bf16_b4_h16_n2048_d64", "bf16", 4, 16, 16, 2048, 64, False, False),
+    "bf16_b4_h16_n2048_d64_q4": Workload("bf16_b4_h16_n2048_d64_q4", "bf16", 4, 16, 16, 2048, 64, False, False, q_mult=4.0),
+    # Llama-2-70B-shaped GQA layer: 64 query heads on 8 KV heads, N=4096, causal
+    "bf16_gqa_b2_h64kv8_n4096_d128_causal": Workload("bf16_gqa_b2_h64kv8_n4096_d128_causal", "bf16", 2, 64, 8, 4096, 128, True, False),
+    # forward + backward, 16 heads, N=8192, causal
+    "bf16_h16_n8192_d128_causal_fwdbwd": Workload("bf16_h16_n8192_d128_causal_fwdbwd", "bf16", 1, 16, 16, 8192, 128, True, True),
+    # long sequence forward + backward, 8 heads, N=65536, causal, 256 sampled rows per head
+    "bf16_h8_n65536_d128_causal_fwdbwd": Workload("bf16_h8_n65536_d128_causal_fwdbwd", "bf16", 1, 8, 8, 65536, 128, True, True, sampled_rows=256),
+}
+
+# Tolerances against the double-precision oracle on the same rounded inputs.
+TOL_O_MAX = 2e-2        # max |O_gpu - O_ref|
+TOL_O_MEAN = 2e-3       # mean |O_gpu - O_ref|
+TOL_LSE_MAX = 1e-3      # max |LSE_gpu - LSE_ref|
+TOL_GRAD_REL_FRO = 1e-2  # ||G_gpu - G_ref||_F / ||G_ref||_F per gradient tensor

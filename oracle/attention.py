@@ -1,0 +1,265 @@
+"""Plain double-precision attention: the definition, written out.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the library never
+imports this module.
+
+Shapes (all numpy float64, C-contiguous is not required):
+    q, do, o, dq : [B, Hq, N, d]
+    k, v, dk, dv : [B, Hkv, N, d]        Hq % Hkv == 0, G = Hq // Hkv
+    lse, D       : [B, Hq, N]
+Query head h reads key/value head h // G (grouped-query attention; the
+Llama-2-70B-shaped workload maps 64 query heads onto 8 KV heads this way).
+
+Causal convention: key j is visible to query i iff j <= i (the pages skip the
+blocks whose key index exceeds the query index; one N for queries and keys, so
+there is no top-left / bottom-right ambiguity and no query row is fully masked).
+
+A library matmul serves as the inner-product step. Rows are independent, so
+computing several whole rows at once is not a change of arithmetic: no row's
+max, sum or product is ever split into partial pieces, except in
+`tiled_forward`, whose whole purpose is to restate the pages' tiled algorithm.
+"""
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+
+def _check(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, Hq, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    Hkv = k.shape[1]
+    if Hkv <= 0 or Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return B, Hq, Hkv, N, d, Hq // Hkv
+
+
+def _scores(qh, kh, scale, causal, row_index):
+    """S = scale * q k^T for the given query rows against all keys, with the
+    causal mask applied as -inf (definition; blogweb.cn section 1).
+
+    qh: [R, d] query rows whose absolute indices are row_index [R]; kh: [N, d].
+    """
+    s = scale * (qh @ kh.T)
+    if causal:
+        key_index = np.arange(kh.shape[0])
+        s = np.where(key_index[None, :] <= row_index[:, None], s, -np.inf)
+    return s
+
+
+def _softmax_rows(s):
+    """Row-wise softmax and natural-log logsumexp of one whole score row at a
+    time. The row max is subtracted before exp (numerical-stability advice,
+    mhpq.cn section 7)."""
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    lse = m + np.log(e.sum(axis=1))
+    p = np.exp(s - lse[:, None])
+    return p, lse
+
+
+def forward(q, k, v, causal, scale):
+    """O = softmax(scale * Q K^T [+ causal mask]) V and LSE = logsumexp of the
+    scaled, masked logits per query row (natural log).
+
+    The forward stores only O and the per-row normaliser (aiknowledge.cn FA3
+    section 3); LSE is that normaliser in log form.
+    Returns (o [B,Hq,N,d], lse [B,Hq,N]).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    o = np.empty((B, Hq, N, d))
+    lse = np.empty((B, Hq, N))
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows)
+            p, lse[b, h] = _softmax_rows(s)
+            o[b, h] = p @ v[b, hk]
+    return o, lse
+
+
+def backward(q, k, v, do, causal, scale):
+    """Gradients of L = <O, dO> with respect to Q, K and V.
+
+    The pages only say that the backward recomputes from the stored
+    normaliser (aiknowledge.cn FA3 section 3; deepschool.ru "Улучшение
+    backward pass"); the derivatives are the textbook ones of softmax:
+        P = exp(S - LSE),  D_i = sum_c dO_ic O_ic,  dP = dO V^T,
+        dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
+    with dK and dV summed over the G query heads that share a KV head.
+    Returns (o, lse, dq, dk, dv).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    o = np.empty((B, Hq, N, d))
+    lse = np.empty((B, Hq, N))
+    dq = np.empty((B, Hq, N, d))
+    dk = np.zeros((B, Hkv, N, d))
+    dv = np.zeros((B, Hkv, N, d))
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows)
+            p, lse[b, h] = _softmax_rows(s)
+            o[b, h] = p @ v[b, hk]
+            D = (do[b, h] * o[b, h]).sum(axis=1)
+            dp = do[b, h] @ v[b, hk].T
+            ds = p * (dp - D[:, None])
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+            dv[b, hk] += p.T @ do[b, h]
+    return o, lse, dq, dk, dv
+
+
+def forward_rows(q, k, v, causal, scale, rows):
+    """O and LSE for selected query rows only (each row costs O(N d)).
+
+    rows: int array [B, Hq, R] of query indices per head.
+    Returns (o [B,Hq,R,d], lse [B,Hq,R]).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    R = rows.shape[2]
+    o = np.empty((B, Hq, R, d))
+    lse = np.empty((B, Hq, R))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            r = rows[b, h]
+            s = _scores(q[b, h, r], k[b, hk], scale, causal, r)
+            p, lse[b, h] = _softmax_rows(s)
+            o[b, h] = p @ v[b, hk]
+    return o, lse
+
+
+def row_statistics(q, k, v, do, causal, scale, block=1024, threads=None):
+    """LSE_i and D_i = dO_i . O_i for EVERY query row, in double.
+
+    Needed to check sampled key rows of dK/dV at lengths where the full score
+    matrix does not fit: a key row's gradient sums over all query rows that
+    see it, each weighted by that row's own LSE and D. The values come from
+    this oracle alone, never from the GPU. Whole rows are computed together in
+    batches of `block`; no row is split.
+    Returns (lse [B,Hq,N], D [B,Hq,N]).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    lse = np.empty((B, Hq, N))
+    D = np.empty((B, Hq, N))
+    jobs = [(b, h, r0) for b in range(B) for h in range(Hq) for r0 in range(0, N, block)]
+
+    def run(job):
+        b, h, r0 = job
+        hk = h // G
+        r = np.arange(r0, min(r0 + block, N))
+        kmax = (r[-1] + 1) if causal else N      # keys past the last row are all masked
+        s = _scores(q[b, h, r], k[b, hk, :kmax], scale, causal, r)
+        p, lse_r = _softmax_rows(s)
+        o_r = p @ v[b, hk, :kmax]
+        lse[b, h, r] = lse_r
+        D[b, h, r] = (do[b, h, r] * o_r).sum(axis=1)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, jobs))
+    return lse, D
+
+
+def backward_rows(q, k, v, do, causal, scale, q_rows, k_rows, lse, D):
+    """dQ for selected query rows and dK, dV for selected key rows.
+
+    q_rows: [B, Hq, R] query indices; k_rows: [B, Hkv, R2] key indices.
+    lse, D: full per-row statistics [B, Hq, N] from `row_statistics` (or
+    `backward`), i.e. the oracle's own values.
+        dQ_i = scale sum_j P_ij (dP_ij - D_i) K_j
+        dK_j = scale sum_{h in group} sum_i P_ij (dP_ij - D_i) Q_i
+        dV_j = sum_{h in group} sum_i P_ij dO_i
+    with P_ij = exp(S_ij - LSE_i) and dP_ij = dO_i . V_j (see `backward`).
+    Returns (dq [B,Hq,R,d], dk [B,Hkv,R2,d], dv [B,Hkv,R2,d]).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    all_rows = np.arange(N)
+    dq = np.empty((B, Hq, q_rows.shape[2], d))
+    dk = np.zeros((B, Hkv, k_rows.shape[2], d))
+    dv = np.zeros((B, Hkv, k_rows.shape[2], d))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            r = q_rows[b, h]
+            s = _scores(q[b, h, r], k[b, hk], scale, causal, r)
+            p = np.exp(s - lse[b, h, r][:, None])
+            dp = do[b, h, r] @ v[b, hk].T
+            dq[b, h] = scale * ((p * (dp - D[b, h, r][:, None])) @ k[b, hk])
+
+            c = k_rows[b, hk]
+            # scores of every query row against the selected keys: [N, R2]
+            st = scale * (q[b, h] @ k[b, hk, c].T)
+            if causal:
+                st = np.where(c[None, :] <= all_rows[:, None], st, -np.inf)
+            pt = np.exp(st - lse[b, h][:, None])
+            dpt = do[b, h] @ v[b, hk, c].T
+            dst = pt * (dpt - D[b, h][:, None])
+            dk[b, hk] += scale * (dst.T @ q[b, h])
+            dv[b, hk] += pt.T @ do[b, h]
+    return dq, dk, dv
+
+
+def tiled_forward(q, k, v, causal, scale, block=64, deferred=True):
+    """The pages' tiled algorithm with online softmax, in double.
+
+    Follows "FlashAttention技术解析" sections 2.1-2.2: for each block of query
+    rows, stream blocks of keys; per key block compute the block scores, the
+    block max m_j, p = exp(S - m_j) and l_j = rowsum(p); merge with the
+    running statistics as m_new = max(m, m_j) and
+    l_new = e^(m - m_new) l + e^(m_j - m_new) l_j.
+      deferred=False: the section 2.1 form, which renormalises the output
+        every iteration: O <- (l/l_new) e^(m-m_new) O + (e^(m_j-m_new)/l_new) p V_j.
+      deferred=True: the FlashAttention-2 form ("FlashAttention v2相比于v1有哪些
+        更新", section 3, "Rescale操作"): keep O unnormalised,
+        O <- e^(m-m_new) O + e^(m_j-m_new) p V_j, and divide by l once at the end.
+    Causal blocks entirely above the diagonal are skipped ("Flash Attention V3
+    技术解析" section 2.1); partially masked entries are -inf. The page's
+    operators lost in extraction are read as in the formulas above.
+    Returns (o, lse) like `forward`.
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    o = np.empty((B, Hq, N, d))
+    lse = np.empty((B, Hq, N))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            for i0 in range(0, N, block):
+                ri = np.arange(i0, min(i0 + block, N))
+                qi = q[b, h, ri]
+                acc = np.zeros((len(ri), d))
+                m = np.full(len(ri), -np.inf)
+                l = np.zeros(len(ri))
+                for j0 in range(0, N, block):
+                    if causal and j0 > ri[-1]:
+                        break                      # block fully above the diagonal
+                    rj = np.arange(j0, min(j0 + block, N))
+                    s = scale * (qi @ k[b, hk, rj].T)
+                    if causal:
+                        s = np.where(rj[None, :] <= ri[:, None], s, -np.inf)
+                    m_j = s.max(axis=1)
+                    p = np.exp(s - m_j[:, None])
+                    l_j = p.sum(axis=1)
+                    m_new = np.maximum(m, m_j)
+                    alpha = np.exp(m - m_new)      # exp(-inf) = 0 on the first block
+                    beta = np.exp(m_j - m_new)
+                    l_new = alpha * l + beta * l_j
+                    pv = p @ v[b, hk, rj]
+                    if deferred:
+                        acc = alpha[:, None] * acc + beta[:, None] * pv
+                    else:
+                        acc = ((l / l_new) * alpha)[:, None] * acc + (beta / l_new)[:, None] * pv
+                    m, l = m_new, l_new
+                o[b, h, ri] = acc / l[:, None] if deferred else acc
+                lse[b, h, ri] = m + np.log(l)
+    return o, lse
+
+
+__all__ = [
+    "forward", "backward", "forward_rows", "row_statistics", "backward_rows",
+    "tiled_forward",
+]
