@@ -1,0 +1,133 @@
+"""Exact attention for GB300 (sm_103a): Python binding of the C ABI in
+include/fa.h.
+
+This module only marshals arguments: every step of the forward and backward
+runs in the CUDA library libfa_gb300.so, built in-tree by
+`__graft_entry__.build()`. There is no fallback: if the library is missing or
+the device is not sm_103, the calls raise.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK = 0
+_STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ARCH",
+    4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_DEVICE",
+}
+
+# Every symbol include/fa.h declares, with its ctypes signature.
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fwd_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                    _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_device_status": (_I, [_VP]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_version": (_I, []),
+}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        msg = _lib.fa_status_string(code).decode() if _lib is not None else ""
+        super().__init__(f"{fn} returned {_STATUS_NAMES.get(code, code)}: {msg}")
+
+
+def load(path=None):
+    """Load the compiled library (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != FA_OK:
+        raise FAError(fn, code)
+
+
+def _stream(t):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _shape(q, k):
+    B, Hq, N, d = q.shape
+    return B, Hq, k.shape[1], N, d
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
+    """O, LSE = attention(q, k, v) on the current stream.
+
+    q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; bf16 (fa_fwd) or fp32 (fa_fwd_f32)
+    contiguous CUDA tensors. Returns (o like q, lse fp32 [B, Hq, N])."""
+    import torch
+    lib = load()
+    B, Hq, Hkv, N, d = _shape(q, k)
+    if scale is None:
+        scale = d ** -0.5
+    for t in (q, k, v):
+        if not t.is_contiguous() or not t.is_cuda or t.dtype != q.dtype:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    fn = {torch.bfloat16: "fa_fwd", torch.float32: "fa_fwd_f32"}.get(q.dtype)
+    if fn is None:
+        raise ValueError("dtype must be bfloat16 or float32")
+    _check(fn, getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
+    return o, lse
+
+
+def bwd_workspace_bytes(B, Hq, Hkv, N, d):
+    return int(load().fa_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None):
+    """dQ, dK, dV of <O, dO> on the current stream (bf16 tensors, fp32 lse)."""
+    import torch
+    lib = load()
+    B, Hq, Hkv, N, d = _shape(q, k)
+    if scale is None:
+        scale = d ** -0.5
+    for t in (q, k, v, o, do):
+        if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
+    nbytes = bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check("fa_bwd", lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                                B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
+    return dq, dk, dv
+
+
+def check_device_status(stream=None):
+    """Synchronise the stream and raise if a kernel's bounded wait ran out."""
+    import torch
+    s = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    _check("fa_device_status", load().fa_device_status(s))

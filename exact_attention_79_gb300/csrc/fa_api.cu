@@ -1,0 +1,248 @@
+// C ABI of the attention library: argument validation, TMA tensor maps,
+// kernel dispatch and the device status word. See include/fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+// Set by kernels whose bounded waits ran out; read and cleared by fa_device_status.
+__device__ unsigned g_status_word;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  std::once_flag once;
+  bool arch_ok = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Checks the current device once (compute capability 10.3) and resolves the
+// device address of the status word on it.
+fa_status device_state(unsigned** status_out, int* num_sms = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  DeviceState& s = g_dev[dev];
+  std::call_once(s.once, [&s, dev] {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
+    s.arch_ok = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) s.num_sms = 0;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) s.status = static_cast<unsigned*>(p);
+  });
+  if (!s.arch_ok) return FA_ERR_ARCH;
+  if (!s.status || s.num_sms <= 0) return FA_ERR_CUDA;
+  *status_out = s.status;
+  if (num_sms) *num_sms = s.num_sms;
+  return FA_OK;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long ns = [] {
+    const char* e = std::getenv("FA_WAIT_LIMIT_MS");
+    long ms = e ? std::strtol(e, nullptr, 10) : 0;
+    if (ms <= 0) ms = 2000;
+    return static_cast<unsigned long long>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D map over a dense [BH, N, d] tensor: dims (d, N, BH), one box = 128 rows
+// by 128 bytes with 128-byte swizzle. Rows past N read as zero and are not
+// written by stores.
+bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long long BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elt_bytes,
+                                 static_cast<cuuint64_t>(d) * N * elt_bytes};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                         const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * Hq;
+  const long long nq = (N + 127) / 128;
+  if (BH > (1LL << 24) || ((nq + 1) / 2) * BH >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                     int Hkv, int N, int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
+  if (st != FA_OK) return st;
+  if (elt == 4 && d != 64) return FA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = device_state(&status);
+  if (st != FA_OK) return st;
+  CUtensorMap mq, mk, mv, mo;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, N, BHkv) || !make_map(&mv, v, elt, d, N, BHkv) ||
+      !make_map(&mo, o, elt, d, N, BHq))
+    return FA_ERR_CUDA;
+  fa::FwdParams p{};
+  p.lse = lse;
+  p.status = status;
+  p.N = N;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.BH = static_cast<int>(BHq);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_limit_ns();
+  const cudaError_t e = fa::launch_fwd(elt, d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct BwdWorkspace {
+  size_t off_lse2, off_d, off_dq, total;
+};
+
+BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
+  const size_t BH = static_cast<size_t>(B) * Hq;
+  const size_t NQP = static_cast<size_t>((N + 127) / 128) * 128;
+  BwdWorkspace w;
+  w.off_lse2 = 0;
+  w.off_d = align256(BH * NQP * 4);
+  w.off_dq = w.off_d + align256(BH * NQP * 4);
+  w.total = w.off_dq + align256(BH * static_cast<size_t>(N) * d * 4);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK) return 0;
+  return bwd_workspace(B, Hq, N, d).total;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                 int N, int d, int causal, float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
+  if (st != FA_OK) return st;
+  const BwdWorkspace w = bwd_workspace(B, Hq, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  int num_sms = 0;
+  st = device_state(&status, &num_sms);
+  if (st != FA_OK) return st;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  fa::BwdMaps m;
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv))
+    return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdParams p{};
+  p.ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
+  p.ws_d = reinterpret_cast<float*>(ws + w.off_d);
+  p.ws_dq = reinterpret_cast<float*>(ws + w.off_dq);
+  p.status = status;
+  p.N = N;
+  p.NQP = ((N + 127) / 128) * 128;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.BH = static_cast<int>(BHq);
+  p.BHkv = static_cast<int>(BHkv);
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_limit_ns();
+  fa::BwdTensors t{o, dO, lse, dq};
+  const cudaError_t e = fa::launch_bwd(d, t, m, p, num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                 int d, int causal, float scale, void* stream) {
+  return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq, int Hkv,
+                     int N, int d, int causal, float scale, void* stream) {
+  return fwd_common(4, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_device_status(void* stream) {
+  unsigned* status = nullptr;
+  fa_status st = device_state(&status);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned host = 0;
+  if (cudaMemcpyFromSymbol(&host, g_status_word, sizeof(host)) != cudaSuccess) return FA_ERR_CUDA;
+  if (host != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return (host & 1u) ? FA_ERR_TIMEOUT : FA_ERR_DEVICE;
+  }
+  return FA_OK;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, or bad size)";
+    case FA_ERR_UNSUPPORTED: return "unsupported combination of sizes or types";
+    case FA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out; outputs of that call are invalid";
+    case FA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case FA_ERR_DEVICE: return "a kernel refused to run on this device's shared-memory layout; outputs invalid";
+  }
+  return "unknown status";
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

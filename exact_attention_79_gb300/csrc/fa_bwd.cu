@@ -1,0 +1,463 @@
+// Backward exact attention on sm_103a: dQ, dK, dV of <O, dO> recomputed from
+// the stored logsumexp.
+//
+// Method: the forward keeps only O and the softmax normaliser and the
+// backward recomputes the probabilities from it ("4.3 FlashAttention-2与
+// FlashAttention-3演进", FlashAttention-3 section 3); the backward is blockwise
+// like the forward (deepschool.ru FlashAttention-2, "Улучшение backward pass");
+// dQ is accumulated with asynchronous fp32 atomic adds in wide transactions
+// ("Flash Attention V3技术解析" 2.1, "梯度计算").
+//
+// Three launches on one stream:
+//  1. bwd_pre_kernel   D_i = sum_c dO_ic O_ic, LSE_i * log2(e) into a padded
+//                      per-tile layout (padding: D = 0, LSE = +inf so that the
+//                      padded query rows get P = 0), and dQacc = 0.
+//  2. bwd_dkdv_kernel  one CTA per 128-key tile of one (batch, KV head). For
+//                      each query head of the group and each query tile that
+//                      can see these keys:
+//                        S^T  = K Q_i^T            (TMEM)
+//                        dP^T = V dO_i^T           (TMEM)
+//                        P^T  = 2^(S^T s log2e - LSE_i log2e)   (registers -> TMEM, bf16)
+//                        dS^T = P^T (dP^T - D_i)   (registers -> shared memory, bf16)
+//                        dV  += P^T dO_i,  dK += dS^T Q_i      (TMEM accumulators)
+//                        dQ_i = dS K               (TMEM, then fp32 atomics into dQacc)
+//                      and finally dK *= scale; dK, dV stored once (deterministic).
+//  3. bwd_dq_kernel    dQ = scale * dQacc -> bf16.
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+
+// ------------------------------------------------------------------ preprocess
+// One 16-lane group per row (d = 128: 8 bf16 per lane; d = 64: 4 per lane).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      const float* __restrict__ lse, BwdParams p) {
+  constexpr int kPer = D / 16;
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthreads = gridDim.x * blockDim.x;
+  const long long rows = static_cast<long long>(p.BH) * p.NQP;
+  // each warp takes two rows per iteration (one per half-warp); the loop trip
+  // count is uniform across the warp so the shuffles below see every lane
+  for (long long w = tid / 32; 2 * w < rows; w += nthreads / 32) {
+    const long long r = 2 * w + ((tid >> 4) & 1);
+    const bool valid_row = r < rows;
+    const int bh = valid_row ? static_cast<int>(r / p.NQP) : 0;
+    const int i = valid_row ? static_cast<int>(r % p.NQP) : p.N;
+    float acc = 0.f;
+    if (i < p.N) {
+      const size_t off = (static_cast<size_t>(bh) * p.N + i) * D + (tid & 15) * kPer;
+      if constexpr (kPer == 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(a2[e]);
+          const float2 y = __bfloat1622float2(b2[e]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
+      } else {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 b = *reinterpret_cast<const uint2*>(dO + off);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 x = __bfloat1622float2(a2[e]);
+          const float2 y = __bfloat1622float2(b2[e]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int s = 8; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if ((tid & 15) == 0 && valid_row) {
+      p.ws_d[r] = acc;
+      p.ws_lse2[r] = (i < p.N) ? lse[static_cast<size_t>(bh) * p.N + i] * kLog2e : INFINITY;
+    }
+  }
+  const long long n4 = static_cast<long long>(p.BH) * p.N * D / 4;
+  float4* acc4 = reinterpret_cast<float4*>(p.ws_dq);
+  for (long long x = tid; x < n4; x += nthreads) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ dQ convert
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(__nv_bfloat16* __restrict__ dq, BwdParams p) {
+  const long long n8 = static_cast<long long>(p.BH) * p.N * D / 8;
+  const float4* src = reinterpret_cast<const float4*>(p.ws_dq);
+  uint4* dst = reinterpret_cast<uint4*>(dq);
+  const float s = p.scale;
+  for (long long x = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; x < n8;
+       x += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = src[2 * x], b = src[2 * x + 1];
+    uint4 r;
+    r.x = pack_bf16x2(a.x * s, a.y * s);
+    r.y = pack_bf16x2(a.z * s, a.w * s);
+    r.z = pack_bf16x2(b.x * s, b.y * s);
+    r.w = pack_bf16x2(b.z * s, b.w * s);
+    dst[x] = r;
+  }
+}
+
+// ------------------------------------------------------------------ dK / dV
+template <int D>
+struct BwdCfg {
+  static constexpr int kNBox = D / 64;                 // bf16: 64 elements per 128-byte row
+  static constexpr int kTileBytes = kNBox * kBoxBytes;  // one [128, D] bf16 tile
+  static constexpr int kDsBytes = 2 * kBoxBytes;       // dS^T [128 keys, 128 queries] bf16
+  static constexpr int kVecBytes = 512;                // 128 fp32 (LSE or D of one query tile)
+  // shared memory: K | V | dS^T | stage0 {Q, dO} | stage1 {Q, dO} | lse2[2] | D[2] | barriers
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffDs = 2 * kTileBytes;
+  static constexpr int kOffStage = kOffDs + kDsBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kOffVec = kOffStage + 2 * kStageBytes;
+  static constexpr int kOffBar = kOffVec + 4 * kVecBytes;
+  static constexpr int kLayoutBytes = kOffBar + 128;
+  static constexpr int kSmemAlloc = 232448;            // the per-block maximum; the base is aligned inside it
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  static constexpr int kThreads = 320;
+  static_assert(kLayoutBytes <= kSmemAlloc, "shared memory budget");
+  static_assert(2 * D + 256 <= 512, "TMEM budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
+                const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  if ((base - raw) + C::kLayoutBytes > static_cast<uint32_t>(C::kSmemAlloc)) {
+    // The layout needs the dynamic window to start within 896 bytes of a
+    // 1 KB boundary; refuse (and report) rather than overrun.
+    if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
+    return;
+  }
+  const uint32_t s_k = base + C::kOffK, s_v = base + C::kOffV, s_ds = base + C::kOffDs;
+  auto s_q = [&](int st) { return base + C::kOffStage + st * C::kStageBytes; };
+  auto s_do = [&](int st) { return base + C::kOffStage + st * C::kStageBytes + C::kTileBytes; };
+  auto s_lse = [&](int st) { return base + C::kOffVec + st * C::kVecBytes; };
+  auto s_dvec = [&](int st) { return base + C::kOffVec + (2 + st) * C::kVecBytes; };
+  const uint32_t bars = base + C::kOffBar;
+  const uint32_t bar_kv_full = bars;
+  auto bar_q_full = [&](int st) { return bars + 8u + 8u * st; };
+  auto bar_q_empty = [&](int st) { return bars + 24u + 8u * st; };
+  const uint32_t bar_s_full = bars + 40, bar_p_ready = bars + 48, bar_dq_full = bars + 56;
+  const uint32_t bar_dq_free = bars + 64, bar_o_final = bars + 72;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 80);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 84);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: (key tile, batch * kv head); the key tiles with the most
+  // query tiles to visit (small index when causal) go first
+  const int jt = blockIdx.x / p.BHkv;
+  const int bhkv = blockIdx.x % p.BHkv;
+  const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int nq = p.NQP / kBM;
+  const int it0 = p.causal ? jt : 0;
+  const int tiles_per_head = nq - it0;
+  const int nsteps = G * tiles_per_head;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_kv_full, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(bar_q_full(st), 1);
+      mbar_init(bar_q_empty(st), 1);
+    }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_p_ready, 256);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_dq_free, 256);
+    mbar_init(bar_o_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_do);
+      mbar_arrive_expect_tx(bar_kv_full, 2 * C::kTileBytes);
+      for (int bx = 0; bx < C::kNBox; ++bx) {
+        tma_load_3d(s_k + bx * kBoxBytes, &map_k, bar_kv_full, bx * 64, jt * kBN, bhkv);
+        tma_load_3d(s_v + bx * kBoxBytes, &map_v, bar_kv_full, bx * 64, jt * kBN, bhkv);
+      }
+      for (int step = 0; step < nsteps; ++step) {
+        const int st = step & 1;
+        if (!mbar_wait(bar_q_empty(st), ((step >> 1) & 1) ^ 1, abort_flag, deadline)) break;
+        const int h = hk * G + step / tiles_per_head;
+        const int it = it0 + step % tiles_per_head;
+        const int bh = b * p.Hq + h;
+        mbar_arrive_expect_tx(bar_q_full(st), 2 * C::kTileBytes + 2 * C::kVecBytes);
+        for (int bx = 0; bx < C::kNBox; ++bx) {
+          tma_load_3d(s_q(st) + bx * kBoxBytes, &map_q, bar_q_full(st), bx * 64, it * kBM, bh);
+          tma_load_3d(s_do(st) + bx * kBoxBytes, &map_do, bar_q_full(st), bx * 64, it * kBM, bh);
+        }
+        const size_t voff = static_cast<size_t>(bh) * p.NQP + static_cast<size_t>(it) * kBM;
+        bulk_load(s_lse(st), p.ws_lse2 + voff, C::kVecBytes, bar_q_full(st));
+        bulk_load(s_dvec(st), p.ws_d + voff, C::kVecBytes, bar_q_full(st));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ tensor-core issuer
+    if (lane == 0) {
+      const uint32_t id_kk = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+      const uint32_t id_kmn = make_idesc(1, 128, D, 0, 1);   // dV, dK: A K-major (or TMEM), B MN-major
+      const uint32_t id_mnmn = make_idesc(1, 128, D, 1, 1);  // dQ: A = dS (MN-major view of dS^T), B = K MN-major
+      bool ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
+      for (int step = 0; step < nsteps && ok; ++step) {
+        const int st = step & 1;
+        if (!mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
+        if (step > 0 && !mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline)) { ok = false; break; }
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T (K = d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + C::kColS, smem_desc_sw128(s_k + off, 16, 1024),
+                      smem_desc_sw128(s_q(st) + off, 16, 1024), id_kk, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + C::kColDP, smem_desc_sw128(s_v + off, 16, 1024),
+                      smem_desc_sw128(s_do(st) + off, 16, 1024), id_kk, kk > 0);
+        }
+        mma_commit(bar_s_full);
+        if (!mbar_wait(bar_p_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
+        tc_fence_after();
+        // dV += P^T dO  (K = 128 queries; P^T of query q sits in S column 64*(q/64) + (q%64)/2)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a = tbase + C::kColS + 64 * (kk >> 2) + (kk & 3) * 8;
+          mma_bf16_ts(tbase + C::kColDV, a, smem_desc_sw128(s_do(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn,
+                      step > 0 || kk > 0);
+        }
+        // dK += dS^T Q  (A = dS^T K-major over queries)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + C::kColDK, smem_desc_sw128(s_ds + off, 16, 1024),
+                      smem_desc_sw128(s_q(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn, step > 0 || kk > 0);
+        }
+        // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_bf16_ss(tbase + C::kColS, smem_desc_sw128(s_ds + kk * 16 * 128, kBoxBytes, 1024),
+                      smem_desc_sw128(s_k + kk * 16 * 128, kBoxBytes, 1024), id_mnmn, kk > 0);
+        }
+        mma_commit(bar_dq_full);
+        mma_commit(bar_q_empty(st));
+      }
+      if (ok) mma_commit(bar_o_final);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax-gradient groups
+    const int g = (warp - 2) >> 2;                 // query-column half: [64g, 64g + 64)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;             // key row (TMEM lane); query row for the dQ drain
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool key_pad = jt * kBN + r >= p.N;      // key rows past N contribute nothing
+    bool ok = true;
+    for (int step = 0; step < nsteps && ok; ++step) {
+      const int st = step & 1;
+      const int h = hk * G + step / tiles_per_head;
+      const int it = it0 + step % tiles_per_head;
+      const bool diag = p.causal && it == jt;
+      ok = mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline) &&
+           mbar_wait(bar_s_full, step & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(gbase + (s_lse(st) - base));
+      const float* dvec = reinterpret_cast<const float*>(gbase + (s_dvec(st) - base));
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * g + 32 * ch;            // first query column of this chunk
+        uint32_t sv[32], dp[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + c0, sv);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + c0, dp);
+        tmem_wait_ld();
+        reg_fence_x32(sv);
+        reg_fence_x32(dp);
+        uint32_t pp[16], dd[16];
+        const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
+        const float4* d4 = reinterpret_cast<const float4*>(dvec + c0);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 lv = l4[c / 4], dv4 = d4[c / 4];
+          const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+          const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          float pr[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = c0 + c + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, -lq[e]));
+            if (key_pad || (diag && q < r)) pv = 0.f;
+            pr[e] = pv;
+            ds[e] = pv * (__uint_as_float(dp[c + e]) - dq4[e]);
+          }
+          pp[c / 2] = pack_bf16x2(pr[0], pr[1]);
+          pp[c / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+          dd[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          dd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        // P^T (bf16 pairs) into TMEM over the S^T columns this group already read
+        tmem_st_32x32b_x16(tbase + lane_off + C::kColS + 64 * g + 16 * ch, pp);
+        // dS^T row r, query columns [c0, c0 + 32): four 16-byte units of box g
+        const uint32_t box = s_ds + g * kBoxBytes;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, 4 * ch + u)),
+                       "r"(dd[4 * u]), "r"(dd[4 * u + 1]), "r"(dd[4 * u + 2]), "r"(dd[4 * u + 3]) : "memory");
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_p_ready);
+
+      // ---- dQ_i drain: TMEM lane = query row r of tile `it`; this group takes columns [g D/2, (g+1) D/2)
+      ok = mbar_wait(bar_dq_full, step & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dq[D / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t t[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + g * (D / 2) + c0, t);
+        tmem_wait_ld();
+        reg_fence_x32(t);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dq[c0 + c] = t[c];
+      }
+      tc_fence_before();
+      mbar_arrive(bar_dq_free);
+      const int qrow = it * kBM + r;
+      if (qrow < p.N) {
+        float4* dst = reinterpret_cast<float4*>(
+            p.ws_dq + ((static_cast<size_t>(b) * p.Hq + h) * p.N + qrow) * D + g * (D / 2));
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u)
+          atomicAdd(dst + u, make_float4(__uint_as_float(dq[4 * u]), __uint_as_float(dq[4 * u + 1]),
+                                         __uint_as_float(dq[4 * u + 2]), __uint_as_float(dq[4 * u + 3])));
+      }
+    }
+    // ---------------------------------------------------------- dK, dV epilogue
+    if (ok) {
+      ok = mbar_wait(bar_o_final, 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      // staging: stage 0's Q buffer for dV, its dO buffer for dK (both idle now)
+      const uint32_t stg_v = s_q(0), stg_k = s_do(0);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which ? p.scale : 1.0f;
+        const uint32_t col = which ? C::kColDK : C::kColDV;
+        const uint32_t stg = which ? stg_k : stg_v;
+#pragma unroll
+        for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
+          uint32_t t[32];
+          tmem_ld_32x32b_x32(tbase + lane_off + col + c0, t);
+          tmem_wait_ld();
+          reg_fence_x32(t);
+          const uint32_t box = stg + (c0 / 64) * kBoxBytes;
+          const int u0 = (c0 % 64) / 8;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(t[8 * u + 2 * e]) * mul, __uint_as_float(t[8 * u + 2 * e + 1]) * mul);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, u0 + u)),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (warp == 2 && lane == 0) {
+        for (int bx = 0; bx < C::kNBox; ++bx) {
+          tma_store_3d(&map_dv, stg_v + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+          tma_store_3d(&map_dk, stg_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+        }
+        tma_store_commit();
+        tma_store_wait_all0();
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    abort_grace_period();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ launch
+template <int D>
+static cudaError_t launch_bwd_d(const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
+                                cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int small_grid = num_sms * 4;
+  bwd_pre_kernel<D><<<small_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(t.o),
+                                                    static_cast<const __nv_bfloat16*>(t.dO), t.lse, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = (p.NQP / kBN) * p.BHkv;
+  bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<D><<<small_grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(t.dq), p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int d, const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
+                       cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128>(t, m, p, num_sms, stream);
+  if (d == 64) return launch_bwd_d<64>(t, m, p, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

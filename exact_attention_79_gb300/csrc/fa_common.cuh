@@ -1,0 +1,41 @@
+// Shared definitions for the attention kernels (device side).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+// Bits of the device status word (read and cleared by fa_device_status).
+constexpr unsigned kDevTimeout = 1u;      // a bounded wait inside a kernel ran out
+constexpr unsigned kDevLayout = 2u;       // a kernel refused to run: shared-memory window misaligned
+
+// Tile geometry shared by every kernel: 128 query rows x 128 keys, the
+// tcgen05 M=128 shape, and 128-byte swizzled shared-memory rows.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 128 bytes
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// After a timed-out wait: keep the CTA alive for a grace period so that TMA
+// copies and tensor-core operations already in flight land before shared
+// memory and TMEM are released.
+__device__ __forceinline__ void abort_grace_period() {
+  uint64_t until = global_timer_ns() + 2000000ull;   // 2 ms
+  while (global_timer_ns() < until) __nanosleep(10000);
+}
+
+// Byte address, inside a 128-byte-swizzled box, of 16-byte unit `u` (0..7)
+// of row `r`: the unit index is XORed with the row's position in its 8-row
+// (1024-byte) group. This is the layout TMA writes with 128-byte swizzle and
+// the layout the UMMA descriptors below describe.
+__device__ __forceinline__ uint32_t swz128(uint32_t box_base, int r, int u) {
+  return box_base + r * 128 + ((u ^ (r & 7)) << 4);
+}
+
+}  // namespace fa

@@ -1,0 +1,448 @@
+// Forward exact attention on sm_103a: O = softmax(scale Q K^T [+ causal]) V
+// and the per-row natural-log logsumexp, with the N x N scores never leaving
+// the SM.
+//
+// Method (pages on FlashAttention v1-v3):
+//  * tiling over key/value blocks with an online softmax that keeps a running
+//    max m and running sum l per query row ("FlashAttention技术解析" 2.1-2.2);
+//  * output kept unnormalised, divided by l once at the end
+//    ("FlashAttention v2相比于v1有哪些更新" section 3, "Rescale操作");
+//  * Q outer, K/V inner, each CTA owns its output tile, no atomics in the
+//    forward (same page, section 5; "FlashAttention技术解析" section 7);
+//  * producer / consumer warp specialisation and ping-pong of two softmax
+//    groups against the tensor core ("Flash Attention V3技术解析" 1.2);
+//  * causal blocks above the diagonal skipped ("Flash Attention V3技术解析" 2.1).
+//
+// GB300 mapping. One CTA = two 128-row query tiles of one (batch, head):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a slot ring
+//   warp 1      tensor-core issuer (one thread) + TMEM owner
+//   warps 2-5   softmax group 0 (query tile 0), one thread per query row
+//   warps 6-9   softmax group 1 (query tile 1)
+// TMEM (512 columns x 128 lanes, fp32): S0 | S1 | O0 | O1. The probabilities P
+// overwrite S in place (bf16 pairs, or tf32) and feed O += P V with A read
+// from TMEM. The rescale of O happens only when a row max grows by more than
+// 2^8 (log2 units of the scaled logits); O and l always share the same
+// reference max, so the final O / l and LSE are unchanged by that choice.
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+
+template <typename T, int D>
+struct FwdCfg {
+  static constexpr int kElt = sizeof(T);
+  static constexpr bool kTf32 = (kElt == 4);
+  static constexpr int kChunk = 128 / kElt;           // elements per 128-byte swizzle row
+  static constexpr int kNBox = D / kChunk;            // TMA boxes per 128-row tile
+  static constexpr int kTileBytes = kNBox * kBoxBytes;
+  static constexpr int kUmmaK = 32 / kElt;            // K per MMA instruction (32 bytes)
+  static constexpr int kStages = (kTileBytes == 16384) ? 8 : 4;   // K/V slot ring
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }
+  static __device__ __forceinline__ uint32_t col_o(int i) { return 256u + D * i; }
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + kBarBytes + 1024;
+  static constexpr uint32_t kFmt = kTf32 ? 2u : 1u;
+  // tf32 operands must be K-major, so V (d contiguous) cannot feed the P V
+  // product directly: the fp32 variant runs one query tile per CTA and its
+  // softmax group transposes each V tile into a K-major V^T buffer (the idle
+  // second query-tile slot). bf16 runs two ping-ponged query tiles per CTA.
+  static constexpr bool kPingPong = !kTf32;
+  static constexpr int kTilesPerCta = kPingPong ? 2 : 1;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(2 * 128 + 2 * D <= 512, "TMEM budget");
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc) {
+  using C = FwdCfg<T, D>;
+#pragma unroll
+  for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
+    const uint32_t kb = kk * 32;                              // byte offset along d
+    const uint32_t off = (kb / 128) * kBoxBytes + (kb % 128);
+    const uint64_t a = smem_desc_sw128(sq + off, 16, 1024);
+    const uint64_t b = smem_desc_sw128(sk + off, 16, 1024);
+    if constexpr (C::kTf32) mma_tf32_ss(d_tmem, a, b, idesc, kk > 0);
+    else mma_bf16_ss(d_tmem, a, b, idesc, kk > 0);
+  }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sv, uint32_t idesc, bool acc) {
+  using C = FwdCfg<T, D>;
+#pragma unroll
+  for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
+    const uint32_t a = p_tmem + kk * 8;                       // 8 TMEM columns per K step
+    if constexpr (C::kTf32) {
+      // sv = V^T [d rows, 128 keys], K-major: four boxes of 32 keys, each D rows x 128 bytes
+      const uint32_t kb = kk * 32;
+      const uint64_t b = smem_desc_sw128(sv + (kb / 128) * (D * 128) + (kb % 128), 16, 1024);
+      mma_tf32_ts(d_tmem, a, b, idesc, acc || kk > 0);
+    } else {
+      // V tile is [keys, d] with d contiguous: MN-major B operand. Leading byte
+      // offset = distance between 128-byte column chunks (one TMA box), stride
+      // byte offset = distance between 8-key groups.
+      const uint64_t b = smem_desc_sw128(sv + kk * C::kUmmaK * 128, kBoxBytes, 1024);
+      mma_bf16_ts(d_tmem, a, b, idesc, acc || kk > 0);
+    }
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+           const FwdParams p) {
+  using C = FwdCfg<T, D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+
+  const uint32_t s_q[2] = {base, base + C::kTileBytes};
+  const uint32_t s_kv = base + 2 * C::kTileBytes;
+  const uint32_t bars = s_kv + C::kStages * C::kTileBytes;
+  auto bar_q_full = [&](int i) { return bars + 8u * i; };                       // 2
+  auto bar_kv_full = [&](int s) { return bars + 16u + 8u * s; };               // kStages
+  auto bar_kv_empty = [&](int s) { return bars + 16u + 8u * (C::kStages + s); };
+  auto bar_s_full = [&](int i) { return bars + 16u + 16u * C::kStages + 8u * i; };
+  auto bar_p_ready = [&](int i) { return bars + 32u + 16u * C::kStages + 8u * i; };
+  auto bar_o_final = [&](int i) { return bars + 48u + 16u * C::kStages + 8u * i; };
+  uint8_t* const gbars = gbase + (bars - base);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 64 + 16 * C::kStages);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 68 + 16 * C::kStages);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: (query-tile pair, batch*head), heaviest causal pairs first
+  const int lin = blockIdx.x;
+  const int pair = p.num_pairs - 1 - lin / p.BH;
+  const int bh = lin % p.BH;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int nq = (p.N + kBM - 1) / kBM;
+  const int qt[2] = {C::kTilesPerCta * pair, C::kTilesPerCta * pair + 1};
+  int nkv[2];
+  nkv[0] = p.causal ? qt[0] + 1 : nq;
+  nkv[1] = (C::kPingPong && qt[1] < nq) ? (p.causal ? qt[1] + 1 : nq) : 0;
+  const int nmax = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_q_full(i), 1);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_p_ready(i), 128);
+      mbar_init(bar_o_final(i), 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      for (int i = 0; i < 2; ++i) {
+        if (nkv[i] == 0) continue;
+        mbar_arrive_expect_tx(bar_q_full(i), C::kTileBytes);
+        for (int bx = 0; bx < C::kNBox; ++bx)
+          tma_load_3d(s_q[i] + bx * kBoxBytes, &map_q, bar_q_full(i), bx * C::kChunk, qt[i] * kBM, bh);
+      }
+      for (int c = 0; c < 2 * nmax; ++c) {
+        const int slot = c % C::kStages;
+        const uint32_t round = c / C::kStages;
+        if (!mbar_wait(bar_kv_empty(slot), (round & 1u) ^ 1u, abort_flag, deadline)) break;
+        mbar_arrive_expect_tx(bar_kv_full(slot), C::kTileBytes);
+        const CUtensorMap* m = (c & 1) ? &map_v : &map_k;
+        const uint32_t dst = s_kv + slot * C::kTileBytes;
+        for (int bx = 0; bx < C::kNBox; ++bx)
+          tma_load_3d(dst + bx * kBoxBytes, m, bar_kv_full(slot), bx * C::kChunk, (c >> 1) * kBN, bh_kv);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ tensor-core issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = make_idesc(C::kFmt, 128, 128, 0, 0);
+      const uint32_t idesc_pv = make_idesc(C::kFmt, 128, D, 0, C::kTf32 ? 0 : 1);
+      const uint32_t s_vt = s_q[1];                 // V^T buffer of the fp32 variant
+      bool ok = true;
+      for (int i = 0; i < 2 && ok; ++i)
+        if (nkv[i] > 0) ok = mbar_wait(bar_q_full(i), 0, abort_flag, deadline);
+      int c = 0;
+      auto take = [&](uint32_t& slot_addr, int& slot) -> bool {
+        slot = c % C::kStages;
+        const bool r = mbar_wait(bar_kv_full(slot), (c / C::kStages) & 1, abort_flag, deadline);
+        slot_addr = s_kv + slot * C::kTileBytes;
+        ++c;
+        return r;
+      };
+      uint32_t sk = 0;
+      int kslot = 0;
+      if (ok) ok = take(sk, kslot);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < 2; ++i) {
+          if (nkv[i] == 0) continue;
+          issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk, idesc_qk);
+          mma_commit(bar_s_full(i));
+        }
+        mma_commit(bar_kv_empty(kslot));
+      }
+      for (int j = 0; j < nmax && ok; ++j) {
+        uint32_t sv = 0, sk_next = 0;
+        int vslot = 0, knext = 0;
+        const bool has_next = j + 1 < nmax;
+        ok = take(sv, vslot);
+        if (ok && has_next) ok = take(sk_next, knext);
+        if (!ok) break;
+        for (int i = 0; i < 2; ++i) {
+          if (j >= nkv[i]) continue;
+          if (!mbar_wait(bar_p_ready(i), j & 1, abort_flag, deadline)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<T, D>(tbase + C::col_o(i), tbase + C::col_s(i), C::kTf32 ? s_vt : sv, idesc_pv, j > 0);
+          if (j + 1 < nkv[i]) {
+            issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk_next, idesc_qk);
+            mma_commit(bar_s_full(i));
+          } else {
+            mma_commit(bar_o_final(i));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar_kv_empty(vslot));
+        if (has_next) mma_commit(bar_kv_empty(knext));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int g = (warp - 2) >> 2;                 // 0 or 1
+    const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;           // query row within the tile
+    const int n_kv = nkv[g];
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tbase + lane_off + C::col_s(g);
+    const uint32_t t_o = tbase + lane_off + C::col_o(g);
+    const int q_row = qt[g] * kBM + row;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;                           // running max, log2 units of scale*s
+    float l = 0.f;                                 // running sum relative to m
+    bool ok = n_kv > 0;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      ok = mbar_wait(bar_s_full(g), j & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(t_s + q4 * 32, sr[q4]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      // mask: causal diagonal tile and the ragged tail of the key range
+      int lim = kBN;
+      const int kv0 = j * kBN;
+      if (p.causal && j == qt[g]) lim = row + 1;
+      if (kv0 + kBN > p.N) lim = min(lim, p.N - kv0);
+      if (lim < kBN) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool grow = mx > m + 8.0f;             // also true on the first tile (m = -inf)
+      const float m_new = grow ? mx : m;
+      const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+      m = m_new;
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;   // a row with no visible key yet keeps P = 0
+      float sum0 = 0.f, sum1 = 0.f;
+      if constexpr (C::kTf32) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pr[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = ex2_approx(fmaf(s[q4 * 32 + c], sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(s[q4 * 32 + c + 1], sl2, neg_m));
+            sum0 += p0;
+            sum1 += p1;
+            pr[c] = __float_as_uint(p0);
+            pr[c + 1] = __float_as_uint(p1);
+          }
+          tmem_st_32x32b_x32(t_s + q4 * 32, pr);
+        }
+      } else {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pr[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2_approx(fmaf(s[h2 * 64 + 2 * c], sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(s[h2 * 64 + 2 * c + 1], sl2, neg_m));
+            sum0 += p0;
+            sum1 += p1;
+            pr[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_32x32b_x32(t_s + h2 * 32, pr);
+        }
+      }
+      l = l * alpha + (sum0 + sum1);
+      if constexpr (C::kTf32) {
+        // V_j (load 2j+1 of the ring) -> V^T in K-major 128-byte-swizzled boxes
+        const int cv = 2 * j + 1;
+        const int vslot = cv % C::kStages;
+        bool vok = mbar_wait(bar_kv_full(vslot), (cv / C::kStages) & 1, abort_flag, deadline);
+        vok = __all_sync(0xffffffffu, vok);
+        if (!vok) { ok = false; break; }
+        const uint32_t sv = s_kv + vslot * C::kTileBytes;
+        const uint32_t svt = s_q[1];
+        const int key = row;                          // this thread moves key row `key`
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 4) {
+          float4 x;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                       : "r"(swz128(sv + (c0 / 32) * kBoxBytes, key, (c0 % 32) / 4)) : "memory");
+          const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c0 + e;
+            const uint32_t dst = swz128(svt + (key / 32) * (D * 128), c, (key % 32) / 4) + (key % 4) * 4;
+            asm volatile("st.shared.f32 [%0], %1;" :: "r"(dst), "f"(xv[e]) : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      // O <- alpha O before the next P V accumulates. The previous P V of this
+      // tile has completed: it was issued before the S MMA whose completion we
+      // just waited for, and the tensor core completes them in order.
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + c0, o);
+          tmem_wait_ld();
+          reg_fence_x32(o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st_32x32b_x32(t_o + c0, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p_ready(g));
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) {
+      ok = mbar_wait(bar_o_final(g), 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const uint32_t stage = s_q[g];     // Q tile no longer needed: all its MMAs completed
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(t_o + c0, o);
+        tmem_wait_ld();
+        reg_fence_x32(o);
+        if constexpr (C::kTf32) {
+          const uint32_t box = stage + (c0 / 32) * kBoxBytes;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 v = make_float4(__uint_as_float(o[4 * u]) * inv_l, __uint_as_float(o[4 * u + 1]) * inv_l,
+                                         __uint_as_float(o[4 * u + 2]) * inv_l, __uint_as_float(o[4 * u + 3]) * inv_l);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, row, u)),
+                         "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+          }
+        } else {
+          const uint32_t box = stage + (c0 / 64) * kBoxBytes;
+          const int u0 = (c0 % 64) / 8;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[8 * u + 2 * e]) * inv_l, __uint_as_float(o[8 * u + 2 * e + 1]) * inv_l);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, row, u0 + u)),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + g, 128);
+      if (warp == 2 + 4 * g && lane == 0) {
+        for (int bx = 0; bx < C::kNBox; ++bx)
+          tma_store_3d(&map_o, stage + bx * kBoxBytes, bx * C::kChunk, qt[g] * kBM, bh);
+        tma_store_commit();
+        tma_store_wait_all0();
+      }
+      if (q_row < p.N) p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    abort_grace_period();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+template <typename T, int D>
+static cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                          const FwdParams& p, int grid, cudaStream_t stream) {
+  using C = FwdCfg<T, D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fwd_kernel<T, D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mo, FwdParams p, cudaStream_t stream) {
+  const int nq = (p.N + kBM - 1) / kBM;
+  p.num_pairs = (dtype_bytes == 2) ? (nq + 1) / 2 : nq;    // query tiles per CTA: 2 (bf16) or 1 (fp32)
+  const int grid = p.num_pairs * p.BH;
+  if (dtype_bytes == 2 && d == 128) return launch<__nv_bfloat16, 128>(mq, mk, mv, mo, p, grid, stream);
+  if (dtype_bytes == 2 && d == 64) return launch<__nv_bfloat16, 64>(mq, mk, mv, mo, p, grid, stream);
+  if (dtype_bytes == 4 && d == 64) return launch<float, 64>(mq, mk, mv, mo, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,48 @@
+// Host-visible interface between the C ABI (fa_api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct FwdParams {
+  float* lse;                      // [B*Hq*N] natural-log logsumexp
+  unsigned* status;                // device status word
+  int N, Hq, Hkv, BH;              // BH = B*Hq
+  int num_pairs;                   // CTAs per head (set by launch_fwd: 2 query tiles per CTA for bf16, 1 for fp32)
+  int causal;
+  float scale_log2;                // scale * log2(e)
+  unsigned long long timeout_ns;   // bound on every wait inside the kernel
+};
+
+// dtype_bytes: 2 = bf16 (tensor-core kind::f16), 4 = fp32 (kind::tf32).
+cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
+
+struct BwdParams {
+  float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows
+  float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows
+  float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled)
+  unsigned* status;                // device status word
+  int N, NQP;                      // NQP = N rounded up to a multiple of 128
+  int Hq, Hkv, BH, BHkv;           // BH = B*Hq, BHkv = B*Hkv
+  int causal;
+  float scale, scale_log2;
+  unsigned long long timeout_ns;
+};
+struct BwdTensors {
+  const void* o;
+  const void* dO;
+  const float* lse;
+  void* dq;
+};
+struct BwdMaps {
+  CUtensorMap q, k, v, dO, dk, dv;
+};
+
+// Preprocess, dK/dV and dQ-convert launches on `stream`, d in {64, 128}.
+cudaError_t launch_bwd(int d, const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
+                       cudaStream_t stream);
+
+}  // namespace fa

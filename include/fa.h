@@ -1,0 +1,106 @@
+/*
+ * fa.h - exact attention (forward and backward) for NVIDIA GB300 (sm_103).
+ *
+ * Computes O = softmax(scale * Q K^T [+ causal mask]) V by streaming key/value
+ * tiles through shared memory with an online softmax (running row max m and
+ * running row sum l), so the N x N score matrix never reaches device memory.
+ * The forward stores O and the per-row logsumexp; the backward recomputes the
+ * scores from that logsumexp to produce dQ, dK and dV.
+ *
+ * Sources: the definition softmax(Q K^T / sqrt(d_k)) V ("FlashAttention v2相比
+ * 于v1有哪些更新", section 1); tiled online softmax ("FlashAttention技术解析",
+ * sections 2.1-2.2); deferred division by l (blogweb.cn page, section 3);
+ * recompute-from-normaliser backward ("4.3 FlashAttention-2与FlashAttention-3
+ * 演进", FlashAttention-3 section 3); causal block skipping and atomic dQ
+ * accumulation ("Flash Attention V3技术解析", section 2.1).
+ *
+ * Conventions shared by every call
+ *   Layout: dense row-major, no strides. Q, O, dO, dQ are [B, Hq, N, d];
+ *     K, V, dK, dV are [B, Hkv, N, d]; LSE is [B, Hq, N] fp32. Query head h
+ *     reads key/value head h / (Hq / Hkv) (grouped-query attention).
+ *   Causal: key j is visible to query i iff j <= i (one N for queries and keys).
+ *   LSE_i = ln sum_j exp(scale * q_i . k_j) over the visible keys.
+ *   Pointers: device pointers, 16-byte aligned, owned by the caller; the
+ *     library never allocates or frees memory during a call and keeps no
+ *     reference after it returns.
+ *   Sizes: B, Hq, Hkv, N >= 1; Hq % Hkv == 0; d in {64, 128}; scale finite
+ *     and > 0.
+ *   stream: a cudaStream_t (NULL = legacy default stream). Every call is
+ *     asynchronous on it; argument errors are reported synchronously and
+ *     launch nothing.
+ *   Device: the current CUDA device must be compute capability 10.3.
+ *   Errors: FA_ERR_INVALID_ARG for bad pointers or sizes, FA_ERR_UNSUPPORTED
+ *     for a valid but unimplemented combination, FA_ERR_ARCH for a device that
+ *     is not sm_103, FA_ERR_CUDA when a launch fails. Inside the kernels every
+ *     wait is bounded; a wait that runs out sets the device status word,
+ *     which fa_device_status reports as FA_ERR_TIMEOUT.
+ *   Threads: calls may come from several host threads; each call is
+ *     independent.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_ARCH = 3,
+  FA_ERR_CUDA = 4,
+  FA_ERR_TIMEOUT = 5,
+  FA_ERR_WORKSPACE = 6,
+  FA_ERR_DEVICE = 7
+} fa_status;
+
+/* Forward, bf16. q, k, v, o: bf16; lse: fp32 [B, Hq, N].
+ * O_i = sum_j softmax_j(scale q_i . k_j) v_j (fp32 accumulation, bf16 result,
+ * round to nearest even); lse as defined above. Tensor-core bf16 MMA with fp32
+ * accumulation; the probabilities are rounded to bf16 before the P V product. */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/* Forward, fp32 in and out (tf32 tensor-core products, fp32 softmax and
+ * accumulation). Same arguments as fa_fwd with fp32 q, k, v, o; d must be 64
+ * (FA_ERR_UNSUPPORTED otherwise). */
+fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                     int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B, Hq, N]
+ * and the fp32 dQ accumulator [B, Hq, N, d], each 256-byte aligned. Returns 0
+ * for invalid sizes. */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+
+/* Backward, bf16. Inputs q, k, v, o, dO (bf16) and lse (fp32) from fa_fwd with
+ * the same sizes, causal flag and scale. Outputs dq [B, Hq, N, d] and dk, dv
+ * [B, Hkv, N, d] (bf16) are overwritten. workspace: caller-owned device
+ * memory of at least fa_bwd_workspace_bytes(...) bytes, 256-byte aligned
+ * (FA_ERR_WORKSPACE if too small); its contents need not be initialised and
+ * are scratch after the call. dK and dV are deterministic; dQ is accumulated
+ * with fp32 atomics, so its last bits may vary from run to run. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran out; that call's
+ * outputs are invalid), FA_ERR_DEVICE (a kernel found the device's
+ * shared-memory window unusable and did nothing) or FA_ERR_CUDA (the stream
+ * reported an error). */
+fa_status fa_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

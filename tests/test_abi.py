@@ -1,0 +1,62 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every symbol
+include/fa.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_attention_79_gb300 as fa
+    if not os.path.exists(fa.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import exact_attention_79_gb300 as fa
+    names = declared_functions()
+    assert names, "no declarations found"
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in fa.SIGNATURES, n
+
+
+def test_status_strings_and_version(lib):
+    for code in range(8):
+        assert lib.fa_status_string(code)
+    assert lib.fa_version() >= 100
+
+
+def test_workspace_size_formula(lib):
+    # lse2 + D: B*Hq*ceil(N/128)*128 floats each; dQ accumulator: B*Hq*N*d floats
+    assert lib.fa_bwd_workspace_bytes(1, 16, 16, 8192, 128) == 2 * 16 * 8192 * 4 + 16 * 8192 * 128 * 4
+    # B*Hq = 8 rows of ceil(100/128)*128 = 128 padded entries: 4096 B each for lse2 and D
+    assert lib.fa_bwd_workspace_bytes(2, 4, 2, 100, 64) == 4096 + 4096 + 8 * 100 * 64 * 4
+    assert lib.fa_bwd_workspace_bytes(1, 3, 2, 128, 128) == 0      # Hq not a multiple of Hkv
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 96) == 0       # unsupported head dim
+
+
+def test_invalid_arguments_rejected_without_device(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    assert lib.fa_fwd(null, fake, fake, fake, fake, 1, 1, 1, 128, 64, 0, 0.125, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 80, 0, 0.125, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 4, 3, 128, 64, 0, 0.125, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 64, 0, 0.0, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 4), 1, 1, 1, 128, 64, 0, 0.1, null) == 1
+    assert lib.fa_fwd_f32(fake, fake, fake, fake, fake, 1, 1, 1, 128, 128, 0, 0.1, null) == 2
+    args = [fake] * 9
+    assert lib.fa_bwd(*args, null, 1 << 30, 1, 1, 1, 128, 128, 1, 0.1, null) == 6
+    assert lib.fa_bwd(*([null] + [fake] * 8), fake, 1 << 30, 1, 1, 1, 128, 128, 1, 0.1, null) == 1

@@ -1,0 +1,127 @@
+"""Backward parity: the CUDA backward (through the C ABI) against the
+double-precision oracle on the same seeded, rounded inputs.
+
+The GPU backward consumes the GPU forward's O and LSE, as a caller would.
+Bar: relative Frobenius error <= 1e-2 per gradient tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_79_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def rel_fro(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def run_fwd_bwd(fa, t, causal, scale):
+    dev = torch.device("cuda:0")
+    g = {k: v.to(dev) for k, v in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=causal, scale=scale)
+    fa.check_device_status()
+    return [x.float().cpu().numpy() for x in (o, lse, dq, dk, dv)]
+
+
+EDGE = [
+    # B, Hq, Hkv, N, d, causal
+    (1, 1, 1, 1, 128, True),
+    (1, 1, 1, 1, 64, False),
+    (1, 2, 1, 127, 128, True),
+    (1, 2, 2, 128, 128, False),
+    (2, 4, 2, 129, 128, True),
+    (1, 8, 1, 257, 128, True),
+    (1, 2, 2, 300, 64, False),
+    (1, 2, 2, 300, 64, True),
+    (1, 3, 3, 640, 128, False),
+    (1, 2, 1, 1000, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", EDGE)
+def test_bwd_edge_sizes(fa, B, Hq, Hkv, N, d, causal):
+    scale = d ** -0.5
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=100 + N, with_grad=True)
+    o, lse, dq, dk, dv = run_fwd_bwd(fa, t, causal, scale)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    ro, rl, rdq, rdk, rdv = oracle.backward(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    assert np.abs(o - ro).max() <= configs.TOL_O_MAX
+    assert np.abs(lse - rl).max() <= configs.TOL_LSE_MAX
+    errs = {n: rel_fro(g, r) for n, g, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv))}
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+
+
+def test_bwd_n8192_full(fa):
+    """Forward + backward, B=1, H=16, N=8192, d=128, causal: every element."""
+    w = configs.WORKLOADS["bf16_h16_n8192_d128_causal_fwdbwd"]
+    t = inputs.make_workload_inputs(w)
+    o, lse, dq, dk, dv = run_fwd_bwd(fa, t, w.causal, w.scale)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    ro, rl, rdq, rdk, rdv = oracle.backward(f["q"], f["k"], f["v"], f["do"], w.causal, w.scale)
+    e_o = np.abs(o - ro)
+    assert e_o.max() <= configs.TOL_O_MAX and e_o.mean() <= configs.TOL_O_MEAN
+    assert np.abs(lse - rl).max() <= configs.TOL_LSE_MAX
+    errs = {n: rel_fro(g, r) for n, g, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv))}
+    print(w.name, "max|dO|", e_o.max(), errs)
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+
+
+def test_bwd_n65536_sampled_rows(fa):
+    """Long sequence: 256 seeded query rows per head for dQ and 256 seeded key
+    rows per head for dK, dV. The key rows need LSE and D of every query row;
+    the oracle computes those itself (never from the GPU)."""
+    w = configs.WORKLOADS["bf16_h8_n65536_d128_causal_fwdbwd"]
+    t = inputs.make_workload_inputs(w)
+    o, lse, dq, dk, dv = run_fwd_bwd(fa, t, w.causal, w.scale)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    qr = inputs.sample_rows(w.B, w.Hq, w.N, w.sampled_rows, seed=1)
+    kr = inputs.sample_rows(w.B, w.Hkv, w.N, w.sampled_rows, seed=2)
+    rl_all, rD_all = oracle.row_statistics(f["q"], f["k"], f["v"], f["do"], w.causal, w.scale)
+    rdq, rdk, rdv = oracle.backward_rows(f["q"], f["k"], f["v"], f["do"], w.causal, w.scale, qr, kr, rl_all, rD_all)
+    bq = np.arange(w.B)[:, None, None]
+    hq = np.arange(w.Hq)[None, :, None]
+    hk = np.arange(w.Hkv)[None, :, None]
+    assert np.abs(lse - rl_all).max() <= configs.TOL_LSE_MAX
+    errs = {"dq": rel_fro(dq[bq, hq, qr], rdq), "dk": rel_fro(dk[bq, hk, kr], rdk), "dv": rel_fro(dv[bq, hk, kr], rdv)}
+    print(w.name, errs)
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+
+
+def test_bwd_dk_dv_deterministic(fa):
+    B, Hq, Hkv, N, d = 1, 8, 2, 700, 128
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=9, with_grad=True)
+    dev = torch.device("cuda:0")
+    g = {k: v.to(dev) for k, v in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=True)
+    a = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True)
+    b = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True)
+    fa.check_device_status()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    # dQ uses fp32 atomics: equal up to summation order
+    assert (a[0].float() - b[0].float()).abs().max().item() < 1e-2
+
+
+def test_bwd_workspace_checks(fa):
+    import ctypes
+    lib = fa.load()
+    B, Hq, Hkv, N, d = 1, 2, 2, 256, 128
+    need = fa.bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    nqp = 256
+    assert need == 2 * B * Hq * nqp * 4 + B * Hq * N * d * 4
+    assert fa.bwd_workspace_bytes(B, Hq, Hkv, N, 96) == 0
+    dev = torch.device("cuda:0")
+    x = torch.zeros(B, Hq, N, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(B, Hq, N, dtype=torch.float32, device=dev)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    args = [P(x)] * 4 + [P(lse), P(x), P(x), P(x), P(x)]
+    assert lib.fa_bwd(*args, P(ws), need - 256, B, Hq, Hkv, N, d, 1, 0.1, None) == 6
+    assert lib.fa_bwd(*args, ctypes.c_void_p(ws.data_ptr() + 16), need, B, Hq, Hkv, N, d, 1, 0.1, None) == 6
+    assert lib.fa_bwd(*args, P(ws), need, B, Hq, Hkv, N, d, 1, -1.0, None) == 1
+    fa.check_device_status()
