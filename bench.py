@@ -1,0 +1,381 @@
+#!/usr/bin/env python3
+"""Attention throughput on GB300: forward + backward TFLOP/s (bf16, d=128).
+
+One step = one pass of the whole path over one batch: fa_fwd, then the three
+backward phases (fa_bwd_preprocess, fa_bwd_dkdv, fa_bwd_dq), all through the
+C ABI. FLOPs are counted as 4 B Hq N^2 d for the forward (halved when causal)
+and 2.5x that for the backward. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+
+--impl reference times the double-precision CPU oracle on the host cores on
+the same workload and metric, each step a bounded slab of query rows.
+Multi-GPU (torchrun): independent replicas, one per rank; value = all ranks'
+FLOPs over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "bf16_h16_n8192_d128_causal_fwdbwd"
+METRIC = "attention TFLOPS fwd+bwd (bf16, d=128) and % of GB300 dense BF16 peak"
+FALLBACK_PEAK_TFLOPS = 1900.0     # used only when MEASURED_PEAKS.json is absent
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, "fallback 1.9 PFLOP/s (MEASURED_PEAKS.json absent)"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9]
+        rows = inside if len(inside) >= 3 else [r for _, r in self.rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "in_window": len(inside)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_rows_flops(rows, N, d, causal):
+    """Algorithmic fwd+bwd FLOPs of the given query rows: 14 d per visible key."""
+    import numpy as np
+    keys = (np.asarray(rows) + 1) if causal else np.full(len(rows), N)
+    return 14.0 * d * float(keys.sum())
+
+
+def oracle_slab_runner(w, seed=0):
+    """Returns (run(rows) -> flops, description): the oracle's full forward +
+    backward arithmetic for a slab of query rows of head (0, 0)."""
+    import numpy as np
+    import oracle
+    from exact_attention_79_gb300 import inputs
+    t = inputs.make_inputs(1, 1, 1, w.N, w.d, w.dtype, seed=seed, with_grad=True)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+
+    def run(rows):
+        oracle.backward_query_rows(f["q"], f["k"], f["v"], f["do"], w.causal, w.scale, 0, 0, rows)
+        return oracle_rows_flops(rows, w.N, w.d, w.causal)
+    return run, np
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(w, budget_s):
+    """The oracle as it stands, on host cores, over seeded random query rows of
+    one head until the time budget is spent."""
+    run, np = oracle_slab_runner(w)
+    rng = np.random.Generator(np.random.PCG64(7))
+    flops = 0.0
+    nrows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        rows = np.sort(rng.choice(w.N, size=min(128, w.N), replace=False))
+        flops += run(rows)
+        nrows += len(rows)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{nrows} seeded query rows of head 0 (full fwd+bwd arithmetic per row, fp64), {dt:.1f} s"}
+
+
+def reference_arm(args, w):
+    """The oracle timed on the host cores, K steps after W warm-up steps; each
+    step a slab of query rows sized so the whole run takes a few minutes."""
+    run, np = oracle_slab_runner(w)
+    rng = np.random.Generator(np.random.PCG64(11))
+    probe_rows = np.sort(rng.choice(w.N, size=min(64, w.N), replace=False))
+    t0 = time.perf_counter()
+    run(probe_rows)
+    per_row = (time.perf_counter() - t0) / len(probe_rows)
+    budget = 150.0
+    R = int(max(1, min(w.N, budget / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        run(np.sort(rng.choice(w.N, size=R, replace=False)))
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flops += run(np.sort(rng.choice(w.N, size=R, replace=False)))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                   "sample_rows_per_step": R},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{R} seeded query rows of head 0 per step (full fwd+bwd arithmetic, fp64)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ traffic from a committed ncu summary
+def traffic_from_profile(kernel_file, kernel_name, workload):
+    """dram bytes per launch from profiles/<kernel>__<workload>.md, if that
+    summary was taken on the current kernel source (its sha256 matches)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_name}__{workload}.md")
+    src = os.path.join(ROOT, "exact_attention_79_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_launch")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ native arm
+def native_arm(args, w):
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_79_gb300 as fa
+    from exact_attention_79_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = fa.load()
+
+    t = inputs.make_workload_inputs(w, with_grad=True)
+    q, k, v, do = (t[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    dims = (w.B, w.Hq, w.Hkv, w.N, w.d)
+    causal = int(w.causal)
+    scale = float(w.scale)
+
+    def check(name, code):
+        if code != 0:
+            raise RuntimeError(f"{name} failed with status {code}")
+
+    def step(ev):
+        ev[0].record(stream)
+        check("fa_fwd", lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), *dims, causal, scale, sptr))
+        ev[1].record(stream)
+        check("fa_bwd_preprocess", lib.fa_bwd_preprocess(P(o), P(lse), P(do), P(ws), ws_bytes, *dims, sptr))
+        ev[2].record(stream)
+        check("fa_bwd_dkdv", lib.fa_bwd_dkdv(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes, *dims,
+                                             causal, scale, sptr))
+        ev[3].record(stream)
+        check("fa_bwd_dq", lib.fa_bwd_dq(P(dq), P(ws), ws_bytes, *dims, scale, sptr))
+        ev[4].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(new_events())
+    fa.check_device_status(stream.cuda_stream)
+
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if world > 1 or \
+        "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    events = [new_events() for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()             # L2 flush between steps (outside the events)
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    fa.check_device_status(stream.cuda_stream)
+
+    seg = [[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)]
+    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    flops_step = w.flops_fwd + w.flops_bwd
+    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
+    names = ["fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    peak, peak_src = peak_tflops()
+    # dominant kernel of the step and its tensor roofline
+    dom = 0 if mean[0] >= mean[2] else 2
+    dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
+    achieved = dom_flops / (mean[dom] / 1e3) / 1e12
+    traffic = traffic_from_profile("fa_fwd.cu" if dom == 0 else "fa_bwd.cu", names[dom], w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
+                "algorithmic_flops_per_launch": dom_flops}
+
+    # ---- end to end: pinned host inputs -> device, the four calls, results -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        host_in = [x.cpu().pin_memory() for x in (q, k, v, do)]
+        host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse, dq, dk, dv)]
+        dev_in = (q, k, v, do)
+        dev_out = (o, lse, dq, dk, dv)
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+        def e2e_step():
+            for dst, src in zip(dev_in, host_in):
+                dst.copy_(src, non_blocking=True)
+            step(new_events())
+            for dst, src in zip(host_out, dev_out):
+                dst.copy_(src, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        fa.check_device_status(stream.cuda_stream)
+        e2e = {"value": world * flops_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    clocks = sampler.summary(t0, t1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "frac_of_peak": value / world / peak,
+        "fwd_tflops": w.flops_fwd / (mean[0] / 1e3) / 1e12,
+        "fwd_frac_of_peak": w.flops_fwd / (mean[0] / 1e3) / 1e12 / peak,
+        "bwd_tflops": w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
+        "kernel_ms": dict(zip(names, mean)),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": t1 - t0,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from exact_attention_79_gb300 import configs
+    w = configs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        reference_arm(args, w)
+        return
+    native_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -152,6 +152,35 @@ BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
   return w;
 }
 
+// Validates sizes and workspace, resolves the device, fills BwdParams.
+fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms) {
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
+  if (st != FA_OK) return st;
+  const BwdWorkspace w = bwd_workspace(B, Hq, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  st = device_state(&status, num_sms);
+  if (st != FA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
+  p->ws_d = reinterpret_cast<float*>(ws + w.off_d);
+  p->ws_dq = reinterpret_cast<float*>(ws + w.off_dq);
+  p->status = status;
+  p->N = N;
+  p->NQP = ((N + 127) / 128) * 128;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->BH = B * Hq;
+  p->BHkv = B * Hkv;
+  p->causal = causal ? 1 : 0;
+  p->scale = scale;
+  p->scale_log2 = scale * 1.4426950408889634f;
+  p->timeout_ns = wait_limit_ns();
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -161,47 +190,59 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
   return bwd_workspace(B, Hq, N, d).total;
 }
 
+fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
+                            size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, void* stream) {
+  if (!o || !lse || !dO || !aligned16(o) || !aligned16(lse) || !aligned16(dO)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, 1.0f, workspace, workspace_bytes, &p, &num_sms);
+  if (st != FA_OK) return st;
+  const cudaError_t e = fa::launch_bwd_pre(d, o, dO, lse, p, num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
+                      float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, dO, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms);
+  if (st != FA_OK) return st;
+  fa::BwdMaps m;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv))
+    return FA_ERR_CUDA;
+  const cudaError_t e = fa::launch_bwd_dkdv(d, m, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+                    float scale, void* stream) {
+  if (!dq || !aligned16(dq)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, scale, workspace, workspace_bytes, &p, &num_sms);
+  if (st != FA_OK) return st;
+  const cudaError_t e = fa::launch_bwd_dq(d, dq, p, num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                  int N, int d, int causal, float scale, void* stream) {
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
+  fa_status st = fa_bwd_preprocess(o, lse, dO, workspace, workspace_bytes, B, Hq, Hkv, N, d, stream);
   if (st != FA_OK) return st;
-  const BwdWorkspace w = bwd_workspace(B, Hq, N, d);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
-    return FA_ERR_WORKSPACE;
-  unsigned* status = nullptr;
-  int num_sms = 0;
-  st = device_state(&status, &num_sms);
+  st = fa_bwd_dkdv(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale, stream);
   if (st != FA_OK) return st;
-  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-  fa::BwdMaps m;
-  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
-      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv))
-    return FA_ERR_CUDA;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  fa::BwdParams p{};
-  p.ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
-  p.ws_d = reinterpret_cast<float*>(ws + w.off_d);
-  p.ws_dq = reinterpret_cast<float*>(ws + w.off_dq);
-  p.status = status;
-  p.N = N;
-  p.NQP = ((N + 127) / 128) * 128;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.BH = static_cast<int>(BHq);
-  p.BHkv = static_cast<int>(BHkv);
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = wait_limit_ns();
-  fa::BwdTensors t{o, dO, lse, dq};
-  const cudaError_t e = fa::launch_bwd(d, t, m, p, num_sms, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return fa_bwd_dq(dq, workspace, workspace_bytes, B, Hq, Hkv, N, d, scale, stream);
 }
-
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                  int d, int causal, float scale, void* stream) {

@@ -431,8 +431,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
 // ------------------------------------------------------------------ launch
 template <int D>
-static cudaError_t launch_bwd_d(const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
-                                cudaStream_t stream) {
+static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static bool configured = false;
   if (!configured) {
@@ -440,24 +439,33 @@ static cudaError_t launch_bwd_d(const BwdTensors& t, const BwdMaps& m, const Bwd
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int small_grid = num_sms * 4;
-  bwd_pre_kernel<D><<<small_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(t.o),
-                                                    static_cast<const __nv_bfloat16*>(t.dO), t.lse, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int grid = (p.NQP / kBN) * p.BHkv;
   bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  bwd_dq_kernel<D><<<small_grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(t.dq), p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(int d, const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
-                       cudaStream_t stream) {
-  if (d == 128) return launch_bwd_d<128>(t, m, p, num_sms, stream);
-  if (d == 64) return launch_bwd_d<64>(t, m, p, num_sms, stream);
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* lse, const BwdParams& p, int num_sms,
+                           cudaStream_t stream) {
+  const auto* o16 = static_cast<const __nv_bfloat16*>(o);
+  const auto* do16 = static_cast<const __nv_bfloat16*>(dO);
+  if (d == 128) bwd_pre_kernel<128><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p);
+  else if (d == 64) bwd_pre_kernel<64><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_dkdv_d<128>(m, p, stream);
+  if (d == 64) return launch_dkdv_d<64>(m, p, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream) {
+  auto* dq16 = static_cast<__nv_bfloat16*>(dq);
+  if (d == 128) bwd_dq_kernel<128><<<num_sms * 4, 256, 0, stream>>>(dq16, p);
+  else if (d == 64) bwd_dq_kernel<64><<<num_sms * 4, 256, 0, stream>>>(dq16, p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -36,18 +36,22 @@ struct FwdCfg {
   static constexpr int kNBox = D / kChunk;            // TMA boxes per 128-row tile
   static constexpr int kTileBytes = kNBox * kBoxBytes;
   static constexpr int kUmmaK = 32 / kElt;            // K per MMA instruction (32 bytes)
-  static constexpr int kStages = (kTileBytes == 16384) ? 8 : 4;   // K/V slot ring
+  static constexpr int kStages = kTf32 ? 2 : ((kTileBytes == 16384) ? 8 : 4);   // K/V slot ring
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }
   static __device__ __forceinline__ uint32_t col_o(int i) { return 256u + D * i; }
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + kBarBytes + 1024;
+  // fp32 extra buffers: the low tf32 parts of Q and of the current K tile
+  static constexpr int kSmemBytes = (2 + kStages + (kTf32 ? 2 : 0)) * kTileBytes + kBarBytes + 1024;
   static constexpr uint32_t kFmt = kTf32 ? 2u : 1u;
   // tf32 operands must be K-major, so V (d contiguous) cannot feed the P V
   // product directly: the fp32 variant runs one query tile per CTA and its
   // softmax group transposes each V tile into a K-major V^T buffer (the idle
-  // second query-tile slot). bf16 runs two ping-ponged query tiles per CTA.
+  // second query-tile slot). To keep the logits (and so the logsumexp) at
+  // fp32 accuracy, Q and K are split into tf32 high and low parts and
+  // S = Qhi Khi + Qhi Klo + Qlo Khi. bf16 runs two ping-ponged query tiles
+  // per CTA.
   static constexpr bool kPingPong = !kTf32;
   static constexpr int kTilesPerCta = kPingPong ? 2 : 1;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -55,7 +59,8 @@ struct FwdCfg {
 };
 
 template <typename T, int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc,
+                                         uint32_t sq_lo = 0, uint32_t sk_lo = 0) {
   using C = FwdCfg<T, D>;
 #pragma unroll
   for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
@@ -63,8 +68,38 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
     const uint32_t off = (kb / 128) * kBoxBytes + (kb % 128);
     const uint64_t a = smem_desc_sw128(sq + off, 16, 1024);
     const uint64_t b = smem_desc_sw128(sk + off, 16, 1024);
-    if constexpr (C::kTf32) mma_tf32_ss(d_tmem, a, b, idesc, kk > 0);
-    else mma_bf16_ss(d_tmem, a, b, idesc, kk > 0);
+    if constexpr (C::kTf32) {
+      mma_tf32_ss(d_tmem, a, b, idesc, kk > 0);
+      mma_tf32_ss(d_tmem, a, smem_desc_sw128(sk_lo + off, 16, 1024), idesc, 1);
+      mma_tf32_ss(d_tmem, smem_desc_sw128(sq_lo + off, 16, 1024), b, idesc, 1);
+    } else {
+      mma_bf16_ss(d_tmem, a, b, idesc, kk > 0);
+    }
+  }
+}
+
+// fp32 variant: row `r` of a [128, D] fp32 tile (128-byte swizzled boxes) is
+// replaced by its tf32 rounding (nearest, ties away) and the remainder is
+// written at the same position of `lo`.
+template <int D>
+__device__ __forceinline__ void split_tf32_row(uint32_t tile, uint32_t lo, int r) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 4) {
+    const uint32_t off = swz128((c0 / 32) * kBoxBytes, r, (c0 % 32) / 4);
+    float x[4];
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3])
+                 : "r"(tile + off) : "memory");
+    uint32_t hi[4];
+    float rem[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi[e]) : "f"(x[e]));
+      rem[e] = x[e] - __uint_as_float(hi[e]);
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(tile + off), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                 "r"(hi[3]) : "memory");
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(lo + off), "f"(rem[0]), "f"(rem[1]), "f"(rem[2]),
+                 "f"(rem[3]) : "memory");
   }
 }
 
@@ -102,16 +137,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
   const uint32_t s_q[2] = {base, base + C::kTileBytes};
   const uint32_t s_kv = base + 2 * C::kTileBytes;
-  const uint32_t bars = s_kv + C::kStages * C::kTileBytes;
+  // fp32 only: low tf32 parts of Q and of the K tile being used (after the ring)
+  const uint32_t s_q_lo = s_kv + C::kStages * C::kTileBytes;
+  const uint32_t s_k_lo = s_q_lo + C::kTileBytes;
+  const uint32_t bars = s_kv + (C::kStages + (C::kTf32 ? 2 : 0)) * C::kTileBytes;
   auto bar_q_full = [&](int i) { return bars + 8u * i; };                       // 2
   auto bar_kv_full = [&](int s) { return bars + 16u + 8u * s; };               // kStages
   auto bar_kv_empty = [&](int s) { return bars + 16u + 8u * (C::kStages + s); };
   auto bar_s_full = [&](int i) { return bars + 16u + 16u * C::kStages + 8u * i; };
   auto bar_p_ready = [&](int i) { return bars + 32u + 16u * C::kStages + 8u * i; };
   auto bar_o_final = [&](int i) { return bars + 48u + 16u * C::kStages + 8u * i; };
+  const uint32_t bar_qk_ready = bars + 64u + 16u * C::kStages;          // fp32: Q and K_0 split
   uint8_t* const gbars = gbase + (bars - base);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 64 + 16 * C::kStages);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 68 + 16 * C::kStages);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 72 + 16 * C::kStages);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 76 + 16 * C::kStages);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -141,6 +180,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
+    mbar_init(bar_qk_ready, 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -197,11 +237,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       uint32_t sk = 0;
       int kslot = 0;
       if (ok) ok = take(sk, kslot);
+      if (ok && C::kTf32) ok = mbar_wait(bar_qk_ready, 0, abort_flag, deadline);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < 2; ++i) {
           if (nkv[i] == 0) continue;
-          issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk, idesc_qk);
+          issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk, idesc_qk, s_q_lo, s_k_lo);
           mma_commit(bar_s_full(i));
         }
         mma_commit(bar_kv_empty(kslot));
@@ -219,7 +260,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           tc_fence_after();
           issue_pv<T, D>(tbase + C::col_o(i), tbase + C::col_s(i), C::kTf32 ? s_vt : sv, idesc_pv, j > 0);
           if (j + 1 < nkv[i]) {
-            issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk_next, idesc_qk);
+            issue_qk<T, D>(tbase + C::col_s(i), s_q[i], sk_next, idesc_qk, s_q_lo, s_k_lo);
             mma_commit(bar_s_full(i));
           } else {
             mma_commit(bar_o_final(i));
@@ -245,6 +286,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     float m = -INFINITY;                           // running max, log2 units of scale*s
     float l = 0.f;                                 // running sum relative to m
     bool ok = n_kv > 0;
+    if constexpr (C::kTf32) {
+      if (ok) {
+        // split this thread's Q row and K_0 row (load 0 of the ring) into tf32 high + low parts
+        bool w = mbar_wait(bar_q_full(0), 0, abort_flag, deadline) &&
+                 mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
+        ok = __all_sync(0xffffffffu, w);
+        if (ok) {
+          split_tf32_row<D>(s_q[0], s_q_lo, row);
+          split_tf32_row<D>(s_kv, s_k_lo, row);
+          fence_proxy_async_smem();
+          mbar_arrive(bar_qk_ready);
+        }
+      }
+    }
     for (int j = 0; j < n_kv && ok; ++j) {
       ok = mbar_wait(bar_s_full(g), j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
@@ -337,6 +392,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const uint32_t dst = swz128(svt + (key / 32) * (D * 128), c, (key % 32) / 4) + (key % 4) * 4;
             asm volatile("st.shared.f32 [%0], %1;" :: "r"(dst), "f"(xv[e]) : "memory");
           }
+        }
+        if (j + 1 < n_kv) {
+          // K_{j+1} (load 2j+2): split before the tensor core computes S_{j+1}. The
+          // previous S, which read the low-part buffer, has completed.
+          const int ck = 2 * j + 2;
+          const int kslot = ck % C::kStages;
+          bool kok = mbar_wait(bar_kv_full(kslot), (ck / C::kStages) & 1, abort_flag, deadline);
+          kok = __all_sync(0xffffffffu, kok);
+          if (!kok) { ok = false; break; }
+          split_tf32_row<D>(s_kv + kslot * C::kTileBytes, s_k_lo, row);
         }
         fence_proxy_async_smem();
       }

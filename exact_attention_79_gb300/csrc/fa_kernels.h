@@ -31,18 +31,14 @@ struct BwdParams {
   float scale, scale_log2;
   unsigned long long timeout_ns;
 };
-struct BwdTensors {
-  const void* o;
-  const void* dO;
-  const float* lse;
-  void* dq;
-};
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;
 };
 
-// Preprocess, dK/dV and dQ-convert launches on `stream`, d in {64, 128}.
-cudaError_t launch_bwd(int d, const BwdTensors& t, const BwdMaps& m, const BwdParams& p, int num_sms,
-                       cudaStream_t stream);
+// The three backward phases, each one launch on `stream`, d in {64, 128}.
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* lse, const BwdParams& p, int num_sms,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream);
 
 }  // namespace fa

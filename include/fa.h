@@ -70,9 +70,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                      int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
-/* Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B, Hq, N]
- * and the fp32 dQ accumulator [B, Hq, N, d], each 256-byte aligned. Returns 0
- * for invalid sizes. */
+/* Bytes of device workspace fa_bwd needs: fp32 LSE * log2(e) and fp32
+ * D = rowsum(dO * O), each [B, Hq, ceil(N/128)*128], and the fp32 dQ
+ * accumulator [B, Hq, N, d], each part 256-byte aligned. Returns 0 for invalid
+ * sizes. */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 
 /* Backward, bf16. Inputs q, k, v, o, dO (bf16) and lse (fp32) from fa_fwd with
@@ -85,6 +86,22 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/* The three phases fa_bwd runs, in this order on one stream, exposed for
+ * callers that schedule or time them separately. Arguments mean what they
+ * mean for fa_bwd; the workspace carries state from one phase to the next.
+ *   fa_bwd_preprocess: D_i = sum_c dO_ic O_ic and LSE_i log2(e) into the
+ *     workspace, and the dQ accumulator zeroed.
+ *   fa_bwd_dkdv: dK and dV (written to dk, dv) and the unscaled fp32 dQ
+ *     accumulator (in the workspace); the tensor-core phase.
+ *   fa_bwd_dq: dq = scale * accumulator, rounded to bf16. */
+fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
+                            size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, void* stream);
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+                      int causal, float scale, void* stream);
+fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+                    float scale, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran out; that call's

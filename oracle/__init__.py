@@ -31,5 +31,6 @@ from .attention import (  # noqa: F401
     forward_rows,
     row_statistics,
     backward_rows,
+    backward_query_rows,
     tiled_forward,
 )

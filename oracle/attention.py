@@ -204,6 +204,29 @@ def backward_rows(q, k, v, do, causal, scale, q_rows, k_rows, lse, D):
     return dq, dk, dv
 
 
+def backward_query_rows(q, k, v, do, causal, scale, b, h, rows):
+    """Everything the given query rows of head (b, h) contribute, in double:
+    their O, LSE, D and dQ rows, and their additive share of dK and dV of the
+    KV head they read. Summing the shares over a partition of the rows gives
+    `backward`'s dK and dV; each row is computed whole (same formulas as
+    `backward`). Used to time the oracle on a bounded slice of a workload.
+    Returns (o [R,d], lse [R], D [R], dq [R,d], dk_part [N,d], dv_part [N,d]).
+    """
+    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    hk = h // G
+    rows = np.asarray(rows)
+    s = _scores(q[b, h, rows], k[b, hk], scale, causal, rows)
+    p, lse = _softmax_rows(s)
+    o = p @ v[b, hk]
+    D = (do[b, h, rows] * o).sum(axis=1)
+    dp = do[b, h, rows] @ v[b, hk].T
+    ds = p * (dp - D[:, None])
+    dq = scale * (ds @ k[b, hk])
+    dk_part = scale * (ds.T @ q[b, h, rows])
+    dv_part = p.T @ do[b, h, rows]
+    return o, lse, D, dq, dk_part, dv_part
+
+
 def tiled_forward(q, k, v, causal, scale, block=64, deferred=True):
     """The pages' tiled algorithm with online softmax, in double.
 
@@ -261,5 +284,5 @@ def tiled_forward(q, k, v, causal, scale, block=64, deferred=True):
 
 __all__ = [
     "forward", "backward", "forward_rows", "row_statistics", "backward_rows",
-    "tiled_forward",
+    "backward_query_rows", "tiled_forward",
 ]

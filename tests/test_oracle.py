@@ -297,6 +297,26 @@ def test_row_modes_equal_full_computation(causal):
         np.testing.assert_allclose(dv_r[0, g], dv[0, g, kr[0, g]], atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_query_row_slabs_sum_to_full_backward(causal):
+    B, Hq, Hkv, N, d = 1, 4, 2, 50, 8
+    q, k, v, do = rand_qkv(B, Hq, Hkv, N, d, seed=44, with_do=True)
+    o, lse, dq, dk, dv = oracle.backward(q, k, v, do, causal, 0.3)
+    dk_sum = np.zeros_like(dk)
+    dv_sum = np.zeros_like(dv)
+    for h in range(Hq):
+        for rows in (np.arange(0, 17), np.arange(17, 40), np.arange(40, 50)):
+            o_r, l_r, D_r, dq_r, dk_p, dv_p = oracle.backward_query_rows(q, k, v, do, causal, 0.3, 0, h, rows)
+            np.testing.assert_allclose(o_r, o[0, h, rows], atol=1e-13)
+            np.testing.assert_allclose(l_r, lse[0, h, rows], atol=1e-13)
+            np.testing.assert_allclose(D_r, (do[0, h, rows] * o[0, h, rows]).sum(-1), atol=1e-13)
+            np.testing.assert_allclose(dq_r, dq[0, h, rows], atol=1e-12)
+            dk_sum[0, h // 2] += dk_p
+            dv_sum[0, h // 2] += dv_p
+    np.testing.assert_allclose(dk_sum, dk, atol=1e-12)
+    np.testing.assert_allclose(dv_sum, dv, atol=1e-12)
+
+
 # ---------------------------------------------------------------- the pages' tiled algorithm
 
 @pytest.mark.parametrize("deferred", [False, True])
