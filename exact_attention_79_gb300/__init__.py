@@ -29,6 +29,7 @@ SIGNATURES = {
     "fa_bwd_preprocess": (_I, [_VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _VP]),
     "fa_bwd_dkdv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_dq": (_I, [_VP, _VP, _SZ, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_bwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_device_status": (_I, [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),

@@ -103,6 +103,24 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
 fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
                     float scale, void* stream);
 
+/* Backward without a caller-provided workspace, for callers that cannot
+ * allocate device memory when they call it (a plugin that only receives
+ * fixed buffers from its host framework, a component that does not own the
+ * device memory pool, a loop that cannot afford cudaMalloc's implicit device
+ * synchronisation). The pages have no counterpart: this is a convenience of
+ * this library. Arguments and results are those of fa_bwd minus the
+ * workspace, which lives instead in a 32 MiB array of device memory owned by
+ * the library (held on every device that loads it until the process exits).
+ * Returns FA_ERR_WORKSPACE, launching nothing, when the problem needs more
+ * than 32 MiB of scratch (fa_bwd_workspace_bytes > 33554432). The first call
+ * on a device looks up the array's device address; make that first call
+ * before any stream capture. Allocates nothing. All calls share the one
+ * array: calls whose work overlaps on the GPU (other streams, other host
+ * threads on the same device) race and corrupt each other's results. */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                         int causal, float scale, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran out; that call's
  * outputs are invalid), FA_ERR_DEVICE (a kernel found the device's
