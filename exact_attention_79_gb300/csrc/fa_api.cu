@@ -214,7 +214,8 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   fa::BwdMaps m;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
   if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
-      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv))
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv) ||
+      !make_map(&m.dqacc, p.ws_dq, 4, d, N, BHq))
     return FA_ERR_CUDA;
   const cudaError_t e = fa::launch_bwd_dkdv(d, m, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

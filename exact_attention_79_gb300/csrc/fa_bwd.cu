@@ -20,7 +20,7 @@
 //                        P^T  = 2^(S^T s log2e - LSE_i log2e)   (registers -> TMEM, bf16)
 //                        dS^T = P^T (dP^T - D_i)   (registers -> shared memory, bf16)
 //                        dV  += P^T dO_i,  dK += dS^T Q_i      (TMEM accumulators)
-//                        dQ_i = dS K               (TMEM, then fp32 atomics into dQacc)
+//                        dQ_i = dS K               (TMEM -> shared -> TMA reduce-add into dQacc)
 //                      and finally dK *= scale; dK, dV stored once (deterministic).
 //  3. bwd_dq_kernel    dQ = scale * dQacc -> bf16.
 #include "fa_common.cuh"
@@ -124,17 +124,17 @@ struct BwdCfg {
   static constexpr int kSmemAlloc = 232448;            // the per-block maximum; the base is aligned inside it
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;     // producer, MMA, 8 softmax-gradient warps, dQ reducer
   static_assert(kLayoutBytes <= kSmemAlloc, "shared memory budget");
   static_assert(2 * D + 256 <= 512, "TMEM budget");
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap map_dqacc, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -155,10 +155,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t bar_kv_full = bars;
   auto bar_q_full = [&](int st) { return bars + 8u + 8u * st; };
   auto bar_q_empty = [&](int st) { return bars + 24u + 8u * st; };
-  const uint32_t bar_s_full = bars + 40, bar_p_ready = bars + 48, bar_dq_full = bars + 56;
-  const uint32_t bar_dq_free = bars + 64, bar_o_final = bars + 72;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 80);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 84);
+  auto bar_dq_staged = [&](int st) { return bars + 40u + 8u * st; };
+  const uint32_t bar_s_full = bars + 56, bar_dp_full = bars + 64, bar_p_ready = bars + 72;
+  const uint32_t bar_ds_ready = bars + 80, bar_dq_full = bars + 88, bar_dq_free = bars + 96;
+  const uint32_t bar_o_final = bars + 104;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 112);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 116);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -180,9 +182,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int st = 0; st < 2; ++st) {
       mbar_init(bar_q_full(st), 1);
       mbar_init(bar_q_empty(st), 1);
+      mbar_init(bar_dq_staged(st), 256);
     }
     mbar_init(bar_s_full, 1);
+    mbar_init(bar_dp_full, 1);
     mbar_init(bar_p_ready, 256);
+    mbar_init(bar_ds_ready, 256);
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 256);
     mbar_init(bar_o_final, 1);
@@ -227,6 +232,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issuer
+    // Per query tile: S^T, [dQ of the previous tile drained] dP^T, [P^T ready]
+    // dV, [dS^T ready] dK, dQ. dQ goes into the dP^T columns, so the next S^T
+    // never waits for a drain; the tensor core runs the in-order MMAs of one
+    // thread in issue order, which keeps every TMEM reuse below safe.
     if (lane == 0) {
       const uint32_t id_kk = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       const uint32_t id_kmn = make_idesc(1, 128, D, 0, 1);   // dV, dK: A K-major (or TMEM), B MN-major
@@ -235,22 +244,23 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       for (int step = 0; step < nsteps && ok; ++step) {
         const int st = step & 1;
         if (!mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
-        if (step > 0 && !mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (K = d)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {                // S^T = K Q^T
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
           mma_bf16_ss(tbase + C::kColS, smem_desc_sw128(s_k + off, 16, 1024),
                       smem_desc_sw128(s_q(st) + off, 16, 1024), id_kk, kk > 0);
         }
+        mma_commit(bar_s_full);
+        if (step > 0 && !mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {                // dP^T = V dO^T
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
           mma_bf16_ss(tbase + C::kColDP, smem_desc_sw128(s_v + off, 16, 1024),
                       smem_desc_sw128(s_do(st) + off, 16, 1024), id_kk, kk > 0);
         }
-        mma_commit(bar_s_full);
+        mma_commit(bar_dp_full);
         if (!mbar_wait(bar_p_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
         // dV += P^T dO  (K = 128 queries; P^T of query q sits in S column 64*(q/64) + (q%64)/2)
@@ -260,6 +270,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_bf16_ts(tbase + C::kColDV, a, smem_desc_sw128(s_do(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn,
                       step > 0 || kk > 0);
         }
+        if (!mbar_wait(bar_ds_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
+        tc_fence_after();
         // dK += dS^T Q  (A = dS^T K-major over queries)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -267,16 +279,36 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_bf16_ss(tbase + C::kColDK, smem_desc_sw128(s_ds + off, 16, 1024),
                       smem_desc_sw128(s_q(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn, step > 0 || kk > 0);
         }
-        // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys)
+        // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys), into the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_bf16_ss(tbase + C::kColS, smem_desc_sw128(s_ds + kk * 16 * 128, kBoxBytes, 1024),
+          mma_bf16_ss(tbase + C::kColDP, smem_desc_sw128(s_ds + kk * 16 * 128, kBoxBytes, 1024),
                       smem_desc_sw128(s_k + kk * 16 * 128, kBoxBytes, 1024), id_mnmn, kk > 0);
         }
         mma_commit(bar_dq_full);
-        mma_commit(bar_q_empty(st));
       }
       if (ok) mma_commit(bar_o_final);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dQ reducer
+    // Adds each staged fp32 dQ tile into the global accumulator with TMA
+    // bulk reductions, then hands the stage buffer back to the producer.
+    if (lane == 0) {
+      for (int step = 0; step < nsteps; ++step) {
+        const int st = step & 1;
+        if (!mbar_wait(bar_dq_staged(st), (step >> 1) & 1, abort_flag, deadline)) break;
+        const int h = hk * G + step / tiles_per_head;
+        const int it = it0 + step % tiles_per_head;
+        const int bh = b * p.Hq + h;
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&map_dqacc, s_q(st) + bx * kBoxBytes, bx * 32, it * kBM, bh);
+        tma_store_commit();
+        tma_store_wait_read0();
+        mbar_arrive(bar_q_empty(st));
+      }
+      tma_store_wait_all0();
     }
     __syncwarp();
   } else {
@@ -290,7 +322,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     bool ok = true;
     for (int step = 0; step < nsteps && ok; ++step) {
       const int st = step & 1;
-      const int h = hk * G + step / tiles_per_head;
       const int it = it0 + step % tiles_per_head;
       const bool diag = p.causal && it == jt;
       ok = mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline) &&
@@ -300,39 +331,60 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(gbase + (s_lse(st) - base));
       const float* dvec = reinterpret_cast<const float*>(gbase + (s_dvec(st) - base));
+      // ---- phase A: P^T = 2^(S^T s log2e - LSE log2e), written over S^T as bf16 pairs
+      float pf[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * g + 32 * ch;            // first query column of this chunk
-        uint32_t sv[32], dp[32];
+        uint32_t sv[32];
         tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + c0, sv);
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + c0, dp);
         tmem_wait_ld();
         reg_fence_x32(sv);
-        reg_fence_x32(dp);
-        uint32_t pp[16], dd[16];
         const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
-        const float4* d4 = reinterpret_cast<const float4*>(dvec + c0);
+        uint32_t pp[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-          const float4 lv = l4[c / 4], dv4 = d4[c / 4];
+          const float4 lv = l4[c / 4];
           const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-          const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-          float pr[4], ds[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int q = c0 + c + e;
             float pv = ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, -lq[e]));
-            if (key_pad || (diag && q < r)) pv = 0.f;
-            pr[e] = pv;
-            ds[e] = pv * (__uint_as_float(dp[c + e]) - dq4[e]);
+            if (key_pad || (diag && c0 + c + e < r)) pv = 0.f;
+            pf[32 * ch + c + e] = pv;
           }
-          pp[c / 2] = pack_bf16x2(pr[0], pr[1]);
-          pp[c / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
-          dd[c / 2] = pack_bf16x2(ds[0], ds[1]);
-          dd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          pp[c / 2] = pack_bf16x2(pf[32 * ch + c], pf[32 * ch + c + 1]);
+          pp[c / 2 + 1] = pack_bf16x2(pf[32 * ch + c + 2], pf[32 * ch + c + 3]);
         }
         // P^T (bf16 pairs) into TMEM over the S^T columns this group already read
         tmem_st_32x32b_x16(tbase + lane_off + C::kColS + 64 * g + 16 * ch, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p_ready);
+      // ---- phase B: dS^T = P^T (dP^T - D) into shared memory (bf16)
+      ok = mbar_wait(bar_dp_full, step & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * g + 32 * ch;
+        uint32_t dp[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + c0, dp);
+        tmem_wait_ld();
+        reg_fence_x32(dp);
+        const float4* d4 = reinterpret_cast<const float4*>(dvec + c0);
+        uint32_t dd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 dv4 = d4[c / 4];
+          const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ds[e] = pf[32 * ch + c + e] * (__uint_as_float(dp[c + e]) - dq4[e]);
+          dd[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          dd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
         // dS^T row r, query columns [c0, c0 + 32): four 16-byte units of box g
         const uint32_t box = s_ds + g * kBoxBytes;
 #pragma unroll
@@ -340,12 +392,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, 4 * ch + u)),
                        "r"(dd[4 * u]), "r"(dd[4 * u + 1]), "r"(dd[4 * u + 2]), "r"(dd[4 * u + 3]) : "memory");
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p_ready);
+      mbar_arrive(bar_ds_ready);
 
-      // ---- dQ_i drain: TMEM lane = query row r of tile `it`; this group takes columns [g D/2, (g+1) D/2)
+      // ---- dQ_i: TMEM (lane = query row r of tile `it`, this group's D/2
+      // columns) -> registers -> the stage buffer of this step, which dV and
+      // dK (its only readers) have finished with -> TMA reduce-add (reducer warp)
       ok = mbar_wait(bar_dq_full, step & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -354,7 +407,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t t[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + g * (D / 2) + c0, t);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + g * (D / 2) + c0, t);
         tmem_wait_ld();
         reg_fence_x32(t);
 #pragma unroll
@@ -362,15 +415,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(bar_dq_free);
-      const int qrow = it * kBM + r;
-      if (qrow < p.N) {
-        float4* dst = reinterpret_cast<float4*>(
-            p.ws_dq + ((static_cast<size_t>(b) * p.Hq + h) * p.N + qrow) * D + g * (D / 2));
+      // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle, box index = column / 32
 #pragma unroll
-        for (int u = 0; u < D / 8; ++u)
-          atomicAdd(dst + u, make_float4(__uint_as_float(dq[4 * u]), __uint_as_float(dq[4 * u + 1]),
-                                         __uint_as_float(dq[4 * u + 2]), __uint_as_float(dq[4 * u + 3])));
+      for (int u = 0; u < D / 8; ++u) {
+        const int col = g * (D / 2) + 4 * u;
+        const uint32_t dst = swz128(s_q(st) + (col / 32) * kBoxBytes, r, (col % 32) / 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(dst), "r"(dq[4 * u]), "r"(dq[4 * u + 1]),
+                     "r"(dq[4 * u + 2]), "r"(dq[4 * u + 3]) : "memory");
       }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_dq_staged(st));
     }
     // ---------------------------------------------------------- dK, dV epilogue
     if (ok) {
@@ -379,8 +433,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
     if (ok) {
       tc_fence_after();
-      // staging: stage 0's Q buffer for dV, its dO buffer for dK (both idle now)
-      const uint32_t stg_v = s_q(0), stg_k = s_do(0);
+      // staging: the V buffer for dV and the K buffer for dK (every MMA has completed)
+      const uint32_t stg_v = s_v, stg_k = s_k;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float mul = which ? p.scale : 1.0f;
@@ -440,7 +494,7 @@ static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStrea
     configured = true;
   }
   const int grid = (p.NQP / kBN) * p.BHkv;
-  bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, p);
+  bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, m.dqacc, p);
   return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@ cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUte
 struct BwdParams {
   float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows
   float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows
-  float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled)
+  float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled, TMA reduce-add target)
   unsigned* status;                // device status word
   int N, NQP;                      // NQP = N rounded up to a multiple of 128
   int Hq, Hkv, BH, BHkv;           // BH = B*Hq, BHkv = B*Hkv
@@ -33,6 +33,7 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;
+  CUtensorMap dqacc;               // fp32 [BH, N, d] accumulator, boxes of 32 columns
 };
 
 // The three backward phases, each one launch on `stream`, d in {64, 128}.
