@@ -240,16 +240,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const uint32_t id_kk = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       const uint32_t id_kmn = make_idesc(1, 128, D, 0, 1);   // dV, dK: A K-major (or TMEM), B MN-major
       const uint32_t id_mnmn = make_idesc(1, 128, D, 1, 1);  // dQ: A = dS (MN-major view of dS^T), B = K MN-major
+      // descriptors built once; each MMA only adds a compile-time offset
+      const uint64_t k_kmaj = smem_desc_sw128(s_k, 16, 1024), k_mn = smem_desc_sw128(s_k, kBoxBytes, 1024);
+      const uint64_t v_kmaj = smem_desc_sw128(s_v, 16, 1024);
+      const uint64_t ds_kmaj = smem_desc_sw128(s_ds, 16, 1024), ds_mn = smem_desc_sw128(s_ds, kBoxBytes, 1024);
+      const uint64_t q_kmaj[2] = {smem_desc_sw128(s_q(0), 16, 1024), smem_desc_sw128(s_q(1), 16, 1024)};
+      const uint64_t q_mn[2] = {smem_desc_sw128(s_q(0), kBoxBytes, 1024), smem_desc_sw128(s_q(1), kBoxBytes, 1024)};
+      const uint64_t do_kmaj[2] = {smem_desc_sw128(s_do(0), 16, 1024), smem_desc_sw128(s_do(1), 16, 1024)};
+      const uint64_t do_mn[2] = {smem_desc_sw128(s_do(0), kBoxBytes, 1024), smem_desc_sw128(s_do(1), kBoxBytes, 1024)};
       bool ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
       for (int step = 0; step < nsteps && ok; ++step) {
         const int st = step & 1;
+        const uint64_t qk = st ? q_kmaj[1] : q_kmaj[0], qm = st ? q_mn[1] : q_mn[0];
+        const uint64_t dok = st ? do_kmaj[1] : do_kmaj[0], dom = st ? do_mn[1] : do_mn[0];
         if (!mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {                // S^T = K Q^T
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
-          mma_bf16_ss(tbase + C::kColS, smem_desc_sw128(s_k + off, 16, 1024),
-                      smem_desc_sw128(s_q(st) + off, 16, 1024), id_kk, kk > 0);
+          mma_bf16_ss(tbase + C::kColS, desc_add(k_kmaj, off), desc_add(qk, off), id_kk, kk > 0);
         }
         mma_commit(bar_s_full);
         if (step > 0 && !mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline)) { ok = false; break; }
@@ -257,8 +266,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {                // dP^T = V dO^T
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
-          mma_bf16_ss(tbase + C::kColDP, smem_desc_sw128(s_v + off, 16, 1024),
-                      smem_desc_sw128(s_do(st) + off, 16, 1024), id_kk, kk > 0);
+          mma_bf16_ss(tbase + C::kColDP, desc_add(v_kmaj, off), desc_add(dok, off), id_kk, kk > 0);
         }
         mma_commit(bar_dp_full);
         if (!mbar_wait(bar_p_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
@@ -267,8 +275,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a = tbase + C::kColS + 64 * (kk >> 2) + (kk & 3) * 8;
-          mma_bf16_ts(tbase + C::kColDV, a, smem_desc_sw128(s_do(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn,
-                      step > 0 || kk > 0);
+          mma_bf16_ts(tbase + C::kColDV, a, desc_add(dom, kk * 16 * 128), id_kmn, step > 0 || kk > 0);
         }
         if (!mbar_wait(bar_ds_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
@@ -276,15 +283,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
-          mma_bf16_ss(tbase + C::kColDK, smem_desc_sw128(s_ds + off, 16, 1024),
-                      smem_desc_sw128(s_q(st) + kk * 16 * 128, kBoxBytes, 1024), id_kmn, step > 0 || kk > 0);
+          mma_bf16_ss(tbase + C::kColDK, desc_add(ds_kmaj, off), desc_add(qm, kk * 16 * 128), id_kmn,
+                      step > 0 || kk > 0);
         }
         // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys), into the dP^T columns
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_bf16_ss(tbase + C::kColDP, smem_desc_sw128(s_ds + kk * 16 * 128, kBoxBytes, 1024),
-                      smem_desc_sw128(s_k + kk * 16 * 128, kBoxBytes, 1024), id_mnmn, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tbase + C::kColDP, desc_add(ds_mn, kk * 16 * 128), desc_add(k_mn, kk * 16 * 128), id_mnmn, kk > 0);
         mma_commit(bar_dq_full);
       }
       if (ok) mma_commit(bar_o_final);

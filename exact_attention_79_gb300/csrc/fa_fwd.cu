@@ -62,12 +62,13 @@ template <typename T, int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc,
                                          uint32_t sq_lo = 0, uint32_t sk_lo = 0) {
   using C = FwdCfg<T, D>;
+  const uint64_t qd = smem_desc_sw128(sq, 16, 1024), kd = smem_desc_sw128(sk, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
     const uint32_t kb = kk * 32;                              // byte offset along d
     const uint32_t off = (kb / 128) * kBoxBytes + (kb % 128);
-    const uint64_t a = smem_desc_sw128(sq + off, 16, 1024);
-    const uint64_t b = smem_desc_sw128(sk + off, 16, 1024);
+    const uint64_t a = desc_add(qd, off);
+    const uint64_t b = desc_add(kd, off);
     if constexpr (C::kTf32) {
       mma_tf32_ss(d_tmem, a, b, idesc, kk > 0);
       mma_tf32_ss(d_tmem, a, smem_desc_sw128(sk_lo + off, 16, 1024), idesc, 1);
@@ -106,20 +107,19 @@ __device__ __forceinline__ void split_tf32_row(uint32_t tile, uint32_t lo, int r
 template <typename T, int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sv, uint32_t idesc, bool acc) {
   using C = FwdCfg<T, D>;
+  // bf16: V tile is [keys, d] with d contiguous, an MN-major B operand: leading
+  // byte offset = distance between 128-byte column chunks (one TMA box), stride
+  // byte offset = distance between 8-key groups. tf32: sv = V^T [d rows, 128
+  // keys], K-major, four boxes of 32 keys, each D rows x 128 bytes.
+  const uint64_t vd = C::kTf32 ? smem_desc_sw128(sv, 16, 1024) : smem_desc_sw128(sv, kBoxBytes, 1024);
 #pragma unroll
   for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
     const uint32_t a = p_tmem + kk * 8;                       // 8 TMEM columns per K step
     if constexpr (C::kTf32) {
-      // sv = V^T [d rows, 128 keys], K-major: four boxes of 32 keys, each D rows x 128 bytes
       const uint32_t kb = kk * 32;
-      const uint64_t b = smem_desc_sw128(sv + (kb / 128) * (D * 128) + (kb % 128), 16, 1024);
-      mma_tf32_ts(d_tmem, a, b, idesc, acc || kk > 0);
+      mma_tf32_ts(d_tmem, a, desc_add(vd, (kb / 128) * (D * 128) + (kb % 128)), idesc, acc || kk > 0);
     } else {
-      // V tile is [keys, d] with d contiguous: MN-major B operand. Leading byte
-      // offset = distance between 128-byte column chunks (one TMA box), stride
-      // byte offset = distance between 8-key groups.
-      const uint64_t b = smem_desc_sw128(sv + kk * C::kUmmaK * 128, kBoxBytes, 1024);
-      mma_bf16_ts(d_tmem, a, b, idesc, acc || kk > 0);
+      mma_bf16_ts(d_tmem, a, desc_add(vd, kk * C::kUmmaK * 128), idesc, acc || kk > 0);
     }
   }
 }
