@@ -26,6 +26,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                     _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_bwd_deterministic": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                  _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_preprocess": (_I, [_VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _VP]),
     "fa_bwd_dkdv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_dq": (_I, [_VP, _VP, _SZ, _I, _I, _I, _I, _I, _F, _VP]),
@@ -108,8 +110,11 @@ def bwd_workspace_bytes(B, Hq, Hkv, N, d):
     return int(load().fa_bwd_workspace_bytes(B, Hq, Hkv, N, d))
 
 
-def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None):
-    """dQ, dK, dV of <O, dO> on the current stream (bf16 tensors, fp32 lse)."""
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
+        deterministic=False):
+    """dQ, dK, dV of <O, dO> on the current stream (bf16 tensors, fp32 lse).
+
+    deterministic=True runs fa_bwd_deterministic (bit-reproducible, slower)."""
     import torch
     lib = load()
     B, Hq, Hkv, N, d = _shape(q, k)
@@ -124,9 +129,10 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check("fa_bwd", lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
-                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-                                B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
+    name = "fa_bwd_deterministic" if deterministic else "fa_bwd"
+    _check(name, getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                                    B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
     return dq, dk, dv
 
 

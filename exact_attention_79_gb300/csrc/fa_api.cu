@@ -138,7 +138,7 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdWorkspace {
-  size_t off_lse2, off_d, off_dq, total;
+  size_t off_lse2, off_d, off_dq, total;   // off_dq: the bytes the deterministic backward needs
 };
 
 BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
@@ -152,13 +152,15 @@ BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
   return w;
 }
 
-// Validates sizes and workspace, resolves the device, fills BwdParams.
+// Validates sizes and workspace, resolves the device, fills BwdParams. With
+// lse_d_only the workspace only has to hold the LSE and D parts.
 fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
-                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms) {
+                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms, bool lse_d_only = false) {
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
   const BwdWorkspace w = bwd_workspace(B, Hq, N, d);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < (lse_d_only ? w.off_dq : w.total))
     return FA_ERR_WORKSPACE;
   unsigned* status = nullptr;
   st = device_state(&status, num_sms);
@@ -243,6 +245,28 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   st = fa_bwd_dkdv(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale, stream);
   if (st != FA_OK) return st;
   return fa_bwd_dq(dq, workspace, workspace_bytes, B, Hq, Hkv, N, d, scale, stream);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                               int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, true);
+  if (st != FA_OK) return st;
+  fa::BwdMaps m;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv) ||
+      !make_map(&m.dq, dq, 2, d, N, BHq))
+    return FA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_pre(d, o, dO, lse, p, num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_deterministic(d, m, p, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,

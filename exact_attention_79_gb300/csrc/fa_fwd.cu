@@ -36,12 +36,15 @@ struct FwdCfg {
   static constexpr int kNBox = D / kChunk;            // TMA boxes per 128-row tile
   static constexpr int kTileBytes = kNBox * kBoxBytes;
   static constexpr int kUmmaK = 32 / kElt;            // K per MMA instruction (32 bytes)
-  static constexpr int kStages = kTf32 ? 2 : ((kTileBytes == 16384) ? 8 : 4);   // K/V slot ring
+  // K/V slot ring, as deep as shared memory allows: the next K tile is
+  // loaded into the slot the producer got back two tiles ago, and a shallow
+  // ring leaves its TMA latency exposed to the tensor core at every tile.
+  static constexpr int kStages = kTf32 ? 3 : ((kTileBytes == 16384) ? 12 : 5);
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }
   static __device__ __forceinline__ uint32_t col_o(int i) { return 256u + D * i; }
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   // fp32 extra buffers: the low tf32 parts of Q and of the current K tile
   static constexpr int kSmemBytes = (2 + kStages + (kTf32 ? 2 : 0)) * kTileBytes + kBarBytes + 1024;
   static constexpr uint32_t kFmt = kTf32 ? 2u : 1u;

@@ -33,7 +33,8 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;
-  CUtensorMap dqacc;               // fp32 [BH, N, d] accumulator, boxes of 32 columns
+  CUtensorMap dqacc;               // fp32 [BH, N, d] accumulator, boxes of 32 columns (fa_bwd)
+  CUtensorMap dq;                  // bf16 dQ output (deterministic backward)
 };
 
 // The three backward phases, each one launch on `stream`, d in {64, 128}.
@@ -41,5 +42,9 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* ls
                            cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream);
+
+// Deterministic backward after launch_bwd_pre: the dK/dV pass and the dQ pass
+// (two launches on `stream`); reads only the LSE and D parts of the workspace.
+cudaError_t launch_bwd_deterministic(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace fa

@@ -87,6 +87,18 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/* Backward with bit-reproducible results: the same arguments as fa_bwd and
+ * the same results within rounding, but dQ, dK and dV come out with the same
+ * bits on every run. dQ is computed in a pass of its own over the key tiles
+ * instead of accumulated across key tiles with reduce-adds, which costs about
+ * 40% more tensor-core work. The workspace only needs its LSE and D parts:
+ * 2 * B * Hq * ceil(N/128)*128 * 4 bytes, each half 256-byte aligned (any
+ * size fa_bwd_workspace_bytes returns is enough). */
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dO, void* dq, void* dk, void* dv, void* workspace,
+                               size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
+                               float scale, void* stream);
+
 /* The three phases fa_bwd runs, in this order on one stream, exposed for
  * callers that schedule or time them separately. Arguments mean what they
  * mean for fa_bwd; the workspace carries state from one phase to the next.
