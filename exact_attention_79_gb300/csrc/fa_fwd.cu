@@ -18,6 +18,12 @@
 //   warp 1      tensor-core issuer (one thread) + TMEM owner
 //   warps 2-5   softmax group 0 (query tile 0), one thread per query row
 //   warps 6-9   softmax group 1 (query tile 1)
+//   warp 10     (bf16) ring watcher: waits for V_j and K_{j+1} to land and
+//               adds one arrival to each group's P-ready barrier, so the
+//               issuer learns "P_j written and its operands resident" from a
+//               single barrier. Every barrier poll of the issuing thread costs
+//               on the order of a hundred cycles during which no MMA is
+//               issued, and the issue queue holds only one or two MMAs.
 // TMEM (512 columns x 128 lanes, fp32): S0 | S1 | O0 | O1. The probabilities P
 // overwrite S in place (bf16 pairs, or tf32) and feed O += P V with A read
 // from TMEM. The rescale of O happens only when a row max grows by more than
@@ -40,7 +46,7 @@ struct FwdCfg {
   // loaded into the slot the producer got back two tiles ago, and a shallow
   // ring leaves its TMA latency exposed to the tensor core at every tile.
   static constexpr int kStages = kTf32 ? 3 : ((kTileBytes == 16384) ? 12 : 5);
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = kTf32 ? 320 : 352;      // bf16 adds the ring watcher warp
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }
   static __device__ __forceinline__ uint32_t col_o(int i) { return 256u + D * i; }
@@ -128,7 +134,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const FwdParams p) {
@@ -176,7 +182,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
       mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_p_ready(i), 128);
+      mbar_init(bar_p_ready(i), C::kPingPong ? 129 : 128);   // + the ring watcher (bf16)
       mbar_init(bar_o_final(i), 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -254,9 +260,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         uint32_t sv = 0, sk_next = 0;
         int vslot = 0, knext = 0;
         const bool has_next = j + 1 < nmax;
-        ok = take(sv, vslot);
-        if (ok && has_next) ok = take(sk_next, knext);
-        if (!ok) break;
+        if constexpr (C::kPingPong) {
+          // residency of V_j and K_{j+1} is folded into the P-ready barriers
+          vslot = c % C::kStages;
+          sv = s_kv + vslot * C::kTileBytes;
+          ++c;
+          if (has_next) {
+            knext = c % C::kStages;
+            sk_next = s_kv + knext * C::kTileBytes;
+            ++c;
+          }
+        } else {
+          ok = take(sv, vslot);
+          if (ok && has_next) ok = take(sk_next, knext);
+          if (!ok) break;
+        }
         for (int i = 0; i < 2; ++i) {
           if (j >= nkv[i]) continue;
           if (!mbar_wait(bar_p_ready(i), j & 1, abort_flag, deadline)) { ok = false; break; }
@@ -272,6 +290,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         if (!ok) break;
         mma_commit(bar_kv_empty(vslot));
         if (has_next) mma_commit(bar_kv_empty(knext));
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ ring watcher (bf16)
+    if (C::kPingPong && lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < nmax && ok; ++j) {
+        // iteration j reads V_j (load 2j+1) and, if there is a next tile, K_{j+1} (load 2j+2)
+        const int cv = 2 * j + 1;
+        ok = mbar_wait(bar_kv_full(cv % C::kStages), (cv / C::kStages) & 1, abort_flag, deadline);
+        if (ok && j + 1 < nmax) {
+          const int ck = 2 * j + 2;
+          ok = mbar_wait(bar_kv_full(ck % C::kStages), (ck / C::kStages) & 1, abort_flag, deadline);
+        }
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j >= nkv[i]) continue;
+          // arrive for phase j only once phase j-1 has completed
+          if (j > 0) ok = mbar_wait(bar_p_ready(i), (j - 1) & 1, abort_flag, deadline);
+          if (ok) mbar_arrive(bar_p_ready(i));
+        }
       }
     }
     __syncwarp();
