@@ -368,13 +368,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 4; c < 128; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
       const bool grow = mx > m + 8.0f;             // also true on the first tile (m = -inf)
       const float m_new = grow ? mx : m;
       const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
@@ -402,10 +402,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           uint32_t pr[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2_approx(fmaf(s[h2 * 64 + 2 * c], sl2, neg_m));
-            const float p1 = ex2_approx(fmaf(s[h2 * 64 + 2 * c + 1], sl2, neg_m));
-            sum0 += p0;
-            sum1 += p1;
+            float x0, x1;
+            fma2_bc(x0, x1, s[h2 * 64 + 2 * c], s[h2 * 64 + 2 * c + 1], sl2, neg_m);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            add2_acc(sum0, sum1, p0, p1);
             pr[c] = pack_bf16x2(p0, p1);
           }
           tmem_st_32x32b_x32(t_s + h2 * 32, pr);
