@@ -302,7 +302,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     if (C::kPingPong && lane == 0) {
       // L: the group whose S MMAs are issued last in each step (group 1 unless absent)
       const int L = (nkv[1] == nmax) ? 1 : 0;
-      bool ok = true;
+      // parity waits only tell phase k from phase k-1: observe every phase of
+      // every slot in order, starting with K_0 (load 0), which only the
+      // issuer needs
+      bool ok = mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
       auto hand_p = [&](int i, int j) {
         // arrive for phase j only once phase j-1 has completed
         if (j > 0) ok = mbar_wait(bar_p_ready(i), (j - 1) & 1, abort_flag, deadline);
@@ -382,15 +385,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // row max: four independent chains of three-input max over 32 logits each
+      float mk[4];
 #pragma unroll
-      for (int c = 4; c < 128; c += 8) {
-        mx0 = fmax3(mx0, s[c], s[c + 1]);
-        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+      for (int k = 0; k < 4; ++k) {
+        const float* v = s + 32 * k;
+        float a = fmax3(v[0], v[1], v[2]);
+#pragma unroll
+        for (int e = 3; e < 31; e += 2) a = fmax3(a, v[e], v[e + 1]);
+        mk[k] = fmaxf(a, v[31]);
       }
-      const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+      const float mx = fmax3(mk[0], mk[1], fmaxf(mk[2], mk[3])) * sl2;
       const bool grow = mx > m + 8.0f;             // also true on the first tile (m = -inf)
       const float m_new = grow ? mx : m;
       const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
