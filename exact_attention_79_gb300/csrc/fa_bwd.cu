@@ -106,13 +106,21 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(__nv_bfloat16* __restrict__
 }
 
 // ------------------------------------------------------------------ dK / dV
+// Shared memory: K | V | dS^T | stage0 {Q, dO} | stage1 {Q, dO} | LSE[2] | D[2] | barriers.
+// dQ_i (fp32, 128 rows x D) leaves through shared memory in two halves, one
+// per softmax-gradient group, written over step i's own stage once its
+// readers are done: columns [0, D/2) over Q_i (read by S^T_i and dK_i),
+// [D/2, D) over dO_i (read by dP^T_i and dV_i). The reducer sends the Q-side
+// half first, since Q_{i+2} is needed earlier in step i+2 than dO_{i+2}; the
+// reductions run at the L2's fp32 reduce rate (about 23 bytes per cycle per
+// SM with every SM reducing), so each half holds its region ~1600 cycles.
 template <int D>
 struct BwdCfg {
   static constexpr int kNBox = D / 64;                 // bf16: 64 elements per 128-byte row
   static constexpr int kTileBytes = kNBox * kBoxBytes;  // one [128, D] bf16 tile
   static constexpr int kDsBytes = 2 * kBoxBytes;       // dS^T [128 keys, 128 queries] bf16
   static constexpr int kVecBytes = 512;                // 128 fp32 (LSE or D of one query tile)
-  // shared memory: K | V | dS^T | stage0 {Q, dO} | stage1 {Q, dO} | lse2[2] | D[2] | barriers
+  static constexpr int kDqHalfBoxes = D / 64;          // fp32 boxes of 32 columns in D/2 columns
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffDs = 2 * kTileBytes;
@@ -120,17 +128,19 @@ struct BwdCfg {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffVec = kOffStage + 2 * kStageBytes;
   static constexpr int kOffBar = kOffVec + 4 * kVecBytes;
-  static constexpr int kLayoutBytes = kOffBar + 128;
+  static constexpr int kLayoutBytes = kOffBar + 192;
   static constexpr int kSmemAlloc = 232448;            // the per-block maximum; the base is aligned inside it
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
-  static constexpr int kThreads = 352;     // producer, MMA, 8 softmax-gradient warps, dQ reducer
+  // producer, MMA, 8 softmax-gradient warps, dQ reducer, ring watcher
+  static constexpr int kThreads = 384;
   static_assert(kLayoutBytes <= kSmemAlloc, "shared memory budget");
   static_assert(2 * D + 256 <= 512, "TMEM budget");
+  static_assert(kDqHalfBoxes * kBoxBytes <= kDsBytes && kDqHalfBoxes * kBoxBytes <= kTileBytes, "dQ staging");
 };
 
 template <int D>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
@@ -141,7 +151,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kLayoutBytes > static_cast<uint32_t>(C::kSmemAlloc)) {
-    // The layout needs the dynamic window to start within 896 bytes of a
+    // The layout needs the dynamic window to start within 832 bytes of a
     // 1 KB boundary; refuse (and report) rather than overrun.
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
@@ -153,14 +163,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   auto s_dvec = [&](int st) { return base + C::kOffVec + (2 + st) * C::kVecBytes; };
   const uint32_t bars = base + C::kOffBar;
   const uint32_t bar_kv_full = bars;
-  auto bar_q_full = [&](int st) { return bars + 8u + 8u * st; };
-  auto bar_q_empty = [&](int st) { return bars + 24u + 8u * st; };
-  auto bar_dq_staged = [&](int st) { return bars + 40u + 8u * st; };
-  const uint32_t bar_s_full = bars + 56, bar_dp_full = bars + 64, bar_p_ready = bars + 72;
-  const uint32_t bar_ds_ready = bars + 80, bar_dq_full = bars + 88, bar_dq_free = bars + 96;
-  const uint32_t bar_o_final = bars + 104;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 112);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 116);
+  auto bar_q_full = [&](int st) { return bars + 8u + 8u * st; };       // Q, LSE, D of the step
+  auto bar_do_full = [&](int st) { return bars + 24u + 8u * st; };
+  auto bar_q_empty = [&](int st) { return bars + 40u + 8u * st; };     // regions read out by the reducer
+  auto bar_do_empty = [&](int st) { return bars + 56u + 8u * st; };
+  // per softmax group and stage: a group cannot stage the same stage again
+  // before the reducer has taken the previous use, so parities never alias
+  auto bar_dq_staged = [&](int g, int st) { return bars + 72u + 16u * g + 8u * st; };
+  const uint32_t bar_s_full = bars + 104, bar_dp_full = bars + 112, bar_p_ready = bars + 120;
+  const uint32_t bar_ds_ready = bars + 128, bar_dq_full = bars + 136, bar_dq_free = bars + 144;
+  const uint32_t bar_o_final = bars + 160;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 168);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 172);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -181,15 +195,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     mbar_init(bar_kv_full, 1);
     for (int st = 0; st < 2; ++st) {
       mbar_init(bar_q_full(st), 1);
+      mbar_init(bar_do_full(st), 1);
       mbar_init(bar_q_empty(st), 1);
-      mbar_init(bar_dq_staged(st), 256);
+      mbar_init(bar_do_empty(st), 1);
+      mbar_init(bar_dq_staged(0, st), 128);
+      mbar_init(bar_dq_staged(1, st), 128);
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_p_ready, 256);
     mbar_init(bar_ds_ready, 256);
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_dq_free, 256);
+    mbar_init(bar_dq_free, 257);           // + the watcher: dO of the next step has landed
     mbar_init(bar_o_final, 1);
     fence_mbar_init();
   }
@@ -202,6 +219,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+  auto step_head = [&](int step) { return b * p.Hq + hk * G + step / tiles_per_head; };
+  auto step_tile = [&](int step) { return it0 + step % tiles_per_head; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -215,27 +234,28 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       for (int step = 0; step < nsteps; ++step) {
         const int st = step & 1;
-        if (!mbar_wait(bar_q_empty(st), ((step >> 1) & 1) ^ 1, abort_flag, deadline)) break;
-        const int h = hk * G + step / tiles_per_head;
-        const int it = it0 + step % tiles_per_head;
-        const int bh = b * p.Hq + h;
-        mbar_arrive_expect_tx(bar_q_full(st), 2 * C::kTileBytes + 2 * C::kVecBytes);
-        for (int bx = 0; bx < C::kNBox; ++bx) {
+        const uint32_t par = ((step >> 1) & 1) ^ 1;
+        const int bh = step_head(step), it = step_tile(step);
+        if (!mbar_wait(bar_q_empty(st), par, abort_flag, deadline)) break;
+        mbar_arrive_expect_tx(bar_q_full(st), C::kTileBytes + 2 * C::kVecBytes);
+        for (int bx = 0; bx < C::kNBox; ++bx)
           tma_load_3d(s_q(st) + bx * kBoxBytes, &map_q, bar_q_full(st), bx * 64, it * kBM, bh);
-          tma_load_3d(s_do(st) + bx * kBoxBytes, &map_do, bar_q_full(st), bx * 64, it * kBM, bh);
-        }
         const size_t voff = static_cast<size_t>(bh) * p.NQP + static_cast<size_t>(it) * kBM;
         bulk_load(s_lse(st), p.ws_lse2 + voff, C::kVecBytes, bar_q_full(st));
         bulk_load(s_dvec(st), p.ws_d + voff, C::kVecBytes, bar_q_full(st));
+        if (!mbar_wait(bar_do_empty(st), par, abort_flag, deadline)) break;
+        mbar_arrive_expect_tx(bar_do_full(st), C::kTileBytes);
+        for (int bx = 0; bx < C::kNBox; ++bx)
+          tma_load_3d(s_do(st) + bx * kBoxBytes, &map_do, bar_do_full(st), bx * 64, it * kBM, bh);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issuer
-    // Per query tile: S^T, [dQ of the previous tile drained] dP^T, [P^T ready]
-    // dV, [dS^T ready] dK, dQ. dQ goes into the dP^T columns, so the next S^T
-    // never waits for a drain; the tensor core runs the in-order MMAs of one
-    // thread in issue order, which keeps every TMEM reuse below safe.
+    // Step i: [P^T_i ready] dV, [dS^T_i ready] dK, dQ_i, then for step i+1:
+    // [Q_{i+1} landed] S^T, [dQ_i read out of TMEM, dO_{i+1} landed] dP^T.
+    // dQ goes into the dP^T columns; one thread's MMAs run in issue order,
+    // which keeps every TMEM reuse below safe.
     if (lane == 0) {
       const uint32_t id_kk = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       const uint32_t id_kmn = make_idesc(1, 128, D, 0, 1);   // dV, dK: A K-major (or TMEM), B MN-major
@@ -248,27 +268,34 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const uint64_t q_mn[2] = {smem_desc_sw128(s_q(0), kBoxBytes, 1024), smem_desc_sw128(s_q(1), kBoxBytes, 1024)};
       const uint64_t do_kmaj[2] = {smem_desc_sw128(s_do(0), 16, 1024), smem_desc_sw128(s_do(1), 16, 1024)};
       const uint64_t do_mn[2] = {smem_desc_sw128(s_do(0), kBoxBytes, 1024), smem_desc_sw128(s_do(1), kBoxBytes, 1024)};
-      bool ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
-      for (int step = 0; step < nsteps && ok; ++step) {
-        const int st = step & 1;
-        const uint64_t qk = st ? q_kmaj[1] : q_kmaj[0], qm = st ? q_mn[1] : q_mn[0];
-        const uint64_t dok = st ? do_kmaj[1] : do_kmaj[0], dom = st ? do_mn[1] : do_mn[0];
-        if (!mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
-        tc_fence_after();
+      auto issue_s = [&](int st) {                          // S^T = K Q^T
+        const uint64_t qk = st ? q_kmaj[1] : q_kmaj[0];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {                // S^T = K Q^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
           mma_bf16_ss(tbase + C::kColS, desc_add(k_kmaj, off), desc_add(qk, off), id_kk, kk > 0);
         }
         mma_commit(bar_s_full);
-        if (step > 0 && !mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline)) { ok = false; break; }
-        tc_fence_after();
+      };
+      auto issue_dp = [&](int st) {                         // dP^T = V dO^T
+        const uint64_t dok = st ? do_kmaj[1] : do_kmaj[0];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {                // dP^T = V dO^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
           mma_bf16_ss(tbase + C::kColDP, desc_add(v_kmaj, off), desc_add(dok, off), id_kk, kk > 0);
         }
         mma_commit(bar_dp_full);
+      };
+      bool ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline) && mbar_wait(bar_q_full(0), 0, abort_flag, deadline);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = mbar_wait(bar_do_full(0), 0, abort_flag, deadline);
+        if (ok) issue_dp(0);
+      }
+      for (int step = 0; step < nsteps && ok; ++step) {
+        const int st = step & 1;
+        const uint64_t qm = st ? q_mn[1] : q_mn[0], dom = st ? do_mn[1] : do_mn[0];
         if (!mbar_wait(bar_p_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
         // dV += P^T dO  (K = 128 queries; P^T of query q sits in S column 64*(q/64) + (q%64)/2)
@@ -291,29 +318,64 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ss(tbase + C::kColDP, desc_add(ds_mn, kk * 16 * 128), desc_add(k_mn, kk * 16 * 128), id_mnmn, kk > 0);
         mma_commit(bar_dq_full);
+        if (step + 1 < nsteps) {
+          const int sn = (step + 1) & 1;
+          if (!mbar_wait(bar_q_full(sn), ((step + 1) >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(sn);                                      // P^T_i in the S columns was read by dV_i
+          if (!mbar_wait(bar_dq_free, step & 1, abort_flag, deadline)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp(sn);
+        }
       }
       if (ok) mma_commit(bar_o_final);
     }
     __syncwarp();
   } else if (warp == 10) {
     // ------------------------------------------------------------ dQ reducer
-    // Adds each staged fp32 dQ tile into the global accumulator with TMA
-    // bulk reductions, then hands the stage buffer back to the producer.
+    // Adds each staged fp32 dQ half into the global accumulator with TMA bulk
+    // reductions, both halves in flight together; each region goes back to
+    // the producer as soon as its half has been read.
     if (lane == 0) {
       for (int step = 0; step < nsteps; ++step) {
         const int st = step & 1;
-        if (!mbar_wait(bar_dq_staged(st), (step >> 1) & 1, abort_flag, deadline)) break;
-        const int h = hk * G + step / tiles_per_head;
-        const int it = it0 + step % tiles_per_head;
-        const int bh = b * p.Hq + h;
+        const int bh = step_head(step), it = step_tile(step);
+        bool ok = true;
+        for (int g = 0; g < 2 && ok; ++g) {
+          ok = mbar_wait(bar_dq_staged(g, st), (step >> 1) & 1, abort_flag, deadline);
+          if (!ok) break;
+          const uint32_t src = g ? s_do(st) : s_q(st);
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&map_dqacc, s_q(st) + bx * kBoxBytes, bx * 32, it * kBM, bh);
-        tma_store_commit();
-        tma_store_wait_read0();
+          for (int bx = 0; bx < C::kDqHalfBoxes; ++bx)
+            tma_reduce_add_3d(&map_dqacc, src + bx * kBoxBytes, g * (D / 2) + bx * 32, it * kBM, bh);
+          tma_store_commit();
+        }
+        if (!ok) break;
+        tma_store_wait_read<1>();
         mbar_arrive(bar_q_empty(st));
+        tma_store_wait_read0();
+        mbar_arrive(bar_do_empty(st));
       }
       tma_store_wait_all0();
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ ring watcher
+    // Adds one arrival to the "dQ_i read out" barrier once dO_{i+1} has
+    // landed, so the issuer learns both from a single poll before dP^T_{i+1}.
+    // Parity waits only tell phase k from phase k-1, so every phase of each
+    // stage's barrier is observed in order, dO_0 (which only the issuer
+    // needs) included: without it, dO_2 could pass for landed while dO_0 was
+    // still in flight.
+    if (lane == 0) {
+      bool ok = mbar_wait(bar_do_full(0), 0, abort_flag, deadline);
+      for (int step = 0; step + 1 < nsteps && ok; ++step) {
+        const int sn = (step + 1) & 1;
+        ok = mbar_wait(bar_do_full(sn), ((step + 1) >> 1) & 1, abort_flag, deadline);
+        // arrive for phase `step` only once phase step-1 has completed
+        if (ok && step > 0) ok = mbar_wait(bar_dq_free, (step - 1) & 1, abort_flag, deadline);
+        if (ok) mbar_arrive(bar_dq_free);
+      }
     }
     __syncwarp();
   } else {
@@ -327,7 +389,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     bool ok = true;
     for (int step = 0; step < nsteps && ok; ++step) {
       const int st = step & 1;
-      const int it = it0 + step % tiles_per_head;
+      const int it = step_tile(step);
       const bool diag = p.causal && it == jt;
       ok = mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline) &&
            mbar_wait(bar_s_full, step & 1, abort_flag, deadline);
@@ -337,99 +399,112 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const float* lse2 = reinterpret_cast<const float*>(gbase + (s_lse(st) - base));
       const float* dvec = reinterpret_cast<const float*>(gbase + (s_dvec(st) - base));
       // ---- phase A: P^T = 2^(S^T s log2e - LSE log2e), written over S^T as bf16 pairs
+      uint32_t sv[2][32];
+      tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + 64 * g, sv[0]);
+      tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + 64 * g + 32, sv[1]);
+      tmem_wait_ld();
+      reg_fence_x32(sv[0]);
+      reg_fence_x32(sv[1]);
       float pf[64];
+      const float4* l4 = reinterpret_cast<const float4*>(lse2 + 64 * g);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * g + 32 * ch;            // first query column of this chunk
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kColS + c0, sv);
-        tmem_wait_ld();
-        reg_fence_x32(sv);
-        const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
-        uint32_t pp[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 lv = l4[c / 4];
-          const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, -lq[e]));
-            if (key_pad || (diag && c0 + c + e < r)) pv = 0.f;
-            pf[32 * ch + c + e] = pv;
-          }
-          pp[c / 2] = pack_bf16x2(pf[32 * ch + c], pf[32 * ch + c + 1]);
-          pp[c / 2 + 1] = pack_bf16x2(pf[32 * ch + c + 2], pf[32 * ch + c + 3]);
-        }
-        // P^T (bf16 pairs) into TMEM over the S^T columns this group already read
-        tmem_st_32x32b_x16(tbase + lane_off + C::kColS + 64 * g + 16 * ch, pp);
+      for (int c = 0; c < 64; c += 4) {
+        const float4 lv = l4[c / 4];
+        fms2_b(pf[c], pf[c + 1], __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+               sl2, lv.x, lv.y);
+        fms2_b(pf[c + 2], pf[c + 3], __uint_as_float(sv[c >> 5][(c & 31) + 2]),
+               __uint_as_float(sv[c >> 5][(c & 31) + 3]), sl2, lv.z, lv.w);
       }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) pf[c] = ex2_approx(pf[c]);
+      if (key_pad || diag) {
+        // causal diagonal tile: query q sees key r only if q >= r
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (key_pad || 64 * g + c < r) pf[c] = 0.f;
+      }
+      uint32_t pp[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pp[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
+      // P^T (bf16 pairs) into TMEM over the S^T columns this group already read
+      tmem_st_32x32b_x32(tbase + lane_off + C::kColS + 64 * g, pp);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_p_ready);
-      // ---- phase B: dS^T = P^T (dP^T - D) into shared memory (bf16)
+      // ---- phase B: dS^T = P^T (dP^T - D) into shared memory (bf16); the
+      // previous dS^T was last read by dK and dQ of the previous step, whose
+      // completion this group waited for before draining dQ
       ok = mbar_wait(bar_dp_full, step & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      uint32_t dp[2][32];
+      tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + 64 * g, dp[0]);
+      tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + 64 * g + 32, dp[1]);
+      tmem_wait_ld();
+      reg_fence_x32(dp[0]);
+      reg_fence_x32(dp[1]);
+      const float4* d4 = reinterpret_cast<const float4*>(dvec + 64 * g);
+      uint32_t dd[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * g + 32 * ch;
-        uint32_t dp[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + c0, dp);
-        tmem_wait_ld();
-        reg_fence_x32(dp);
-        const float4* d4 = reinterpret_cast<const float4*>(dvec + c0);
-        uint32_t dd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 dv4 = d4[c / 4];
-          const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) ds[e] = pf[32 * ch + c + e] * (__uint_as_float(dp[c + e]) - dq4[e]);
-          dd[c / 2] = pack_bf16x2(ds[0], ds[1]);
-          dd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-        // dS^T row r, query columns [c0, c0 + 32): four 16-byte units of box g
-        const uint32_t box = s_ds + g * kBoxBytes;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, 4 * ch + u)),
-                       "r"(dd[4 * u]), "r"(dd[4 * u + 1]), "r"(dd[4 * u + 2]), "r"(dd[4 * u + 3]) : "memory");
+      for (int c = 0; c < 64; c += 4) {
+        const float4 dv4 = d4[c / 4];
+        float ds[4];
+        dsub_mul2(ds[0], ds[1], __uint_as_float(dp[c >> 5][c & 31]), __uint_as_float(dp[c >> 5][(c & 31) + 1]),
+                  dv4.x, dv4.y, pf[c], pf[c + 1]);
+        dsub_mul2(ds[2], ds[3], __uint_as_float(dp[c >> 5][(c & 31) + 2]), __uint_as_float(dp[c >> 5][(c & 31) + 3]),
+                  dv4.z, dv4.w, pf[c + 2], pf[c + 3]);
+        dd[c / 2] = pack_bf16x2(ds[0], ds[1]);
+        dd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
+      // dS^T row r, query columns [64g, 64g + 64): the eight 16-byte units of box g
+      const uint32_t box = s_ds + g * kBoxBytes;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, u)),
+                     "r"(dd[4 * u]), "r"(dd[4 * u + 1]), "r"(dd[4 * u + 2]), "r"(dd[4 * u + 3]) : "memory");
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds_ready);
 
       // ---- dQ_i: TMEM (lane = query row r of tile `it`, this group's D/2
-      // columns) -> registers -> the stage buffer of this step, which dV and
-      // dK (its only readers) have finished with -> TMA reduce-add (reducer warp)
+      // columns) -> registers -> shared memory over Q_i (group 0) or dO_i
+      // (group 1), whose MMA readers have all completed -> TMA reduce-add
       ok = mbar_wait(bar_dq_full, step & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t dq[D / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t t[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + g * (D / 2) + c0, t);
+      if constexpr (D / 2 == 64) {
+        uint32_t t2[2][32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + g * (D / 2), t2[0]);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + g * (D / 2) + 32, t2[1]);
         tmem_wait_ld();
-        reg_fence_x32(t);
+        reg_fence_x32(t2[0]);
+        reg_fence_x32(t2[1]);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) dq[c0 + c] = t[c];
+        for (int c = 0; c < 64; ++c) dq[c] = t2[c >> 5][c & 31];
+      } else {
+        uint32_t t1[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kColDP + g * (D / 2), t1);
+        tmem_wait_ld();
+        reg_fence_x32(t1);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dq[c] = t1[c];
       }
       tc_fence_before();
       mbar_arrive(bar_dq_free);
-      // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle, box index = column / 32
+      // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle
+      const uint32_t dst0 = g ? s_do(st) : s_q(st);
 #pragma unroll
       for (int u = 0; u < D / 8; ++u) {
-        const int col = g * (D / 2) + 4 * u;
-        const uint32_t dst = swz128(s_q(st) + (col / 32) * kBoxBytes, r, (col % 32) / 4);
+        const int col = 4 * u;                       // column within this group's half
+        const uint32_t dst = swz128(dst0 + (col / 32) * kBoxBytes, r, (col % 32) / 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(dst), "r"(dq[4 * u]), "r"(dq[4 * u + 1]),
                      "r"(dq[4 * u + 2]), "r"(dq[4 * u + 3]) : "memory");
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar_dq_staged(st));
+      mbar_arrive(bar_dq_staged(g, st));
     }
     // ---------------------------------------------------------- dK, dV epilogue
     if (ok) {
@@ -451,7 +526,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           tmem_ld_32x32b_x32(tbase + lane_off + col + c0, t);
           tmem_wait_ld();
           reg_fence_x32(t);
-          const uint32_t box = stg + (c0 / 64) * kBoxBytes;
+          const uint32_t bx = stg + (c0 / 64) * kBoxBytes;
           const int u0 = (c0 % 64) / 8;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -459,7 +534,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               w[e] = pack_bf16x2(__uint_as_float(t[8 * u + 2 * e]) * mul, __uint_as_float(t[8 * u + 2 * e + 1]) * mul);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, r, u0 + u)),
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(bx, r, u0 + u)),
                          "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
           }
         }
