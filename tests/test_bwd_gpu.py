@@ -130,3 +130,26 @@ def test_bwd_workspace_checks(fa):
     assert lib.fa_bwd(*args, ctypes.c_void_p(ws.data_ptr() + 16), need, B, Hq, Hkv, N, d, 1, 0.1, None) == 6
     assert lib.fa_bwd(*args, P(ws), need, B, Hq, Hkv, N, d, 1, -1.0, None) == 1
     fa.check_device_status()
+
+
+def test_bwd_long_sequence_repeatable(fa):
+    """Many query steps per key tile (up to 256) and several waves of CTAs:
+    three backward launches must give bit-identical dK and dV (they are
+    accumulated in a fixed order), finite and bounded gradients, and dQ equal
+    up to the summation order of its fp32 reductions. A pipeline race that
+    lets an MMA read a stage before its tile has landed shows up here as a
+    whole tile of garbage."""
+    B, Hq, Hkv, N, d = 1, 4, 4, 32768, 128
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=77, with_grad=True)
+    dev = torch.device("cuda:0")
+    g = {k: v.to(dev) for k, v in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=True)
+    runs = [fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True) for _ in range(3)]
+    fa.check_device_status()
+    dq0, dk0, dv0 = runs[0]
+    for x in (dq0, dk0, dv0):
+        xf = x.float()
+        assert bool(torch.isfinite(xf).all()) and float(xf.abs().max()) < 1e3
+    for dq, dk, dv in runs[1:]:
+        assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+        assert float((dq.float() - dq0.float()).abs().max()) < 1e-2
