@@ -128,7 +128,7 @@ struct BwdCfg {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffVec = kOffStage + 2 * kStageBytes;
   static constexpr int kOffBar = kOffVec + 4 * kVecBytes;
-  static constexpr int kLayoutBytes = kOffBar + 192;
+  static constexpr int kLayoutBytes = kOffBar + 256;
   static constexpr int kSmemAlloc = 232448;            // the per-block maximum; the base is aligned inside it
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
@@ -151,7 +151,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kLayoutBytes > static_cast<uint32_t>(C::kSmemAlloc)) {
-    // The layout needs the dynamic window to start within 832 bytes of a
+    // The layout needs the dynamic window to start within 768 bytes of a
     // 1 KB boundary; refuse (and report) rather than overrun.
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
@@ -167,14 +167,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   auto bar_do_full = [&](int st) { return bars + 24u + 8u * st; };
   auto bar_q_empty = [&](int st) { return bars + 40u + 8u * st; };     // regions read out by the reducer
   auto bar_do_empty = [&](int st) { return bars + 56u + 8u * st; };
-  // per softmax group and stage: a group cannot stage the same stage again
+  // per softmax group, stage and 32-column fp32 box: the reducer starts on a
+  // box as soon as it is written; a group cannot stage the same stage again
   // before the reducer has taken the previous use, so parities never alias
-  auto bar_dq_staged = [&](int g, int st) { return bars + 72u + 16u * g + 8u * st; };
-  const uint32_t bar_s_full = bars + 104, bar_dp_full = bars + 112, bar_p_ready = bars + 120;
-  const uint32_t bar_ds_ready = bars + 128, bar_dq_full = bars + 136, bar_dq_free = bars + 144;
-  const uint32_t bar_o_final = bars + 160;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 168);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 172);
+  auto bar_dq_staged = [&](int g, int st, int bx) { return bars + 72u + 8u * (4 * g + 2 * st + bx); };
+  const uint32_t bar_s_full = bars + 136, bar_dp_full = bars + 144, bar_p_ready = bars + 152;
+  const uint32_t bar_ds_ready = bars + 160, bar_dq_full = bars + 168, bar_dq_free = bars + 176;
+  const uint32_t bar_o_final = bars + 184;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 192);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 196);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -198,8 +199,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(bar_do_full(st), 1);
       mbar_init(bar_q_empty(st), 1);
       mbar_init(bar_do_empty(st), 1);
-      mbar_init(bar_dq_staged(0, st), 128);
-      mbar_init(bar_dq_staged(1, st), 128);
+      for (int bx = 0; bx < C::kDqHalfBoxes; ++bx) {
+        mbar_init(bar_dq_staged(0, st, bx), 128);
+        mbar_init(bar_dq_staged(1, st, bx), 128);
+      }
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
@@ -341,17 +344,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int st = step & 1;
         const int bh = step_head(step), it = step_tile(step);
         bool ok = true;
+        // group 0's boxes first (its region, Q, is needed first again), each
+        // box as soon as it has been written
         for (int g = 0; g < 2 && ok; ++g) {
-          ok = mbar_wait(bar_dq_staged(g, st), (step >> 1) & 1, abort_flag, deadline);
-          if (!ok) break;
           const uint32_t src = g ? s_do(st) : s_q(st);
-#pragma unroll
-          for (int bx = 0; bx < C::kDqHalfBoxes; ++bx)
+          for (int bx = 0; bx < C::kDqHalfBoxes && ok; ++bx) {
+            ok = mbar_wait(bar_dq_staged(g, st, bx), (step >> 1) & 1, abort_flag, deadline);
+            if (!ok) break;
             tma_reduce_add_3d(&map_dqacc, src + bx * kBoxBytes, g * (D / 2) + bx * 32, it * kBM, bh);
-          tma_store_commit();
+            tma_store_commit();
+          }
         }
         if (!ok) break;
-        tma_store_wait_read<1>();
+        tma_store_wait_read<C::kDqHalfBoxes>();
         mbar_arrive(bar_q_empty(st));
         tma_store_wait_read0();
         mbar_arrive(bar_do_empty(st));
@@ -494,17 +499,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(bar_dq_free);
-      // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle
+      // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle, each released
+      // to the reducer as soon as this group has written it
       const uint32_t dst0 = g ? s_do(st) : s_q(st);
 #pragma unroll
-      for (int u = 0; u < D / 8; ++u) {
-        const int col = 4 * u;                       // column within this group's half
-        const uint32_t dst = swz128(dst0 + (col / 32) * kBoxBytes, r, (col % 32) / 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(dst), "r"(dq[4 * u]), "r"(dq[4 * u + 1]),
-                     "r"(dq[4 * u + 2]), "r"(dq[4 * u + 3]) : "memory");
+      for (int bx = 0; bx < C::kDqHalfBoxes; ++bx) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t dst = swz128(dst0 + bx * kBoxBytes, r, u);
+          const int c = 32 * bx + 4 * u;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(dst), "r"(dq[c]), "r"(dq[c + 1]),
+                       "r"(dq[c + 2]), "r"(dq[c + 3]) : "memory");
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_dq_staged(g, st, bx));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar_dq_staged(g, st));
     }
     // ---------------------------------------------------------- dK, dV epilogue
     if (ok) {
