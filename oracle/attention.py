@@ -23,6 +23,11 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
+# Granularity of a block mask: one 128 x 128 tile of the tiled algorithm
+# ("FlashAttention技术解析" section 6.2 skips whole blocks the same way the
+# causal mask skips the blocks above the diagonal).
+BLOCK = 128
+
 
 def _check(q, k, v):
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
@@ -36,52 +41,70 @@ def _check(q, k, v):
     return B, Hq, Hkv, N, d, Hq // Hkv
 
 
-def _scores(qh, kh, scale, causal, row_index):
+def _scores(qh, kh, scale, causal, row_index, block_mask_bh=None):
     """S = scale * q k^T for the given query rows against all keys, with the
     causal mask applied as -inf (definition; blogweb.cn section 1).
 
     qh: [R, d] query rows whose absolute indices are row_index [R]; kh: [N, d].
+    block_mask_bh: optional [nq, nk] booleans; key j is visible to query i only
+    if block_mask_bh[i // BLOCK, j // BLOCK] (and j <= i when causal).
     """
     s = scale * (qh @ kh.T)
+    key_index = np.arange(kh.shape[0])
     if causal:
-        key_index = np.arange(kh.shape[0])
         s = np.where(key_index[None, :] <= row_index[:, None], s, -np.inf)
+    if block_mask_bh is not None:
+        allowed = np.asarray(block_mask_bh, dtype=bool)[row_index[:, None] // BLOCK, key_index[None, :] // BLOCK]
+        s = np.where(allowed, s, -np.inf)
     return s
 
 
 def _softmax_rows(s):
     """Row-wise softmax and natural-log logsumexp of one whole score row at a
     time. The row max is subtracted before exp (numerical-stability advice,
-    mhpq.cn section 7)."""
-    m = s.max(axis=1)
+    mhpq.cn section 7). A row with no visible key (possible only under a block
+    mask) has P = 0 and LSE = -inf, so its output is 0."""
+    vis = np.isfinite(s).any(axis=1)
+    m = np.where(vis, s.max(axis=1), 0.0)
     e = np.exp(s - m[:, None])
-    lse = m + np.log(e.sum(axis=1))
-    p = np.exp(s - lse[:, None])
+    with np.errstate(divide="ignore"):
+        lse = np.where(vis, m + np.log(np.where(vis, e.sum(axis=1), 1.0)), -np.inf)
+    p = np.where(vis[:, None], np.exp(s - np.where(vis, lse, 0.0)[:, None]), 0.0)
     return p, lse
 
 
-def forward(q, k, v, causal, scale):
+def _block_mask_bh(block_mask, B, Hq, N):
+    """Broadcast an optional block mask to [B, Hq, nq, nk] booleans."""
+    if block_mask is None:
+        return None
+    n = (N + BLOCK - 1) // BLOCK
+    return np.broadcast_to(np.asarray(block_mask, dtype=bool), (B, Hq, n, n))
+
+
+def forward(q, k, v, causal, scale, block_mask=None):
     """O = softmax(scale * Q K^T [+ causal mask]) V and LSE = logsumexp of the
     scaled, masked logits per query row (natural log).
 
     The forward stores only O and the per-row normaliser (aiknowledge.cn FA3
-    section 3); LSE is that normaliser in log form.
+    section 3); LSE is that normaliser in log form. block_mask: optional
+    booleans broadcastable to [B, Hq, ceil(N/128), ceil(N/128)] (see _scores).
     Returns (o [B,Hq,N,d], lse [B,Hq,N]).
     """
     B, Hq, Hkv, N, d, G = _check(q, k, v)
+    bm = _block_mask_bh(block_mask, B, Hq, N)
     o = np.empty((B, Hq, N, d))
     lse = np.empty((B, Hq, N))
     rows = np.arange(N)
     for b in range(B):
         for h in range(Hq):
             hk = h // G
-            s = _scores(q[b, h], k[b, hk], scale, causal, rows)
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h])
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
     return o, lse
 
 
-def backward(q, k, v, do, causal, scale):
+def backward(q, k, v, do, causal, scale, block_mask=None):
     """Gradients of L = <O, dO> with respect to Q, K and V.
 
     The pages only say that the backward recomputes from the stored
@@ -90,9 +113,12 @@ def backward(q, k, v, do, causal, scale):
         P = exp(S - LSE),  D_i = sum_c dO_ic O_ic,  dP = dO V^T,
         dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
     with dK and dV summed over the G query heads that share a KV head.
+    block_mask as in `forward`; a row with no visible key has dQ = 0 and adds
+    nothing to dK or dV.
     Returns (o, lse, dq, dk, dv).
     """
     B, Hq, Hkv, N, d, G = _check(q, k, v)
+    bm = _block_mask_bh(block_mask, B, Hq, N)
     o = np.empty((B, Hq, N, d))
     lse = np.empty((B, Hq, N))
     dq = np.empty((B, Hq, N, d))
@@ -102,7 +128,7 @@ def backward(q, k, v, do, causal, scale):
     for b in range(B):
         for h in range(Hq):
             hk = h // G
-            s = _scores(q[b, h], k[b, hk], scale, causal, rows)
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h])
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
             D = (do[b, h] * o[b, h]).sum(axis=1)

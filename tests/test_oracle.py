@@ -336,9 +336,12 @@ def _planted(monkeypatch, kind):
     real_scores = oa._scores
     real_softmax = oa._softmax_rows
     if kind == "drop_scale":
-        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r: real_scores(qh, kh, 1.0, c, r))
+        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None: real_scores(qh, kh, 1.0, c, r, bm))
+    elif kind == "block_mask_transposed":
+        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None: real_scores(
+            qh, kh, s, c, r, None if bm is None else np.swapaxes(bm, 0, 1)))
     elif kind == "mask_strict":
-        def f(qh, kh, s, causal, r):
+        def f(qh, kh, s, causal, r, bm=None):
             out = s * (qh @ kh.T)
             if causal:
                 out = np.where(np.arange(kh.shape[0])[None, :] < r[:, None], out, -np.inf)
@@ -359,7 +362,7 @@ def _planted(monkeypatch, kind):
         monkeypatch.setattr(oa, "_softmax_rows", g)
 
 
-@pytest.mark.parametrize("kind", ["drop_scale", "mask_strict", "lse_log2", "no_max_shift"])
+@pytest.mark.parametrize("kind", ["drop_scale", "mask_strict", "lse_log2", "no_max_shift", "block_mask_transposed"])
 def test_pins_fail_on_planted_mistakes(monkeypatch, kind):
     """Each planted mistake must break at least one of the pins above."""
     _planted(monkeypatch, kind)
@@ -369,6 +372,7 @@ def test_pins_fail_on_planted_mistakes(monkeypatch, kind):
         lambda: test_against_brute_force(True, 2, 1, 5, 3),
         lambda: test_single_key_gives_that_value_row(),
         lambda: test_zero_query_is_uniform_average(True),
+        lambda: test_block_mask_matches_torch_sdpa(False),
     ]
     for c in checks:
         try:
@@ -389,3 +393,82 @@ def test_transposed_operand_would_be_caught():
     assert np.abs(p @ v[0, 0] - o_t[0, 0]).max() > 1e-3
     o, _ = oracle.forward(q, k, v, True, 0.5)
     np.testing.assert_allclose(o, o_t, atol=1e-12)
+
+
+# ---------------------------------------------------------------- block masks
+def _block_mask(B, Hq, n, density, seed):
+    """Random block mask with the diagonal block always on, so every query row
+    sees at least one key (its own) and torch's masked softmax stays finite."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    m = rng.random((B, Hq, n, n)) < density
+    m[..., np.arange(n), np.arange(n)] = True
+    return m
+
+
+def _expand(block_mask, N):
+    bm = np.repeat(np.repeat(block_mask, oa.BLOCK, axis=-2), oa.BLOCK, axis=-1)
+    return bm[..., :N, :N]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_all_ones_is_dense(causal):
+    """An all-true block mask changes nothing, bit for bit."""
+    q, k, v, do = rand_qkv(1, 2, 1, 300, 8, seed=41, with_do=True)
+    n = 3
+    ones = np.ones((1, 2, n, n), dtype=bool)
+    a = oa.backward(q, k, v, do, causal, 0.3)
+    b = oa.backward(q, k, v, do, causal, 0.3, block_mask=ones)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_matches_torch_sdpa(causal):
+    """Forward and gradients against torch float64 scaled_dot_product_attention
+    with the same mask expanded to elements (AND the causal mask), an
+    independent library routine; rows of 300 keys span three blocks, the last
+    one ragged, and the mask is not symmetric."""
+    B, Hq, Hkv, N, d = 1, 4, 2, 300, 8
+    q, k, v, do = rand_qkv(B, Hq, Hkv, N, d, seed=43, with_do=True)
+    bm = _block_mask(B, Hq, 3, 0.5, seed=44)
+    assert not np.array_equal(bm, np.swapaxes(bm, -1, -2))
+    o, lse, dq, dk, dv = oa.backward(q, k, v, do, causal, 0.25, block_mask=bm)
+    allowed = _expand(bm, N)
+    if causal:
+        allowed = allowed & np.tril(np.ones((N, N), dtype=bool))
+    G = Hq // Hkv
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    kk = tk.repeat_interleave(G, dim=1)
+    vv = tv.repeat_interleave(G, dim=1)
+    to = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, attn_mask=torch.tensor(allowed), scale=0.25)
+    to.backward(torch.tensor(do))
+    s = 0.25 * torch.einsum("bhid,bhjd->bhij", tq.detach(), kk.detach())
+    s = s.masked_fill(~torch.tensor(allowed), float("-inf"))
+    tlse = torch.logsumexp(s, dim=-1)
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, tlse.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_block_mask_empty_rows():
+    """A query block with no visible key block: its rows give O = 0,
+    LSE = -inf and dQ = 0, and they add nothing to dK, dV; so dK, dV equal
+    those of the unmasked problem with those rows' dO set to zero (then
+    dP = 0, D = 0 and dS = 0 for them)."""
+    B, Hq, Hkv, N, d = 1, 2, 2, 384, 8
+    q, k, v, do = rand_qkv(B, Hq, Hkv, N, d, seed=45, with_do=True)
+    bm = np.ones((B, Hq, 3, 3), dtype=bool)
+    bm[:, 0, 1, :] = False                      # head 0, query block 1 sees nothing
+    o, lse, dq, dk, dv = oa.backward(q, k, v, do, False, 0.3, block_mask=bm)
+    rows = slice(128, 256)
+    assert np.all(o[:, 0, rows] == 0) and np.all(np.isneginf(lse[:, 0, rows])) and np.all(dq[:, 0, rows] == 0)
+    do0 = do.copy()
+    do0[:, 0, rows] = 0
+    _, _, dq_ref, dk_ref, dv_ref = oa.backward(q, k, v, do0, False, 0.3)
+    np.testing.assert_allclose(dk, dk_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_ref, rtol=1e-12, atol=1e-13)
+    other = [r for r in range(N) if not 128 <= r < 256]
+    np.testing.assert_allclose(dq[:, 0, other], dq_ref[:, 0, other], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dq[:, 1], dq_ref[:, 1], rtol=1e-12, atol=1e-13)
