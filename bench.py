@@ -41,6 +41,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd", choices=["fused", "deterministic"], default="fused",
+                    help="backward timed: fa_bwd's three phases (default) or fa_bwd_deterministic")
     return ap.parse_args()
 
 
@@ -244,10 +246,20 @@ def native_arm(args, w):
         if code != 0:
             raise RuntimeError(f"{name} failed with status {code}")
 
+    det = args.bwd == "deterministic"
+
     def step(ev):
         ev[0].record(stream)
         check("fa_fwd", lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), *dims, causal, scale, sptr))
         ev[1].record(stream)
+        if det:
+            # one call: preprocess, dK/dV pass, dQ pass (no atomics)
+            check("fa_bwd_deterministic", lib.fa_bwd_deterministic(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq),
+                                                                   P(dk), P(dv), P(ws), ws_bytes, *dims, causal,
+                                                                   scale, sptr))
+            for e in ev[2:]:
+                e.record(stream)
+            return
         check("fa_bwd_preprocess", lib.fa_bwd_preprocess(P(o), P(lse), P(do), P(ws), ws_bytes, *dims, sptr))
         ev[2].record(stream)
         check("fa_bwd_dkdv", lib.fa_bwd_dkdv(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes, *dims,
@@ -295,12 +307,15 @@ def native_arm(args, w):
     value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
     mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
     names = ["fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    if det:
+        names = ["fwd_kernel", "bwd_deterministic (preprocess + det_dkdv_kernel + det_dq_kernel)", "-", "-"]
     peak, peak_src = peak_tflops()
     # dominant kernel of the step and its tensor roofline
-    dom = 0 if mean[0] >= mean[2] else 2
+    dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if det else 2)
     dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
     achieved = dom_flops / (mean[dom] / 1e3) / 1e12
-    traffic = traffic_from_profile("fa_fwd.cu" if dom == 0 else "fa_bwd.cu", names[dom], w.name)
+    traffic = None if (det and dom != 0) else traffic_from_profile("fa_fwd.cu" if dom == 0 else "fa_bwd.cu",
+                                                                   names[dom], w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
                 "algorithmic_flops_per_launch": dom_flops}
@@ -348,12 +363,12 @@ def native_arm(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU", "bwd_variant": args.bwd},
         "frac_of_peak": value / world / peak,
         "fwd_tflops": w.flops_fwd / (mean[0] / 1e3) / 1e12,
         "fwd_frac_of_peak": w.flops_fwd / (mean[0] / 1e3) / 1e12 / peak,
         "bwd_tflops": w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
-        "kernel_ms": dict(zip(names, mean)),
+        "kernel_ms": {n: m for n, m in zip(names, mean) if n != "-"},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,

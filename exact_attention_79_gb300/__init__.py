@@ -20,9 +20,11 @@ _STATUS_NAMES = {
 
 # Every symbol include/fa.h declares, with its ctypes signature.
 _VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_LL = ctypes.c_longlong
 SIGNATURES = {
     "fa_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fwd_blocksparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _LL, _LL, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                     _I, _I, _I, _I, _I, _I, _F, _VP]),
@@ -83,11 +85,31 @@ def _shape(q, k):
     return B, Hq, k.shape[1], N, d
 
 
-def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
+def _mask_args(block_mask, B, Hq, N, device):
+    """Pointer and byte strides of a block mask tensor: uint8 or bool on the
+    device, shape [B or 1, Hq or 1, T, T] with T = ceil(N / 128), the last two
+    dimensions dense (a size-1 batch or head dimension broadcasts)."""
+    import torch
+    T = (N + 127) // 128
+    if block_mask.dtype not in (torch.uint8, torch.bool) or block_mask.device != device:
+        raise ValueError("block_mask must be a uint8 or bool tensor on the device of q")
+    if block_mask.dim() != 4 or tuple(block_mask.shape[2:]) != (T, T) or block_mask.shape[0] not in (1, B) or \
+            block_mask.shape[1] not in (1, Hq):
+        raise ValueError(f"block_mask must be [B or 1, Hq or 1, {T}, {T}]")
+    if block_mask.stride(3) != 1 or block_mask.stride(2) != T:
+        raise ValueError("the last two dimensions of block_mask must be dense")
+    sb = 0 if block_mask.shape[0] == 1 else block_mask.stride(0)
+    sh = 0 if block_mask.shape[1] == 1 else block_mask.stride(1)
+    return _ptr(block_mask), sb, sh
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
     """O, LSE = attention(q, k, v) on the current stream.
 
     q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; bf16 (fa_fwd) or fp32 (fa_fwd_f32)
-    contiguous CUDA tensors. Returns (o like q, lse fp32 [B, Hq, N])."""
+    contiguous CUDA tensors. block_mask (bf16 only): uint8/bool
+    [B or 1, Hq or 1, T, T], T = ceil(N/128), nonzero where query tile i may
+    see key tile j (fa_fwd_blocksparse). Returns (o like q, lse fp32 [B, Hq, N])."""
     import torch
     lib = load()
     B, Hq, Hkv, N, d = _shape(q, k)
@@ -98,6 +120,14 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
             raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if block_mask is not None:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("block masks need bf16 inputs")
+        mp, sb, sh = _mask_args(block_mask, B, Hq, N, q.device)
+        _check("fa_fwd_blocksparse", lib.fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), mp, sb, sh,
+                                                            B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                                            _stream(q)))
+        return o, lse
     fn = {torch.bfloat16: "fa_fwd", torch.float32: "fa_fwd_f32"}.get(q.dtype)
     if fn is None:
         raise ValueError("dtype must be bfloat16 or float32")

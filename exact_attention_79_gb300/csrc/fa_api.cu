@@ -107,7 +107,8 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
 }
 
 fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                     int Hkv, int N, int d, int causal, float scale, void* stream) {
+                     int Hkv, int N, int d, int causal, float scale, void* stream,
+                     const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
@@ -131,6 +132,10 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_limit_ns();
+  p.mask = mask;
+  p.mask_sb = mask_sb;
+  p.mask_sh = mask_sh;
+  p.mask_nt = (N + 127) / 128;
   const cudaError_t e = fa::launch_fwd(elt, d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -272,6 +277,15 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                  int d, int causal, float scale, void* stream) {
   return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const unsigned char* block_mask, long long mask_stride_b, long long mask_stride_h, int B,
+                             int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
+  if (!block_mask || mask_stride_b < 0 || mask_stride_h < 0) return FA_ERR_INVALID_ARG;
+  if ((N + 127) / 128 > fa::kMaskMaxTiles) return FA_ERR_UNSUPPORTED;
+  return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream, block_mask, mask_stride_b,
+                    mask_stride_h);
 }
 
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq, int Hkv,

@@ -135,12 +135,14 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kSparse>
 __global__ void __launch_bounds__(352, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const FwdParams p) {
   using C = FwdCfg<T, D>;
+  // the block-sparse variant gives one ring slot to its list of key tiles
+  constexpr int kSt = kSparse ? C::kStages - 1 : C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -149,19 +151,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const uint32_t s_q[2] = {base, base + C::kTileBytes};
   const uint32_t s_kv = base + 2 * C::kTileBytes;
   // fp32 only: low tf32 parts of Q and of the K tile being used (after the ring)
-  const uint32_t s_q_lo = s_kv + C::kStages * C::kTileBytes;
+  const uint32_t s_q_lo = s_kv + kSt * C::kTileBytes;
   const uint32_t s_k_lo = s_q_lo + C::kTileBytes;
-  const uint32_t bars = s_kv + (C::kStages + (C::kTf32 ? 2 : 0)) * C::kTileBytes;
+  const uint32_t bars = s_kv + (kSt + (C::kTf32 ? 2 : 0)) * C::kTileBytes;
   auto bar_q_full = [&](int i) { return bars + 8u * i; };                       // 2
   auto bar_kv_full = [&](int s) { return bars + 16u + 8u * s; };               // kStages
-  auto bar_kv_empty = [&](int s) { return bars + 16u + 8u * (C::kStages + s); };
-  auto bar_s_full = [&](int i) { return bars + 16u + 16u * C::kStages + 8u * i; };
-  auto bar_p_ready = [&](int i) { return bars + 32u + 16u * C::kStages + 8u * i; };
-  auto bar_o_final = [&](int i) { return bars + 48u + 16u * C::kStages + 8u * i; };
-  const uint32_t bar_qk_ready = bars + 64u + 16u * C::kStages;          // fp32: Q and K_0 split
+  auto bar_kv_empty = [&](int s) { return bars + 16u + 8u * (kSt + s); };
+  auto bar_s_full = [&](int i) { return bars + 16u + 16u * kSt + 8u * i; };
+  auto bar_p_ready = [&](int i) { return bars + 32u + 16u * kSt + 8u * i; };
+  auto bar_o_final = [&](int i) { return bars + 48u + 16u * kSt + 8u * i; };
+  const uint32_t bar_qk_ready = bars + 64u + 16u * kSt;          // fp32: Q and K_0 split
   uint8_t* const gbars = gbase + (bars - base);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 72 + 16 * C::kStages);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 76 + 16 * C::kStages);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 72 + 16 * kSt);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 76 + 16 * kSt);
+  // block-sparse: the key tiles either query tile may see, ascending, after the
+  // barriers; entry = tile | (visible to tile 0) << 14 | (visible to tile 1) << 15
+  int* const list_count = reinterpret_cast<int*>(gbars + 480);       // [0] all, [1] group 0's prefix
+  uint16_t* const tile_list = reinterpret_cast<uint16_t*>(gbars + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -177,7 +183,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   int nkv[2];
   nkv[0] = p.causal ? qt[0] + 1 : nq;
   nkv[1] = (C::kPingPong && qt[1] < nq) ? (p.causal ? qt[1] + 1 : nq) : 0;
-  const int nmax = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
+  const bool has_tile[2] = {true, C::kPingPong && qt[1] < nq};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -187,12 +193,39 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(bar_p_ready(i), C::kPingPong ? 129 : 128);   // + the ring watcher (bf16)
       mbar_init(bar_o_final(i), 1);
     }
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
     mbar_init(bar_qk_ready, 128);
     fence_mbar_init();
+  }
+  if constexpr (kSparse) {
+    if (warp == 0) {
+      // compact the key tiles visible to either query tile (within its causal
+      // range) into the list, 32 candidates per round
+      const unsigned char* m0 = p.mask + static_cast<long long>(b) * p.mask_sb +
+                                static_cast<long long>(h) * p.mask_sh + static_cast<long long>(qt[0]) * p.mask_nt;
+      const unsigned char* m1 = m0 + p.mask_nt;
+      const int nscan = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
+      int count = 0, count0 = 0;
+      for (int base0 = 0; base0 < nscan; base0 += 32) {
+        const int jj = base0 + lane;
+        const bool a0 = jj < nkv[0] && m0[jj] != 0;
+        const bool a1 = jj < nkv[1] && m1[jj] != 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, a0 || a1);
+        const unsigned bal0 = __ballot_sync(0xffffffffu, (a0 || a1) && jj < nkv[0]);
+        if (a0 || a1)
+          tile_list[count + __popc(bal & ((1u << lane) - 1u))] =
+              static_cast<uint16_t>(jj | (a0 ? 1 << 14 : 0) | (a1 ? 1 << 15 : 0));
+        count += __popc(bal);
+        count0 += __popc(bal0);
+      }
+      if (lane == 0) {
+        list_count[0] = count;
+        list_count[1] = count0;
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
@@ -203,6 +236,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+  if constexpr (kSparse) {
+    // steps now index the list; group 0 takes the prefix inside its causal range
+    nkv[0] = list_count[1];
+    nkv[1] = has_tile[1] ? list_count[0] : 0;
+  }
+  const int nmax = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
+  // key tile of step j
+  auto kv_tile = [&](int j) -> int { return kSparse ? (tile_list[j] & 0x3FFF) : j; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -217,14 +258,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           tma_load_3d(s_q[i] + bx * kBoxBytes, &map_q, bar_q_full(i), bx * C::kChunk, qt[i] * kBM, bh);
       }
       for (int c = 0; c < 2 * nmax; ++c) {
-        const int slot = c % C::kStages;
-        const uint32_t round = c / C::kStages;
+        const int slot = c % kSt;
+        const uint32_t round = c / kSt;
         if (!mbar_wait(bar_kv_empty(slot), (round & 1u) ^ 1u, abort_flag, deadline)) break;
         mbar_arrive_expect_tx(bar_kv_full(slot), C::kTileBytes);
         const CUtensorMap* m = (c & 1) ? &map_v : &map_k;
         const uint32_t dst = s_kv + slot * C::kTileBytes;
         for (int bx = 0; bx < C::kNBox; ++bx)
-          tma_load_3d(dst + bx * kBoxBytes, m, bar_kv_full(slot), bx * C::kChunk, (c >> 1) * kBN, bh_kv);
+          tma_load_3d(dst + bx * kBoxBytes, m, bar_kv_full(slot), bx * C::kChunk, kv_tile(c >> 1) * kBN, bh_kv);
       }
     }
     __syncwarp();
@@ -239,15 +280,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         if (nkv[i] > 0) ok = mbar_wait(bar_q_full(i), 0, abort_flag, deadline);
       int c = 0;
       auto take = [&](uint32_t& slot_addr, int& slot) -> bool {
-        slot = c % C::kStages;
-        const bool r = mbar_wait(bar_kv_full(slot), (c / C::kStages) & 1, abort_flag, deadline);
+        slot = c % kSt;
+        const bool r = mbar_wait(bar_kv_full(slot), (c / kSt) & 1, abort_flag, deadline);
         slot_addr = s_kv + slot * C::kTileBytes;
         ++c;
         return r;
       };
       uint32_t sk = 0;
       int kslot = 0;
-      if (ok) ok = take(sk, kslot);
+      if (ok && nmax > 0) ok = take(sk, kslot);     // (a block-sparse CTA may have no key tile)
       if (ok && C::kTf32) ok = mbar_wait(bar_qk_ready, 0, abort_flag, deadline);
       if (ok) {
         tc_fence_after();
@@ -264,11 +305,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const bool has_next = j + 1 < nmax;
         if constexpr (C::kPingPong) {
           // residency of V_j and K_{j+1} is folded into the P-ready barriers
-          vslot = c % C::kStages;
+          vslot = c % kSt;
           sv = s_kv + vslot * C::kTileBytes;
           ++c;
           if (has_next) {
-            knext = c % C::kStages;
+            knext = c % kSt;
             sk_next = s_kv + knext * C::kTileBytes;
             ++c;
           }
@@ -305,7 +346,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       // parity waits only tell phase k from phase k-1: observe every phase of
       // every slot in order, starting with K_0 (load 0), which only the
       // issuer needs
-      bool ok = mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
+      bool ok = nmax == 0 || mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
       auto hand_p = [&](int i, int j) {
         // arrive for phase j only once phase j-1 has completed
         if (j > 0) ok = mbar_wait(bar_p_ready(i), (j - 1) & 1, abort_flag, deadline);
@@ -314,10 +355,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       for (int j = 0; j < nmax && ok; ++j) {
         // step j reads V_j (load 2j+1) and, if there is a next tile, K_{j+1} (load 2j+2)
         const int cv = 2 * j + 1;
-        ok = mbar_wait(bar_kv_full(cv % C::kStages), (cv / C::kStages) & 1, abort_flag, deadline);
+        ok = mbar_wait(bar_kv_full(cv % kSt), (cv / kSt) & 1, abort_flag, deadline);
         if (ok && j + 1 < nmax) {
           const int ck = 2 * j + 2;
-          ok = mbar_wait(bar_kv_full(ck % C::kStages), (ck / C::kStages) & 1, abort_flag, deadline);
+          ok = mbar_wait(bar_kv_full(ck % kSt), (ck / kSt) & 1, abort_flag, deadline);
         }
         if (ok && L == 1 && j < nkv[0]) hand_p(0, j);
         // S_L(j) done: it was issued after every MMA that reads K_j or V_{j-1},
@@ -326,8 +367,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         // phases ahead of the parity asked for.
         if (ok) ok = mbar_wait(bar_s_full(L), j & 1, abort_flag, deadline);
         if (ok) {
-          mbar_arrive(bar_kv_empty((2 * j) % C::kStages));
-          if (j > 0) mbar_arrive(bar_kv_empty((2 * j - 1) % C::kStages));
+          mbar_arrive(bar_kv_empty((2 * j) % kSt));
+          if (j > 0) mbar_arrive(bar_kv_empty((2 * j - 1) % kSt));
         }
         if (ok) hand_p(L, j);
       }
@@ -378,9 +419,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
       // mask: causal diagonal tile and the ragged tail of the key range
       int lim = kBN;
-      const int kv0 = j * kBN;
-      if (p.causal && j == qt[g]) lim = row + 1;
+      const int kvt = kv_tile(j);
+      const int kv0 = kvt * kBN;
+      if (p.causal && kvt == qt[g]) lim = row + 1;
       if (kv0 + kBN > p.N) lim = min(lim, p.N - kv0);
+      if (kSparse && !((tile_list[j] >> (14 + g)) & 1)) lim = 0;   // tile visible to the other query tile only
       if (lim < kBN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
@@ -437,8 +480,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       if constexpr (C::kTf32) {
         // V_j (load 2j+1 of the ring) -> V^T in K-major 128-byte-swizzled boxes
         const int cv = 2 * j + 1;
-        const int vslot = cv % C::kStages;
-        bool vok = mbar_wait(bar_kv_full(vslot), (cv / C::kStages) & 1, abort_flag, deadline);
+        const int vslot = cv % kSt;
+        bool vok = mbar_wait(bar_kv_full(vslot), (cv / kSt) & 1, abort_flag, deadline);
         vok = __all_sync(0xffffffffu, vok);
         if (!vok) { ok = false; break; }
         const uint32_t sv = s_kv + vslot * C::kTileBytes;
@@ -461,8 +504,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           // K_{j+1} (load 2j+2): split before the tensor core computes S_{j+1}. The
           // previous S, which read the low-part buffer, has completed.
           const int ck = 2 * j + 2;
-          const int kslot = ck % C::kStages;
-          bool kok = mbar_wait(bar_kv_full(kslot), (ck / C::kStages) & 1, abort_flag, deadline);
+          const int kslot = ck % kSt;
+          bool kok = mbar_wait(bar_kv_full(kslot), (ck / kSt) & 1, abort_flag, deadline);
           kok = __all_sync(0xffffffffu, kok);
           if (!kok) { ok = false; break; }
           split_tf32_row<D>(s_kv + kslot * C::kTileBytes, s_k_lo, row);
@@ -489,20 +532,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_arrive(bar_p_ready(g));
     }
     // ---------------------------------------------------------- epilogue
+    // A block-sparse query tile that sees no key tile at all skips the loop
+    // and writes O = 0, LSE = -inf; so does any row that saw no key (l = 0).
+    const bool empty = kSparse && has_tile[g] && n_kv == 0;
     if (ok) {
       ok = mbar_wait(bar_o_final(g), 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok || empty) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const uint32_t stage = s_q[g];     // Q tile no longer needed: all its MMAs completed
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(t_o + c0, o);
-        tmem_wait_ld();
-        reg_fence_x32(o);
+        if (!empty) {
+          tmem_ld_32x32b_x32(t_o + c0, o);
+          tmem_wait_ld();
+          reg_fence_x32(o);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
         if constexpr (C::kTf32) {
           const uint32_t box = stage + (c0 / 32) * kBoxBytes;
 #pragma unroll
@@ -534,7 +585,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         tma_store_commit();
         tma_store_wait_all0();
       }
-      if (q_row < p.N) p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m + log2f(l)) * kLn2;
+      if (q_row < p.N) p.lse[static_cast<size_t>(bh) * p.N + q_row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -549,17 +600,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kSparse>
 static cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
                           const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<T, D>;
+  // the block-sparse variant: one ring slot fewer, the tile list after the barriers
+  constexpr int kSmem = kSparse ? C::kSmemBytes - C::kTileBytes + 2 * kMaskMaxTiles : C::kSmemBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  fwd_kernel<T, D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  fwd_kernel<T, D, kSparse><<<grid, C::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -568,9 +622,15 @@ cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUte
   const int nq = (p.N + kBM - 1) / kBM;
   p.num_pairs = (dtype_bytes == 2) ? (nq + 1) / 2 : nq;    // query tiles per CTA: 2 (bf16) or 1 (fp32)
   const int grid = p.num_pairs * p.BH;
-  if (dtype_bytes == 2 && d == 128) return launch<__nv_bfloat16, 128>(mq, mk, mv, mo, p, grid, stream);
-  if (dtype_bytes == 2 && d == 64) return launch<__nv_bfloat16, 64>(mq, mk, mv, mo, p, grid, stream);
-  if (dtype_bytes == 4 && d == 64) return launch<float, 64>(mq, mk, mv, mo, p, grid, stream);
+  const bool sparse = p.mask != nullptr;
+  if (sparse && (dtype_bytes != 2 || nq > kMaskMaxTiles)) return cudaErrorInvalidValue;
+  if (dtype_bytes == 2 && d == 128)
+    return sparse ? launch<__nv_bfloat16, 128, true>(mq, mk, mv, mo, p, grid, stream)
+                  : launch<__nv_bfloat16, 128, false>(mq, mk, mv, mo, p, grid, stream);
+  if (dtype_bytes == 2 && d == 64)
+    return sparse ? launch<__nv_bfloat16, 64, true>(mq, mk, mv, mo, p, grid, stream)
+                  : launch<__nv_bfloat16, 64, false>(mq, mk, mv, mo, p, grid, stream);
+  if (dtype_bytes == 4 && d == 64) return launch<float, 64, false>(mq, mk, mv, mo, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

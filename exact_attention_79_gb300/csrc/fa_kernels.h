@@ -14,7 +14,13 @@ struct FwdParams {
   int causal;
   float scale_log2;                // scale * log2(e)
   unsigned long long timeout_ns;   // bound on every wait inside the kernel
+  // optional block mask (bf16 only): byte (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_nt + j]
+  // says whether query tile i may see key tile j (128 x 128 tiles); nullptr = dense
+  const unsigned char* mask;
+  long long mask_sb, mask_sh;
+  int mask_nt;                     // tiles per row = ceil(N / 128)
 };
+constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 
 // dtype_bytes: 2 = bf16 (tensor-core kind::f16), 4 = fp32 (kind::tf32).
 cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,

@@ -64,6 +64,23 @@ typedef enum {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/* Forward with a block mask, bf16 ("FlashAttention技术解析", section 6.2: whole
+ * blocks are skipped, as the causal mask skips the blocks above the diagonal).
+ * Same arguments and outputs as fa_fwd, plus a block mask over 128 x 128 tiles:
+ *   block_mask  device bytes; byte (b, h, i, j) at
+ *               block_mask[b * mask_stride_b + h * mask_stride_h + i * T + j],
+ *               T = ceil(N / 128), h the query head; nonzero = query tile i may
+ *               see key tile j. Strides are in bytes and may be 0 (one mask
+ *               broadcast over batches or heads); caller-owned, read only.
+ * Key j is visible to query i iff the (i/128, j/128) byte is nonzero and, when
+ * causal, j <= i. Key tiles no query tile of a CTA sees are never loaded or
+ * multiplied. A query row that sees no key gets O = 0 and lse = -inf.
+ * FA_ERR_INVALID_ARG for a null mask or negative strides; FA_ERR_UNSUPPORTED
+ * for N > 131072. */
+fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const unsigned char* block_mask, long long mask_stride_b, long long mask_stride_h,
+                             int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
 /* Forward, fp32 in and out (tf32 tensor-core products, fp32 softmax and
  * accumulation). Same arguments as fa_fwd with fp32 q, k, v, o; d must be 64
  * (FA_ERR_UNSUPPORTED otherwise). */
