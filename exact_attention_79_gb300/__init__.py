@@ -30,6 +30,9 @@ SIGNATURES = {
                     _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_deterministic": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                                   _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_bwd_blocksparse_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_bwd_blocksparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _LL, _LL,
+                                _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_preprocess": (_I, [_VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _VP]),
     "fa_bwd_dkdv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_dq": (_I, [_VP, _VP, _SZ, _I, _I, _I, _I, _I, _F, _VP]),
@@ -141,10 +144,11 @@ def bwd_workspace_bytes(B, Hq, Hkv, N, d):
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
-        deterministic=False):
+        deterministic=False, block_mask=None):
     """dQ, dK, dV of <O, dO> on the current stream (bf16 tensors, fp32 lse).
 
-    deterministic=True runs fa_bwd_deterministic (bit-reproducible, slower)."""
+    deterministic=True runs fa_bwd_deterministic (bit-reproducible, slower);
+    block_mask (as in fwd) runs fa_bwd_blocksparse."""
     import torch
     lib = load()
     B, Hq, Hkv, N, d = _shape(q, k)
@@ -153,12 +157,22 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     for t in (q, k, v, o, do):
         if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
             raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
-    nbytes = bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    if block_mask is not None and deterministic:
+        raise ValueError("the deterministic backward has no block-sparse form")
+    nbytes = (int(lib.fa_bwd_blocksparse_workspace_bytes(B, Hq, Hkv, N, d)) if block_mask is not None
+              else bwd_workspace_bytes(B, Hq, Hkv, N, d))
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if block_mask is not None:
+        mp, sb, sh = _mask_args(block_mask, B, Hq, N, q.device)
+        _check("fa_bwd_blocksparse", lib.fa_bwd_blocksparse(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), workspace.numel(), mp, sb, sh, B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+            _stream(q)))
+        return dq, dk, dv
     name = "fa_bwd_deterministic" if deterministic else "fa_bwd"
     _check(name, getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),

@@ -144,9 +144,10 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdWorkspace {
   size_t off_lse2, off_d, off_dq, total;   // off_dq: the bytes the deterministic backward needs
+  size_t off_count, off_list, total_sparse;  // block-sparse: per dK/dV CTA, its step count and step list
 };
 
-BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
+BwdWorkspace bwd_workspace(int B, int Hq, int Hkv, int N, int d) {
   const size_t BH = static_cast<size_t>(B) * Hq;
   const size_t NQP = static_cast<size_t>((N + 127) / 128) * 128;
   BwdWorkspace w;
@@ -154,18 +155,24 @@ BwdWorkspace bwd_workspace(int B, int Hq, int N, int d) {
   w.off_d = align256(BH * NQP * 4);
   w.off_dq = w.off_d + align256(BH * NQP * 4);
   w.total = w.off_dq + align256(BH * static_cast<size_t>(N) * d * 4);
+  const size_t ctas = (NQP / 128) * static_cast<size_t>(B) * Hkv;
+  const size_t G = static_cast<size_t>(Hq / (Hkv > 0 ? Hkv : 1));
+  w.off_count = w.total;
+  w.off_list = w.off_count + align256(ctas * 4);
+  w.total_sparse = w.off_list + align256(ctas * G * (NQP / 128) * 4);
   return w;
 }
 
 // Validates sizes and workspace, resolves the device, fills BwdParams. With
 // lse_d_only the workspace only has to hold the LSE and D parts.
 fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
-                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms, bool lse_d_only = false) {
+                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms, bool lse_d_only = false,
+                    const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0) {
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
-  const BwdWorkspace w = bwd_workspace(B, Hq, N, d);
+  const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, N, d);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-      workspace_bytes < (lse_d_only ? w.off_dq : w.total))
+      workspace_bytes < (mask ? w.total_sparse : (lse_d_only ? w.off_dq : w.total)))
     return FA_ERR_WORKSPACE;
   unsigned* status = nullptr;
   st = device_state(&status, num_sms);
@@ -185,6 +192,12 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   p->scale = scale;
   p->scale_log2 = scale * 1.4426950408889634f;
   p->timeout_ns = wait_limit_ns();
+  p->mask = mask;
+  p->mask_sb = mask_sb;
+  p->mask_sh = mask_sh;
+  p->mask_nt = (N + 127) / 128;
+  p->ws_count = mask ? reinterpret_cast<int*>(ws + w.off_count) : nullptr;
+  p->ws_list = mask ? reinterpret_cast<unsigned*>(ws + w.off_list) : nullptr;
   return FA_OK;
 }
 
@@ -194,7 +207,40 @@ extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
   if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK) return 0;
-  return bwd_workspace(B, Hq, N, d).total;
+  return bwd_workspace(B, Hq, Hkv, N, d).total;
+}
+
+size_t fa_bwd_blocksparse_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK || (N + 127) / 128 > fa::kMaskMaxTiles) return 0;
+  return bwd_workspace(B, Hq, Hkv, N, d).total_sparse;
+}
+
+fa_status fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             const unsigned char* block_mask, long long mask_stride_b, long long mask_stride_h,
+                             int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  if (!block_mask || mask_stride_b < 0 || mask_stride_h < 0) return FA_ERR_INVALID_ARG;
+  if ((N + 127) / 128 > fa::kMaskMaxTiles) return FA_ERR_UNSUPPORTED;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, false,
+                           block_mask, mask_stride_b, mask_stride_h);
+  if (st != FA_OK) return st;
+  fa::BwdMaps m;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv) ||
+      !make_map(&m.dqacc, p.ws_dq, 4, d, N, BHq))
+    return FA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_pre(d, o, dO, lse, p, num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_blocklist(p, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(d, m, p, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq(d, dq, p, num_sms, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,

@@ -139,7 +139,7 @@ struct BwdCfg {
   static_assert(kDqHalfBoxes * kBoxBytes <= kDsBytes && kDqHalfBoxes * kBoxBytes <= kTileBytes, "dQ staging");
 };
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(384, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -189,7 +189,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int nq = p.NQP / kBM;
   const int it0 = p.causal ? jt : 0;
   const int tiles_per_head = nq - it0;
-  const int nsteps = G * tiles_per_head;
+  // block-sparse: only the (head, query tile) steps the mask lets see this key
+  // tile, in the dense order, from the list bwd_blocklist_kernel compacted
+  const int nsteps = kSparse ? p.ws_count[blockIdx.x] : G * tiles_per_head;
+  const unsigned* const steps = kSparse ? p.ws_list + static_cast<size_t>(blockIdx.x) * G * nq : nullptr;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -222,8 +225,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
-  auto step_head = [&](int step) { return b * p.Hq + hk * G + step / tiles_per_head; };
-  auto step_tile = [&](int step) { return it0 + step % tiles_per_head; };
+  auto step_head = [&](int step) {
+    return b * p.Hq + hk * G + (kSparse ? static_cast<int>(steps[step] >> 16) : step / tiles_per_head);
+  };
+  auto step_tile = [&](int step) {
+    return kSparse ? static_cast<int>(steps[step] & 0xFFFFu) : it0 + step % tiles_per_head;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -289,8 +296,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mma_commit(bar_dp_full);
       };
-      bool ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline) && mbar_wait(bar_q_full(0), 0, abort_flag, deadline);
-      if (ok) {
+      // (a block-sparse key tile may have no step at all: dK = dV = 0)
+      bool ok = nsteps == 0 ||
+                (mbar_wait(bar_kv_full, 0, abort_flag, deadline) && mbar_wait(bar_q_full(0), 0, abort_flag, deadline));
+      if (ok && nsteps > 0) {
         tc_fence_after();
         issue_s(0);
         ok = mbar_wait(bar_do_full(0), 0, abort_flag, deadline);
@@ -373,7 +382,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // needs) included: without it, dO_2 could pass for landed while dO_0 was
     // still in flight.
     if (lane == 0) {
-      bool ok = mbar_wait(bar_do_full(0), 0, abort_flag, deadline);
+      bool ok = nsteps == 0 || mbar_wait(bar_do_full(0), 0, abort_flag, deadline);
       for (int step = 0; step + 1 < nsteps && ok; ++step) {
         const int sn = (step + 1) & 1;
         ok = mbar_wait(bar_do_full(sn), ((step + 1) >> 1) & 1, abort_flag, deadline);
@@ -518,6 +527,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // ---------------------------------------------------------- dK, dV epilogue
     if (ok) {
       ok = mbar_wait(bar_o_final, 0, abort_flag, deadline);
+      // with no step nothing waited for K and V, whose buffers stage dK and dV
+      // below: let their loads land first
+      if (nsteps == 0) ok = ok && mbar_wait(bar_kv_full, 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -532,9 +544,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
           uint32_t t[32];
-          tmem_ld_32x32b_x32(tbase + lane_off + col + c0, t);
-          tmem_wait_ld();
-          reg_fence_x32(t);
+          if (nsteps > 0) {
+            tmem_ld_32x32b_x32(tbase + lane_off + col + c0, t);
+            tmem_wait_ld();
+            reg_fence_x32(t);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) t[c] = 0u;
+          }
           const uint32_t bx = stg + (c0 / 64) * kBoxBytes;
           const int u0 = (c0 % 64) / 8;
 #pragma unroll
@@ -573,17 +590,61 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 }
 
 // ------------------------------------------------------------------ launch
-template <int D>
+template <int D, bool kSparse>
 static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = (p.NQP / kBN) * p.BHkv;
-  bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, m.dqacc, p);
+  bwd_dkdv_kernel<D, kSparse><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv,
+                                                                             m.dqacc, p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ block list
+// One warp per dK/dV CTA (key tile jt, batch b, KV head hk): compacts the
+// (head in group, query tile) steps whose mask byte lets the query tile see
+// key tile jt, in the order the dense kernel visits them.
+__global__ void __launch_bounds__(256) bwd_blocklist_kernel(BwdParams p) {
+  const int cta = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  const int nqt = p.NQP / kBM;
+  if (cta >= nqt * p.BHkv) return;
+  const int jt = cta / p.BHkv, bhkv = cta % p.BHkv;
+  const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int it0 = p.causal ? jt : 0;
+  const int per_head = nqt - it0;
+  const int total = G * per_head;
+  unsigned* const list = p.ws_list + static_cast<size_t>(cta) * G * nqt;
+  int count = 0;
+  for (int base = 0; base < total; base += 32) {
+    const int s = base + lane;
+    bool a = false;
+    unsigned e = 0;
+    if (s < total) {
+      const int hl = s / per_head, it = it0 + s % per_head;
+      const long long off = static_cast<long long>(b) * p.mask_sb + static_cast<long long>(hk * G + hl) * p.mask_sh +
+                            static_cast<long long>(it) * p.mask_nt + jt;
+      a = p.mask[off] != 0;
+      e = static_cast<unsigned>(it) | (static_cast<unsigned>(hl) << 16);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, a);
+    if (a) list[count + __popc(bal & ((1u << lane) - 1u))] = e;
+    count += __popc(bal);
+  }
+  if (lane == 0) p.ws_count[cta] = count;
+}
+
+cudaError_t launch_bwd_blocklist(const BwdParams& p, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(p.NQP / kBM) * p.BHkv;
+  const int blocks = static_cast<int>((warps + 7) / 8);
+  bwd_blocklist_kernel<<<blocks, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -598,8 +659,9 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* ls
 }
 
 cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_dkdv_d<128>(m, p, stream);
-  if (d == 64) return launch_dkdv_d<64>(m, p, stream);
+  const bool sparse = p.mask != nullptr;
+  if (d == 128) return sparse ? launch_dkdv_d<128, true>(m, p, stream) : launch_dkdv_d<128, false>(m, p, stream);
+  if (d == 64) return sparse ? launch_dkdv_d<64, true>(m, p, stream) : launch_dkdv_d<64, false>(m, p, stream);
   return cudaErrorInvalidValue;
 }
 

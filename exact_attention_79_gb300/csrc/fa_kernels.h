@@ -36,6 +36,14 @@ struct BwdParams {
   int causal;
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  // optional block mask, laid out as in FwdParams; nullptr = dense. With a
+  // mask, ws_count[c] and ws_list[c * G * NQP/128 ...] hold the active steps
+  // (query tile | head-in-group << 16) of dK/dV CTA c = key tile * BHkv + b*Hkv + hk.
+  const unsigned char* mask;
+  long long mask_sb, mask_sh;
+  int mask_nt;
+  int* ws_count;
+  unsigned* ws_list;
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;
@@ -47,6 +55,8 @@ struct BwdMaps {
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* lse, const BwdParams& p, int num_sms,
                            cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream);
+// block-sparse backward: compacts each dK/dV CTA's active (head, query tile) steps
+cudaError_t launch_bwd_blocklist(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream);
 
 // Deterministic backward after launch_bwd_pre: the dK/dV pass and the dQ pass

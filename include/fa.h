@@ -116,6 +116,22 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
                                float scale, void* stream);
 
+/* Backward with the same block mask as fa_fwd_blocksparse (same layout, same
+ * visibility rule), bf16; the forward's O and lse must come from
+ * fa_fwd_blocksparse with that mask. Outputs and numerics as fa_bwd; a (query
+ * tile, key tile) pair the mask hides costs nothing, and gradients of rows that
+ * see no key are zero. The workspace must hold
+ * fa_bwd_blocksparse_workspace_bytes(B, Hq, Hkv, N, d) bytes (fa_bwd's parts
+ * plus each dK/dV block's list of visible query steps), 256-byte aligned,
+ * caller-owned, scratch after the call. FA_ERR_INVALID_ARG for a null mask or
+ * negative strides, FA_ERR_WORKSPACE for a short or misaligned workspace,
+ * FA_ERR_UNSUPPORTED for N > 131072. */
+size_t fa_bwd_blocksparse_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+fa_status fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             const unsigned char* block_mask, long long mask_stride_b, long long mask_stride_h,
+                             int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
 /* The three phases fa_bwd runs, in this order on one stream, exposed for
  * callers that schedule or time them separately. Arguments mean what they
  * mean for fa_bwd; the workspace carries state from one phase to the next.
