@@ -21,6 +21,17 @@ class Workload:
     backward: bool      # whether the workload includes the backward pass
     q_mult: float = 1.0  # Q is multiplied by this before rounding (logit stress run)
     sampled_rows: int = 0  # >0: check only this many seeded query/key rows per head
+    block_window: int = 0  # >0: block-sparse local attention, query tile i sees key tiles i-W+1 .. i
+
+    def block_mask(self):
+        """[1, 1, T, T] booleans of the local-window block mask (None when dense)."""
+        if not self.block_window:
+            return None
+        import numpy as np
+        T = (self.N + 127) // 128
+        i = np.arange(T)[:, None]
+        j = np.arange(T)[None, :]
+        return ((j <= i) & (j > i - self.block_window))[None, None]
 
     @property
     def scale(self) -> float:
@@ -28,6 +39,14 @@ class Workload:
 
     @property
     def flops_fwd(self) -> float:
+        if self.block_window:
+            # visible 128 x 128 blocks: full off the diagonal, half on it (the
+            # dense causal count 4 B H N^2 d / 2 is the same rule over all blocks)
+            m = self.block_mask()[0, 0]
+            T = m.shape[0]
+            diag = int(m[range(T), range(T)].sum())
+            blocks = int(m.sum()) - diag + (0.5 * diag if self.causal else diag)
+            return 4.0 * self.B * self.Hq * 128 * 128 * self.d * blocks
         f = 4.0 * self.B * self.Hq * self.N * self.N * self.d
         return f / 2 if self.causal else f
 
@@ -40,6 +59,7 @@ class Workload:
             "workload": self.name, "dtype": self.dtype, "B": self.B, "Hq": self.Hq,
             "Hkv": self.Hkv, "N": self.N, "d": self.d, "causal": self.causal,
             "scale": self.scale, "backward": self.backward,
+            **({"block_window_tiles": self.block_window} if self.block_window else {}),
         }
 
 
@@ -55,6 +75,8 @@ WORKLOADS = {
     "bf16_h16_n8192_d128_causal_fwdbwd": Workload("bf16_h16_n8192_d128_causal_fwdbwd", "bf16", 1, 16, 16, 8192, 128, True, True),
     # long sequence forward + backward, 8 heads, N=65536, causal, 256 sampled rows per head
     "bf16_h8_n65536_d128_causal_fwdbwd": Workload("bf16_h8_n65536_d128_causal_fwdbwd", "bf16", 1, 8, 8, 65536, 128, True, True, sampled_rows=256),
+    # block-sparse local attention (a window of 16 key tiles = 2048 keys, causal), 16 heads, N=32768
+    "bf16_h16_n32768_d128_local16_fwdbwd": Workload("bf16_h16_n32768_d128_local16_fwdbwd", "bf16", 1, 16, 16, 32768, 128, True, True, block_window=16),
 }
 
 # Tolerances against the double-precision oracle on the same rounded inputs.

@@ -140,13 +140,15 @@ def backward(q, k, v, do, causal, scale, block_mask=None):
     return o, lse, dq, dk, dv
 
 
-def forward_rows(q, k, v, causal, scale, rows):
+def forward_rows(q, k, v, causal, scale, rows, block_mask=None):
     """O and LSE for selected query rows only (each row costs O(N d)).
 
-    rows: int array [B, Hq, R] of query indices per head.
+    rows: int array [B, Hq, R] of query indices per head; block_mask as in
+    `forward`.
     Returns (o [B,Hq,R,d], lse [B,Hq,R]).
     """
     B, Hq, Hkv, N, d, G = _check(q, k, v)
+    bm = _block_mask_bh(block_mask, B, Hq, N)
     R = rows.shape[2]
     o = np.empty((B, Hq, R, d))
     lse = np.empty((B, Hq, R))
@@ -154,7 +156,7 @@ def forward_rows(q, k, v, causal, scale, rows):
         for h in range(Hq):
             hk = h // G
             r = rows[b, h]
-            s = _scores(q[b, h, r], k[b, hk], scale, causal, r)
+            s = _scores(q[b, h, r], k[b, hk], scale, causal, r, None if bm is None else bm[b, h])
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
     return o, lse

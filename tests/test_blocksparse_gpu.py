@@ -182,3 +182,44 @@ def test_blocksparse_bwd_all_ones_equals_dense_dkdv(fa):
     fa.check_device_status()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert float((a[0].float() - b[0].float()).abs().max()) < 1e-2
+
+
+def test_blocksparse_local_window_workload_sampled_rows(fa):
+    """The block-sparse bench workload at full size (16 heads, N = 32768, a
+    causal window of 16 key tiles, the mask broadcast over heads as bench.py
+    passes it): 256 seeded query rows per head against the oracle."""
+    w = configs.WORKLOADS["bf16_h16_n32768_d128_local16_fwdbwd"]
+    t = inputs.make_workload_inputs(w, with_grad=False)
+    m = w.block_mask()
+    dev = torch.device("cuda:0")
+    q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
+    mt = torch.tensor(m, dtype=torch.uint8, device=dev)
+    o, lse = fa.fwd(q, k, v, causal=True, scale=w.scale, block_mask=mt)
+    fa.check_device_status()
+    rows = inputs.sample_rows(w.B, w.Hq, w.N, 256, seed=1)
+    f = {n: inputs.to_f64(t[n]) for n in ("q", "k", "v")}
+    ro, rl = oracle.forward_rows(f["q"], f["k"], f["v"], True, w.scale, rows, block_mask=m)
+    bi = np.arange(w.B)[:, None, None]
+    hi = np.arange(w.Hq)[None, :, None]
+    check_fwd(o.float().cpu().numpy()[bi, hi, rows], lse.cpu().numpy()[bi, hi, rows], ro, rl)
+
+
+def test_blocksparse_local_window_workload_bwd_repeatable(fa):
+    """The same workload's backward at full size: two launches give
+    bit-identical dK and dV, finite and bounded gradients, and dQ equal up to
+    the order of its fp32 reductions; key tiles are visited by at most 16
+    query tiles, so every dK/dV block has a short, varied step list."""
+    w = configs.WORKLOADS["bf16_h16_n32768_d128_local16_fwdbwd"]
+    t = inputs.make_workload_inputs(w, with_grad=True)
+    dev = torch.device("cuda:0")
+    g = {n: x.to(dev) for n, x in t.items()}
+    mt = torch.tensor(w.block_mask(), dtype=torch.uint8, device=dev)
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=True, scale=w.scale, block_mask=mt)
+    a = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=w.scale, block_mask=mt)
+    b = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=w.scale, block_mask=mt)
+    fa.check_device_status()
+    for x in a:
+        xf = x.float()
+        assert bool(torch.isfinite(xf).all()) and float(xf.abs().max()) < 1e3
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert float((a[0].float() - b[0].float()).abs().max()) < 1e-2

@@ -472,3 +472,16 @@ def test_block_mask_empty_rows():
     other = [r for r in range(N) if not 128 <= r < 256]
     np.testing.assert_allclose(dq[:, 0, other], dq_ref[:, 0, other], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dq[:, 1], dq_ref[:, 1], rtol=1e-12, atol=1e-13)
+
+
+def test_block_mask_rows_mode_matches_full():
+    """forward_rows with a block mask gives the same rows as forward."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 300, 8
+    q, k, v = rand_qkv(B, Hq, Hkv, N, d, seed=47)
+    bm = _block_mask(B, Hq, 3, 0.5, seed=48)
+    o, lse = oa.forward(q, k, v, True, 0.2, block_mask=bm)
+    rows = np.array([[[0, 5, 130, 299]] * Hq])
+    ro, rl = oa.forward_rows(q, k, v, True, 0.2, rows, block_mask=bm)
+    for h in range(Hq):
+        np.testing.assert_array_equal(ro[0, h], o[0, h, rows[0, h]])
+        np.testing.assert_array_equal(rl[0, h], lse[0, h, rows[0, h]])
