@@ -11,8 +11,11 @@ Query head h reads key/value head h // G (grouped-query attention; the
 Llama-2-70B-shaped workload maps 64 query heads onto 8 KV heads this way).
 
 Causal convention: key j is visible to query i iff j <= i (the pages skip the
-blocks whose key index exceeds the query index; one N for queries and keys, so
-there is no top-left / bottom-right ambiguity and no query row is fully masked).
+blocks whose key index exceeds the query index). `forward`, `backward` and
+`forward_rows` also take keys of another length Nk than the Nq queries
+(k, v: [B, Hkv, Nk, d]); the queries are then the last Nq positions of the Nk
+(bottom-right alignment): key j is visible to query i iff j <= i + (Nk - Nq),
+so with Nq > Nk the first Nq - Nk query rows see no key.
 
 A library matmul serves as the inner-product step. Rows are independent, so
 computing several whole rows at once is not a change of arithmetic: no row's
@@ -41,18 +44,32 @@ def _check(q, k, v):
     return B, Hq, Hkv, N, d, Hq // Hkv
 
 
-def _scores(qh, kh, scale, causal, row_index, block_mask_bh=None):
+def _check_qk(q, k, v):
+    """As _check, but k and v may hold Nk != Nq positions."""
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, Hq, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if Hkv <= 0 or Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return B, Hq, Hkv, Nq, Nk, d, Hq // Hkv
+
+
+def _scores(qh, kh, scale, causal, row_index, block_mask_bh=None, off=0):
     """S = scale * q k^T for the given query rows against all keys, with the
     causal mask applied as -inf (definition; blogweb.cn section 1).
 
-    qh: [R, d] query rows whose absolute indices are row_index [R]; kh: [N, d].
+    qh: [R, d] query rows whose absolute indices are row_index [R]; kh: [Nk, d].
+    Causal: key j visible to query i iff j <= i + off, off = Nk - Nq.
     block_mask_bh: optional [nq, nk] booleans; key j is visible to query i only
-    if block_mask_bh[i // BLOCK, j // BLOCK] (and j <= i when causal).
+    if block_mask_bh[i // BLOCK, j // BLOCK] (and the causal rule holds).
     """
     s = scale * (qh @ kh.T)
     key_index = np.arange(kh.shape[0])
     if causal:
-        s = np.where(key_index[None, :] <= row_index[:, None], s, -np.inf)
+        s = np.where(key_index[None, :] <= row_index[:, None] + off, s, -np.inf)
     if block_mask_bh is not None:
         allowed = np.asarray(block_mask_bh, dtype=bool)[row_index[:, None] // BLOCK, key_index[None, :] // BLOCK]
         s = np.where(allowed, s, -np.inf)
@@ -90,7 +107,9 @@ def forward(q, k, v, causal, scale, block_mask=None):
     booleans broadcastable to [B, Hq, ceil(N/128), ceil(N/128)] (see _scores).
     Returns (o [B,Hq,N,d], lse [B,Hq,N]).
     """
-    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    B, Hq, Hkv, N, Nk, d, G = _check_qk(q, k, v)
+    if block_mask is not None and Nk != N:
+        raise ValueError("block masks need Nq == Nk")
     bm = _block_mask_bh(block_mask, B, Hq, N)
     o = np.empty((B, Hq, N, d))
     lse = np.empty((B, Hq, N))
@@ -98,7 +117,7 @@ def forward(q, k, v, causal, scale, block_mask=None):
     for b in range(B):
         for h in range(Hq):
             hk = h // G
-            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h])
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h], Nk - N)
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
     return o, lse
@@ -117,18 +136,20 @@ def backward(q, k, v, do, causal, scale, block_mask=None):
     nothing to dK or dV.
     Returns (o, lse, dq, dk, dv).
     """
-    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    B, Hq, Hkv, N, Nk, d, G = _check_qk(q, k, v)
+    if block_mask is not None and Nk != N:
+        raise ValueError("block masks need Nq == Nk")
     bm = _block_mask_bh(block_mask, B, Hq, N)
     o = np.empty((B, Hq, N, d))
     lse = np.empty((B, Hq, N))
     dq = np.empty((B, Hq, N, d))
-    dk = np.zeros((B, Hkv, N, d))
-    dv = np.zeros((B, Hkv, N, d))
+    dk = np.zeros((B, Hkv, Nk, d))
+    dv = np.zeros((B, Hkv, Nk, d))
     rows = np.arange(N)
     for b in range(B):
         for h in range(Hq):
             hk = h // G
-            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h])
+            s = _scores(q[b, h], k[b, hk], scale, causal, rows, None if bm is None else bm[b, h], Nk - N)
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
             D = (do[b, h] * o[b, h]).sum(axis=1)
@@ -147,7 +168,9 @@ def forward_rows(q, k, v, causal, scale, rows, block_mask=None):
     `forward`.
     Returns (o [B,Hq,R,d], lse [B,Hq,R]).
     """
-    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    B, Hq, Hkv, N, Nk, d, G = _check_qk(q, k, v)
+    if block_mask is not None and Nk != N:
+        raise ValueError("block masks need Nq == Nk")
     bm = _block_mask_bh(block_mask, B, Hq, N)
     R = rows.shape[2]
     o = np.empty((B, Hq, R, d))
@@ -156,7 +179,7 @@ def forward_rows(q, k, v, causal, scale, rows, block_mask=None):
         for h in range(Hq):
             hk = h // G
             r = rows[b, h]
-            s = _scores(q[b, h, r], k[b, hk], scale, causal, r, None if bm is None else bm[b, h])
+            s = _scores(q[b, h, r], k[b, hk], scale, causal, r, None if bm is None else bm[b, h], Nk - N)
             p, lse[b, h] = _softmax_rows(s)
             o[b, h] = p @ v[b, hk]
     return o, lse

@@ -336,12 +336,15 @@ def _planted(monkeypatch, kind):
     real_scores = oa._scores
     real_softmax = oa._softmax_rows
     if kind == "drop_scale":
-        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None: real_scores(qh, kh, 1.0, c, r, bm))
+        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None, off=0: real_scores(qh, kh, 1.0, c, r, bm,
+                                                                                               off))
     elif kind == "block_mask_transposed":
-        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None: real_scores(
-            qh, kh, s, c, r, None if bm is None else np.swapaxes(bm, 0, 1)))
+        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None, off=0: real_scores(
+            qh, kh, s, c, r, None if bm is None else np.swapaxes(bm, 0, 1), off))
+    elif kind == "causal_top_left":
+        monkeypatch.setattr(oa, "_scores", lambda qh, kh, s, c, r, bm=None, off=0: real_scores(qh, kh, s, c, r, bm, 0))
     elif kind == "mask_strict":
-        def f(qh, kh, s, causal, r, bm=None):
+        def f(qh, kh, s, causal, r, bm=None, off=0):
             out = s * (qh @ kh.T)
             if causal:
                 out = np.where(np.arange(kh.shape[0])[None, :] < r[:, None], out, -np.inf)
@@ -362,7 +365,8 @@ def _planted(monkeypatch, kind):
         monkeypatch.setattr(oa, "_softmax_rows", g)
 
 
-@pytest.mark.parametrize("kind", ["drop_scale", "mask_strict", "lse_log2", "no_max_shift", "block_mask_transposed"])
+@pytest.mark.parametrize("kind", ["drop_scale", "mask_strict", "lse_log2", "no_max_shift", "block_mask_transposed",
+                                  "causal_top_left"])
 def test_pins_fail_on_planted_mistakes(monkeypatch, kind):
     """Each planted mistake must break at least one of the pins above."""
     _planted(monkeypatch, kind)
@@ -373,6 +377,7 @@ def test_pins_fail_on_planted_mistakes(monkeypatch, kind):
         lambda: test_single_key_gives_that_value_row(),
         lambda: test_zero_query_is_uniform_average(True),
         lambda: test_block_mask_matches_torch_sdpa(False),
+        lambda: test_kv_length_matches_torch_sdpa(200, 300, True),
     ]
     for c in checks:
         try:
@@ -483,5 +488,67 @@ def test_block_mask_rows_mode_matches_full():
     rows = np.array([[[0, 5, 130, 299]] * Hq])
     ro, rl = oa.forward_rows(q, k, v, True, 0.2, rows, block_mask=bm)
     for h in range(Hq):
+        np.testing.assert_array_equal(ro[0, h], o[0, h, rows[0, h]])
+        np.testing.assert_array_equal(rl[0, h], lse[0, h, rows[0, h]])
+
+
+# ---------------------------------------------------------------- Nq != Nk
+@pytest.mark.parametrize("Nq,Nk,causal", [(200, 300, True), (200, 300, False), (300, 200, True), (1, 257, True)])
+def test_kv_length_matches_torch_sdpa(Nq, Nk, causal):
+    """Queries as the last Nq of Nk positions (bottom-right causal): forward,
+    LSE and gradients against torch float64 scaled_dot_product_attention with
+    the explicit element mask j <= i + Nk - Nq. Rows that see no key (Nq > Nk)
+    are compared to the oracle's convention O = 0, LSE = -inf, dQ = 0."""
+    B, Hq, Hkv, d = 1, 4, 2, 8
+    rng = np.random.default_rng(Nq * 1000 + Nk)
+    q = rng.standard_normal((B, Hq, Nq, d))
+    k = rng.standard_normal((B, Hkv, Nk, d))
+    v = rng.standard_normal((B, Hkv, Nk, d))
+    do = rng.standard_normal((B, Hq, Nq, d))
+    o, lse, dq, dk, dv = oa.backward(q, k, v, do, causal, 0.3)
+    allowed = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        allowed = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    seen = allowed.any(axis=1)
+    G = Hq // Hkv
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    kk = tk.repeat_interleave(G, dim=1)
+    vv = tv.repeat_interleave(G, dim=1)
+    am = torch.tensor(allowed)
+    am_safe = am | torch.tensor(~seen)[:, None]          # keep torch finite on rows that see nothing
+    to = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, attn_mask=am_safe, scale=0.3)
+    to = to * torch.tensor(seen, dtype=to.dtype)[:, None]
+    to.backward(torch.tensor(do))
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=1e-10, atol=1e-12)
+    s = 0.3 * torch.einsum("bhid,bhjd->bhij", tq.detach(), kk.detach()).masked_fill(~am, float("-inf"))
+    tl = torch.logsumexp(s, dim=-1).numpy()
+    np.testing.assert_allclose(lse[..., seen], tl[..., seen], rtol=1e-10, atol=1e-12)
+    assert np.all(np.isneginf(lse[..., ~seen])) and np.all(dq[:, :, ~seen] == 0)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_single_query_decoding_sees_every_key():
+    """One query at the end of Nk keys, causal, sees all of them: the same as
+    the non-causal result (a closed form of the bottom-right rule)."""
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 2, 1, 8))
+    k = rng.standard_normal((1, 2, 77, 8))
+    v = rng.standard_normal((1, 2, 77, 8))
+    a = oa.forward(q, k, v, True, 0.5)
+    b = oa.forward(q, k, v, False, 0.5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_kv_length_rows_mode_matches_full():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 2, 150, 8))
+    k = rng.standard_normal((1, 1, 400, 8))
+    v = rng.standard_normal((1, 1, 400, 8))
+    o, lse = oa.forward(q, k, v, True, 0.4)
+    rows = np.array([[[0, 7, 149]] * 2])
+    ro, rl = oa.forward_rows(q, k, v, True, 0.4, rows)
+    for h in range(2):
         np.testing.assert_array_equal(ro[0, h], o[0, h, rows[0, h]])
         np.testing.assert_array_equal(rl[0, h], lse[0, h, rows[0, h]])
