@@ -24,6 +24,9 @@ _LL = ctypes.c_longlong
 SIGNATURES = {
     "fa_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fwd_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_bwd_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                       _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_blocksparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _LL, _LL, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
@@ -112,7 +115,9 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
     q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; bf16 (fa_fwd) or fp32 (fa_fwd_f32)
     contiguous CUDA tensors. block_mask (bf16 only): uint8/bool
     [B or 1, Hq or 1, T, T], T = ceil(N/128), nonzero where query tile i may
-    see key tile j (fa_fwd_blocksparse). Returns (o like q, lse fp32 [B, Hq, N])."""
+    see key tile j (fa_fwd_blocksparse). k and v may hold another number of
+    positions Nk than q (bf16, fa_fwd_kv: the queries are the last N of Nk
+    positions for the causal rule). Returns (o like q, lse fp32 [B, Hq, N])."""
     import torch
     lib = load()
     B, Hq, Hkv, N, d = _shape(q, k)
@@ -123,6 +128,13 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
             raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    Nk = k.shape[2]
+    if Nk != N:
+        if q.dtype != torch.bfloat16 or block_mask is not None:
+            raise ValueError("keys of another length need bf16 inputs and no block mask")
+        _check("fa_fwd_kv", lib.fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, Nk, d,
+                                          int(bool(causal)), float(scale), _stream(q)))
+        return o, lse
     if block_mask is not None:
         if q.dtype != torch.bfloat16:
             raise ValueError("block masks need bf16 inputs")
@@ -159,6 +171,9 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
             raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
     if block_mask is not None and deterministic:
         raise ValueError("the deterministic backward has no block-sparse form")
+    Nk = k.shape[2]
+    if Nk != N and (deterministic or block_mask is not None):
+        raise ValueError("keys of another length: only the default backward")
     nbytes = (int(lib.fa_bwd_blocksparse_workspace_bytes(B, Hq, Hkv, N, d)) if block_mask is not None
               else bwd_workspace_bytes(B, Hq, Hkv, N, d))
     if workspace is None:
@@ -166,6 +181,11 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if Nk != N:
+        _check("fa_bwd_kv", lib.fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                          _ptr(dv), _ptr(workspace), workspace.numel(), B, Hq, Hkv, N, Nk, d,
+                                          int(bool(causal)), float(scale), _stream(q)))
+        return dq, dk, dv
     if block_mask is not None:
         mp, sb, sh = _mask_args(block_mask, B, Hq, N, q.device)
         _check("fa_bwd_blocksparse", lib.fa_bwd_blocksparse(

@@ -108,24 +108,29 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
 
 fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, int N, int d, int causal, float scale, void* stream,
-                     const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0) {
+                     const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0,
+                     int Nk = -1) {
+  if (Nk < 0) Nk = N;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
   if (elt == 4 && d != 64) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = device_state(&status);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-  if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, N, BHkv) || !make_map(&mv, v, elt, d, N, BHkv) ||
-      !make_map(&mo, o, elt, d, N, BHq))
+  if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, Nk, BHkv) ||
+      !make_map(&mv, v, elt, d, Nk, BHkv) || !make_map(&mo, o, elt, d, N, BHq))
     return FA_ERR_CUDA;
   fa::FwdParams p{};
   p.lse = lse;
   p.status = status;
   p.N = N;
+  p.Nk = Nk;
+  p.causal_off = Nk - N;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.BH = static_cast<int>(BHq);
@@ -167,9 +172,12 @@ BwdWorkspace bwd_workspace(int B, int Hq, int Hkv, int N, int d) {
 // lse_d_only the workspace only has to hold the LSE and D parts.
 fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
                     size_t workspace_bytes, fa::BwdParams* p, int* num_sms, bool lse_d_only = false,
-                    const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0) {
+                    const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0,
+                    int Nk = -1) {
+  if (Nk < 0) Nk = N;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
+  if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
   const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, N, d);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < (mask ? w.total_sparse : (lse_d_only ? w.off_dq : w.total)))
@@ -184,6 +192,9 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   p->status = status;
   p->N = N;
   p->NQP = ((N + 127) / 128) * 128;
+  p->Nk = Nk;
+  p->NKP = ((Nk + 127) / 128) * 128;
+  p->causal_off = Nk - N;
   p->Hq = Hq;
   p->Hkv = Hkv;
   p->BH = B * Hq;
@@ -254,24 +265,39 @@ fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, voi
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
-                      void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
-                      float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+fa_status bwd_dkdv_common(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                          void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int Nk, int d,
+                          int causal, float scale, void* stream) {
   const void* ptrs[] = {q, k, v, dO, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms);
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, false,
+                           nullptr, 0, 0, Nk);
   if (st != FA_OK) return st;
   fa::BwdMaps m;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, N, BHkv) || !make_map(&m.v, v, 2, d, N, BHkv) ||
-      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, N, BHkv) || !make_map(&m.dv, dv, 2, d, N, BHkv) ||
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, Nk, BHkv) ||
+      !make_map(&m.v, v, 2, d, Nk, BHkv) || !make_map(&m.dO, dO, 2, d, N, BHq) ||
+      !make_map(&m.dk, dk, 2, d, Nk, BHkv) || !make_map(&m.dv, dv, 2, d, Nk, BHkv) ||
       !make_map(&m.dqacc, p.ws_dq, 4, d, N, BHq))
     return FA_ERR_CUDA;
   const cudaError_t e = fa::launch_bwd_dkdv(d, m, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
+                      float scale, void* stream) {
+  return bwd_dkdv_common(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, N, d, causal, scale,
+                         stream);
 }
 
 fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
@@ -296,6 +322,20 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   st = fa_bwd_dkdv(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale, stream);
   if (st != FA_OK) return st;
   return fa_bwd_dq(dq, workspace, workspace_bytes, B, Hq, Hkv, N, d, scale, stream);
+}
+
+fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                    int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  fa_status st = fa_bwd_preprocess(o, lse, dO, workspace, workspace_bytes, B, Hq, Hkv, Nq, d, stream);
+  if (st != FA_OK) return st;
+  st = bwd_dkdv_common(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
+  if (st != FA_OK) return st;
+  return fa_bwd_dq(dq, workspace, workspace_bytes, B, Hq, Hkv, Nq, d, scale, stream);
 }
 
 fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -323,6 +363,12 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                  int d, int causal, float scale, void* stream) {
   return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int causal, float scale, void* stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, Nq, d, causal, scale, stream, nullptr, 0, 0, Nk);
 }
 
 fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -187,7 +187,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int nq = p.NQP / kBM;
-  const int it0 = p.causal ? jt : 0;
+  // first query tile that sees key tile jt: causal, the one holding query
+  // row jt*128 - (Nk - N) (bottom-right alignment; jt itself when Nk == N)
+  const int first_row = jt * kBN - p.causal_off;
+  const int it0 = p.causal ? (first_row <= 0 ? 0 : min(nq, first_row / kBM)) : 0;
   const int tiles_per_head = nq - it0;
   // block-sparse: only the (head, query tile) steps the mask lets see this key
   // tile, in the dense order, from the list bwd_blocklist_kernel compacted
@@ -399,12 +402,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int r = quarter * 32 + lane;             // key row (TMEM lane); query row for the dQ drain
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    const bool key_pad = jt * kBN + r >= p.N;      // key rows past N contribute nothing
+    const bool key_pad = jt * kBN + r >= p.Nk;     // key rows past Nk contribute nothing
     bool ok = true;
     for (int step = 0; step < nsteps && ok; ++step) {
       const int st = step & 1;
       const int it = step_tile(step);
-      const bool diag = p.causal && it == jt;
+      // causal: query q of tile `it` sees key r of tile jt iff q + lim_off >= r
+      const int lim_off = it * kBM + p.causal_off - jt * kBN;
+      const bool diag = p.causal && lim_off < kBN - 1;
       ok = mbar_wait(bar_q_full(st), (step >> 1) & 1, abort_flag, deadline) &&
            mbar_wait(bar_s_full, step & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
@@ -432,10 +437,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
       for (int c = 0; c < 64; ++c) pf[c] = ex2_approx(pf[c]);
       if (key_pad || diag) {
-        // causal diagonal tile: query q sees key r only if q >= r
+        // causal tile the diagonal crosses: query q sees key r only if q + lim_off >= r
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (key_pad || 64 * g + c < r) pf[c] = 0.f;
+          if (key_pad || 64 * g + c + lim_off < r) pf[c] = 0.f;
       }
       uint32_t pp[32];
 #pragma unroll
@@ -600,7 +605,7 @@ static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStrea
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = (p.NQP / kBN) * p.BHkv;
+  const int grid = (p.NKP / kBN) * p.BHkv;
   bwd_dkdv_kernel<D, kSparse><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv,
                                                                              m.dqacc, p);
   return cudaGetLastError();

@@ -179,10 +179,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int nq = (p.N + kBM - 1) / kBM;
+  const int nk = (p.Nk + kBN - 1) / kBN;
   const int qt[2] = {C::kTilesPerCta * pair, C::kTilesPerCta * pair + 1};
+  // key tiles a query tile reaches: causal, up to the one holding key
+  // (last row + Nk - N), none if that is negative
+  auto reach = [&](int t) {
+    if (!p.causal) return nk;
+    const int last = t * kBM + kBM - 1 + p.causal_off;
+    return last < 0 ? 0 : min(nk, last / kBN + 1);
+  };
   int nkv[2];
-  nkv[0] = p.causal ? qt[0] + 1 : nq;
-  nkv[1] = (C::kPingPong && qt[1] < nq) ? (p.causal ? qt[1] + 1 : nq) : 0;
+  nkv[0] = reach(qt[0]);
+  nkv[1] = (C::kPingPong && qt[1] < nq) ? reach(qt[1]) : 0;
   const bool has_tile[2] = {true, C::kPingPong && qt[1] < nq};
 
   if (threadIdx.x == 0) {
@@ -421,8 +429,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       int lim = kBN;
       const int kvt = kv_tile(j);
       const int kv0 = kvt * kBN;
-      if (p.causal && kvt == qt[g]) lim = row + 1;
-      if (kv0 + kBN > p.N) lim = min(lim, p.N - kv0);
+      if (p.causal) lim = min(lim, q_row + p.causal_off - kv0 + 1);   // bottom-right: key <= row + Nk - N
+      if (kv0 + kBN > p.Nk) lim = min(lim, p.Nk - kv0);
       if (kSparse && !((tile_list[j] >> (14 + g)) & 1)) lim = 0;   // tile visible to the other query tile only
       if (lim < kBN) {
 #pragma unroll
@@ -532,9 +540,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_arrive(bar_p_ready(g));
     }
     // ---------------------------------------------------------- epilogue
-    // A block-sparse query tile that sees no key tile at all skips the loop
-    // and writes O = 0, LSE = -inf; so does any row that saw no key (l = 0).
-    const bool empty = kSparse && has_tile[g] && n_kv == 0;
+    // A query tile that sees no key tile at all (block mask, or more queries
+    // than keys under the causal rule) skips the loop and writes O = 0,
+    // LSE = -inf; so does any row that saw no key (l = 0).
+    const bool empty = has_tile[g] && n_kv == 0;
     if (ok) {
       ok = mbar_wait(bar_o_final(g), 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);

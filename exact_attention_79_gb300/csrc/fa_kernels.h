@@ -9,7 +9,9 @@ namespace fa {
 struct FwdParams {
   float* lse;                      // [B*Hq*N] natural-log logsumexp
   unsigned* status;                // device status word
-  int N, Hq, Hkv, BH;              // BH = B*Hq
+  int N, Hq, Hkv, BH;              // N: query positions; BH = B*Hq
+  int Nk;                          // key positions (== N unless the caller passes another length)
+  int causal_off;                  // Nk - N: key j visible to query i iff j <= i + causal_off (when causal)
   int num_pairs;                   // CTAs per head (set by launch_fwd: 2 query tiles per CTA for bf16, 1 for fp32)
   int causal;
   float scale_log2;                // scale * log2(e)
@@ -31,7 +33,9 @@ struct BwdParams {
   float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows
   float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled, TMA reduce-add target)
   unsigned* status;                // device status word
-  int N, NQP;                      // NQP = N rounded up to a multiple of 128
+  int N, NQP;                      // query positions; NQP = N rounded up to a multiple of 128
+  int Nk, NKP;                     // key positions and Nk rounded up to a multiple of 128
+  int causal_off;                  // Nk - N (bottom-right causal alignment)
   int Hq, Hkv, BH, BHkv;           // BH = B*Hq, BHkv = B*Hkv
   int causal;
   float scale, scale_log2;

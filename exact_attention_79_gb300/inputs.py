@@ -21,17 +21,18 @@ def _normal(rng, shape):
     return rng.standard_normal(size=shape, dtype=np.float32)
 
 
-def make_inputs(B, Hq, Hkv, N, d, dtype="bf16", seed=0, q_mult=1.0, with_grad=False):
+def make_inputs(B, Hq, Hkv, N, d, dtype="bf16", seed=0, q_mult=1.0, with_grad=False, Nk=None):
     """Return a dict of CPU torch tensors q, k, v (and do when with_grad) in the
-    storage dtype ("bf16" or "fp32")."""
+    storage dtype ("bf16" or "fp32"). Nk: positions of k and v (default N)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     tdt = _TORCH_DTYPE[dtype]
+    Nk = N if Nk is None else Nk
     q = _normal(rng, (B, Hq, N, d))
     if q_mult != 1.0:
         q *= np.float32(q_mult)
     out = {"q": torch.from_numpy(q).to(tdt)}
-    out["k"] = torch.from_numpy(_normal(rng, (B, Hkv, N, d))).to(tdt)
-    out["v"] = torch.from_numpy(_normal(rng, (B, Hkv, N, d))).to(tdt)
+    out["k"] = torch.from_numpy(_normal(rng, (B, Hkv, Nk, d))).to(tdt)
+    out["v"] = torch.from_numpy(_normal(rng, (B, Hkv, Nk, d))).to(tdt)
     if with_grad:
         out["do"] = torch.from_numpy(_normal(rng, (B, Hq, N, d))).to(tdt)
     return out

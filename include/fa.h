@@ -64,6 +64,17 @@ typedef enum {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/* Forward with keys of another length than the queries, bf16: q, o
+ * [B, Hq, Nq, d], k, v [B, Hkv, Nk, d], lse [B, Hq, Nq]. The queries are the
+ * last Nq of Nk positions (a chunk of a longer sequence whose earlier keys are
+ * cached): when causal, key j is visible to query i iff j <= i + (Nk - Nq)
+ * (bottom-right alignment; Nq == Nk is fa_fwd's rule). With Nq > Nk the first
+ * Nq - Nk query rows see no key and get O = 0, lse = -inf. No page treats
+ * unequal lengths; this is the plainest extension of the causal rule.
+ * Errors as fa_fwd (FA_ERR_INVALID_ARG also for Nk < 1). */
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale, void* stream);
+
 /* Forward with a block mask, bf16 ("FlashAttention技术解析", section 6.2: whole
  * blocks are skipped, as the causal mask skips the blocks above the diagonal).
  * Same arguments and outputs as fa_fwd, plus a block mask over 128 x 128 tiles:
@@ -115,6 +126,14 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                const void* dO, void* dq, void* dk, void* dv, void* workspace,
                                size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
                                float scale, void* stream);
+
+/* Backward of fa_fwd_kv (same shapes, same visibility rule; o and lse from
+ * fa_fwd_kv): dq [B, Hq, Nq, d], dk, dv [B, Hkv, Nk, d]. The workspace is
+ * fa_bwd_workspace_bytes(B, Hq, Hkv, Nq, d) bytes (it scales with the
+ * queries). Gradients of rows that see no key are zero. Errors as fa_bwd. */
+fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale, void* stream);
 
 /* Backward with the same block mask as fa_fwd_blocksparse (same layout, same
  * visibility rule), bf16; the forward's O and lse must come from
