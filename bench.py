@@ -233,6 +233,7 @@ def native_arm(args, w):
     lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     sparse = bool(w.block_window)
+    kvlen = bool(w.Nk)
     ws_bytes = (int(lib.fa_bwd_blocksparse_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)) if sparse
                 else fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d))
     mask = torch.tensor(w.block_mask(), dtype=torch.uint8, device=dev) if sparse else None
@@ -250,10 +251,21 @@ def native_arm(args, w):
             raise RuntimeError(f"{name} failed with status {code}")
 
     det = args.bwd == "deterministic"
-    if sparse and det:
-        raise SystemExit("the deterministic backward has no block-sparse form")
+    if (sparse or kvlen) and det:
+        raise SystemExit("the deterministic backward has no block-sparse or unequal-length form")
 
     def step(ev):
+        if kvlen:
+            # queries are the last N of Nk positions (fa_fwd_kv / fa_bwd_kv)
+            ev[0].record(stream)
+            check("fa_fwd_kv", lib.fa_fwd_kv(P(q), P(k), P(v), P(o), P(lse), w.B, w.Hq, w.Hkv, w.N, w.Nk, w.d,
+                                             causal, scale, sptr))
+            ev[1].record(stream)
+            check("fa_bwd_kv", lib.fa_bwd_kv(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), P(ws),
+                                             ws_bytes, w.B, w.Hq, w.Hkv, w.N, w.Nk, w.d, causal, scale, sptr))
+            for e in ev[2:]:
+                e.record(stream)
+            return
         if sparse:
             # the broadcast mask: byte strides 0 over batch and heads
             ev[0].record(stream)
@@ -328,12 +340,14 @@ def native_arm(args, w):
         names = ["fwd_kernel", "bwd_deterministic (preprocess + det_dkdv_kernel + det_dq_kernel)", "-", "-"]
     if sparse:
         names = ["fwd_kernel (block-sparse)", "bwd_blocksparse (preprocess + block list + dkdv + dq convert)", "-", "-"]
+    if kvlen:
+        names = ["fwd_kernel (Nq != Nk)", "bwd_kv (preprocess + dkdv + dq convert)", "-", "-"]
     peak, peak_src = peak_tflops()
     # dominant kernel of the step and its tensor roofline
-    dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if (det or sparse) else 2)
+    dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if (det or sparse or kvlen) else 2)
     dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
     achieved = dom_flops / (mean[dom] / 1e3) / 1e12
-    traffic = None if ((det or sparse) and dom != 0) else traffic_from_profile(
+    traffic = None if ((det or sparse or kvlen) and dom != 0) else traffic_from_profile(
         "fa_fwd.cu" if dom == 0 else "fa_bwd.cu", names[dom], w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
@@ -390,11 +404,11 @@ def native_arm(args, w):
         "kernel_ms": {n: m for n, m in zip(names, mean) if n != "-"},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": (5 if sparse else 4) * args.steps,
+        "gpu_launches": (5 if sparse else 4) * args.steps,   # fwd, preprocess, [block list], dK/dV, dQ convert
         "clocks": clocks,
         "wall_s_timed_region": t1 - t0,
     }
-    if world == 1 and not args.no_cpu_baseline and not sparse:
+    if world == 1 and not args.no_cpu_baseline and not sparse and not kvlen:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 

@@ -22,6 +22,7 @@ class Workload:
     q_mult: float = 1.0  # Q is multiplied by this before rounding (logit stress run)
     sampled_rows: int = 0  # >0: check only this many seeded query/key rows per head
     block_window: int = 0  # >0: block-sparse local attention, query tile i sees key tiles i-W+1 .. i
+    Nk: int = 0            # >0: key positions when they differ from N (queries = the last N of Nk)
 
     def block_mask(self):
         """[1, 1, T, T] booleans of the local-window block mask (None when dense)."""
@@ -39,6 +40,15 @@ class Workload:
 
     @property
     def flops_fwd(self) -> float:
+        if self.Nk:
+            # exact visible (query, key) pairs: causal, query i sees keys 0 .. i + Nk - N
+            if self.causal:
+                off = self.Nk - self.N
+                i = range(self.N)
+                pairs = sum(max(0, min(self.Nk, r + off + 1)) for r in i)
+            else:
+                pairs = self.N * self.Nk
+            return 4.0 * self.B * self.Hq * self.d * pairs
         if self.block_window:
             # visible 128 x 128 blocks: full off the diagonal, half on it (the
             # dense causal count 4 B H N^2 d / 2 is the same rule over all blocks)
@@ -60,6 +70,7 @@ class Workload:
             "Hkv": self.Hkv, "N": self.N, "d": self.d, "causal": self.causal,
             "scale": self.scale, "backward": self.backward,
             **({"block_window_tiles": self.block_window} if self.block_window else {}),
+            **({"Nk": self.Nk} if self.Nk else {}),
         }
 
 
@@ -76,6 +87,9 @@ WORKLOADS = {
     # long sequence forward + backward, 8 heads, N=65536, causal, 256 sampled rows per head
     "bf16_h8_n65536_d128_causal_fwdbwd": Workload("bf16_h8_n65536_d128_causal_fwdbwd", "bf16", 1, 8, 8, 65536, 128, True, True, sampled_rows=256),
     # block-sparse local attention (a window of 16 key tiles = 2048 keys, causal), 16 heads, N=32768
+    # chunked prefill: 4096 new queries at the end of 32768 positions, GQA 32 query heads on 8 KV heads, causal
+    "bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd": Workload(
+        "bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd", "bf16", 1, 32, 8, 4096, 128, True, True, Nk=32768),
     "bf16_h16_n32768_d128_local16_fwdbwd": Workload("bf16_h16_n32768_d128_local16_fwdbwd", "bf16", 1, 16, 16, 32768, 128, True, True, block_window=16),
 }
 
