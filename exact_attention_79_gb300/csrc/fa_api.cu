@@ -98,7 +98,10 @@ bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long
 fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
+  // head dims up to 128 in steps of 8 (16-byte rows for TMA); the kernels are
+  // built for 64 and 128 and a smaller d runs in the next one up, the columns
+  // past d read as zeros and never written
+  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * Hq;
   const long long nq = (N + 127) / 128;
@@ -344,6 +347,7 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // the two-pass kernels exist for 64 and 128 only
   fa::BwdParams p{};
   int num_sms = 0;
   fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, true);

@@ -29,11 +29,12 @@
 namespace fa {
 
 // ------------------------------------------------------------------ preprocess
-// One 16-lane group per row (d = 128: 8 bf16 per lane; d = 64: 4 per lane).
+// One 16-lane group per row (d = 128: 8 bf16 per lane; d = 64: 4 per lane;
+// D = 0: any other d, one element per lane and step).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
-                                                      const float* __restrict__ lse, BwdParams p) {
+                                                      const float* __restrict__ lse, BwdParams p, int d) {
   constexpr int kPer = D / 16;
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int nthreads = gridDim.x * blockDim.x;
@@ -46,7 +47,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const int bh = valid_row ? static_cast<int>(r / p.NQP) : 0;
     const int i = valid_row ? static_cast<int>(r % p.NQP) : p.N;
     float acc = 0.f;
-    if (i < p.N) {
+    if (i < p.N && D == 0) {
+      const size_t row0 = (static_cast<size_t>(bh) * p.N + i) * d;
+      for (int c = tid & 15; c < d; c += 16)
+        acc = fmaf(__bfloat162float(o[row0 + c]), __bfloat162float(dO[row0 + c]), acc);
+    } else if (i < p.N) {
       const size_t off = (static_cast<size_t>(bh) * p.N + i) * D + (tid & 15) * kPer;
       if constexpr (kPer == 8) {
         const uint4 a = *reinterpret_cast<const uint4*>(o + off);
@@ -81,15 +86,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       p.ws_lse2[r] = (i < p.N) ? lse[static_cast<size_t>(bh) * p.N + i] * kLog2e : INFINITY;
     }
   }
-  const long long n4 = static_cast<long long>(p.BH) * p.N * D / 4;
+  const long long n4 = static_cast<long long>(p.BH) * p.N * d / 4;
   float4* acc4 = reinterpret_cast<float4*>(p.ws_dq);
   for (long long x = tid; x < n4; x += nthreads) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ dQ convert
-template <int D>
-__global__ void __launch_bounds__(256) bwd_dq_kernel(__nv_bfloat16* __restrict__ dq, BwdParams p) {
-  const long long n8 = static_cast<long long>(p.BH) * p.N * D / 8;
+__global__ void __launch_bounds__(256) bwd_dq_kernel(__nv_bfloat16* __restrict__ dq, BwdParams p, int d) {
+  const long long n8 = static_cast<long long>(p.BH) * p.N * d / 8;     // d is a multiple of 8
   const float4* src = reinterpret_cast<const float4*>(p.ws_dq);
   uint4* dst = reinterpret_cast<uint4*>(dq);
   const float s = p.scale;
@@ -657,23 +661,24 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* ls
                            cudaStream_t stream) {
   const auto* o16 = static_cast<const __nv_bfloat16*>(o);
   const auto* do16 = static_cast<const __nv_bfloat16*>(dO);
-  if (d == 128) bwd_pre_kernel<128><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p);
-  else if (d == 64) bwd_pre_kernel<64><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p);
+  if (d == 128) bwd_pre_kernel<128><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
+  else if (d == 64) bwd_pre_kernel<64><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
+  else if (d >= 8 && d <= 128 && d % 8 == 0) bwd_pre_kernel<0><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   const bool sparse = p.mask != nullptr;
-  if (d == 128) return sparse ? launch_dkdv_d<128, true>(m, p, stream) : launch_dkdv_d<128, false>(m, p, stream);
-  if (d == 64) return sparse ? launch_dkdv_d<64, true>(m, p, stream) : launch_dkdv_d<64, false>(m, p, stream);
+  // d < 128 runs in the kernel for the next size up (zero-filled columns)
+  if (d > 64 && d <= 128) return sparse ? launch_dkdv_d<128, true>(m, p, stream) : launch_dkdv_d<128, false>(m, p, stream);
+  if (d >= 8 && d <= 64) return sparse ? launch_dkdv_d<64, true>(m, p, stream) : launch_dkdv_d<64, false>(m, p, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream) {
   auto* dq16 = static_cast<__nv_bfloat16*>(dq);
-  if (d == 128) bwd_dq_kernel<128><<<num_sms * 4, 256, 0, stream>>>(dq16, p);
-  else if (d == 64) bwd_dq_kernel<64><<<num_sms * 4, 256, 0, stream>>>(dq16, p);
+  if (d >= 8 && d <= 128 && d % 8 == 0) bwd_dq_kernel<<<num_sms * 4, 256, 0, stream>>>(dq16, p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

@@ -633,10 +633,12 @@ cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUte
   const int grid = p.num_pairs * p.BH;
   const bool sparse = p.mask != nullptr;
   if (sparse && (dtype_bytes != 2 || nq > kMaskMaxTiles)) return cudaErrorInvalidValue;
-  if (dtype_bytes == 2 && d == 128)
+  // d < 128 runs in the kernel for the next size up: TMA fills the columns
+  // past d with zeros on load and skips them on store
+  if (dtype_bytes == 2 && d > 64 && d <= 128)
     return sparse ? launch<__nv_bfloat16, 128, true>(mq, mk, mv, mo, p, grid, stream)
                   : launch<__nv_bfloat16, 128, false>(mq, mk, mv, mo, p, grid, stream);
-  if (dtype_bytes == 2 && d == 64)
+  if (dtype_bytes == 2 && d <= 64)
     return sparse ? launch<__nv_bfloat16, 64, true>(mq, mk, mv, mo, p, grid, stream)
                   : launch<__nv_bfloat16, 64, false>(mq, mk, mv, mo, p, grid, stream);
   if (dtype_bytes == 4 && d == 64) return launch<float, 64, false>(mq, mk, mv, mo, p, grid, stream);

@@ -45,14 +45,15 @@ def test_workspace_size_formula(lib):
     # B*Hq = 8 rows of ceil(100/128)*128 = 128 padded entries: 4096 B each for lse2 and D
     assert lib.fa_bwd_workspace_bytes(2, 4, 2, 100, 64) == 4096 + 4096 + 8 * 100 * 64 * 4
     assert lib.fa_bwd_workspace_bytes(1, 3, 2, 128, 128) == 0      # Hq not a multiple of Hkv
-    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 96) == 0       # unsupported head dim
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 100) == 0      # head dim not a multiple of 8
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 136) == 0      # head dim above 128
 
 
 def test_invalid_arguments_rejected_without_device(lib):
     null = ctypes.c_void_p(0)
     fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
     assert lib.fa_fwd(null, fake, fake, fake, fake, 1, 1, 1, 128, 64, 0, 0.125, null) == 1
-    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 80, 0, 0.125, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 84, 0, 0.125, null) == 1     # d not a multiple of 8
     assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 4, 3, 128, 64, 0, 0.125, null) == 1
     assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 64, 0, 0.0, null) == 1
     assert lib.fa_fwd(fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 4), 1, 1, 1, 128, 64, 0, 0.1, null) == 1

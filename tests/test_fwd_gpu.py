@@ -125,7 +125,7 @@ def test_fwd_rejects_bad_arguments(fa):
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     s = ctypes.c_void_p(0)
     assert lib.fa_fwd(None, P(x), P(x), P(x), P(lse), 1, 2, 2, 128, 64, 0, 0.125, s) == 1
-    assert lib.fa_fwd(P(x), P(x), P(x), P(x), P(lse), 1, 2, 2, 128, 96, 0, 0.125, s) == 1
+    assert lib.fa_fwd(P(x), P(x), P(x), P(x), P(lse), 1, 2, 2, 128, 100, 0, 0.125, s) == 1
     assert lib.fa_fwd(P(x), P(x), P(x), P(x), P(lse), 1, 2, 3, 128, 64, 0, 0.125, s) == 1
     assert lib.fa_fwd(P(x), P(x), P(x), P(x), P(lse), 1, 2, 2, 0, 64, 0, 0.125, s) == 1
     assert lib.fa_fwd(P(x), P(x), P(x), P(x), P(lse), 1, 2, 2, 128, 64, 0, float("nan"), s) == 1
