@@ -18,13 +18,15 @@
  *   Layout: dense row-major, no strides. Q, O, dO, dQ are [B, Hq, N, d];
  *     K, V, dK, dV are [B, Hkv, N, d]; LSE is [B, Hq, N] fp32. Query head h
  *     reads key/value head h / (Hq / Hkv) (grouped-query attention).
- *   Causal: key j is visible to query i iff j <= i (one N for queries and keys).
+ *   Causal: key j is visible to query i iff j <= i (one N for queries and
+ *     keys; fa_fwd_kv / fa_bwd_kv extend the rule to other key lengths).
  *   LSE_i = ln sum_j exp(scale * q_i . k_j) over the visible keys.
  *   Pointers: device pointers, 16-byte aligned, owned by the caller; the
  *     library never allocates or frees memory during a call and keeps no
  *     reference after it returns.
- *   Sizes: B, Hq, Hkv, N >= 1; Hq % Hkv == 0; d in {64, 128}; scale finite
- *     and > 0.
+ *   Sizes: B, Hq, Hkv, N >= 1; Hq % Hkv == 0; d a multiple of 8 from 8 to
+ *     128 (d other than 64 and 128 runs in the next larger kernel, the extra
+ *     columns read as zeros and never written); scale finite and > 0.
  *   stream: a cudaStream_t (NULL = legacy default stream). Every call is
  *     asynchronous on it; argument errors are reported synchronously and
  *     launch nothing.
