@@ -208,6 +208,25 @@ def traffic_from_profile(kernel_file, kernel_name, workload):
         return None
 
 
+# ------------------------------------------------------------------ replicas across ranks
+def max_over_ranks(x, world):
+    """The largest of every rank's x (one float); x itself on a single rank.
+    The replicas share no data; this is the only collective of the bench."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_step, steps, slowest_total_ms):
+    """Work of all replicas (each did `steps` steps of `flops_per_step`) over
+    the slowest replica's time (weak scaling)."""
+    return world * flops_per_step * steps / (slowest_total_ms / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ native arm
 def native_arm(args, w):
     import ctypes
@@ -327,13 +346,9 @@ def native_arm(args, w):
 
     seg = [[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)]
     step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world)
     flops_step = w.flops_fwd + w.flops_bwd
-    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
     names = ["fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
     if det:
@@ -378,11 +393,7 @@ def native_arm(args, w):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b) / args.e2e_steps
-        if world > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, world)
         fa.check_device_status(stream.cuda_stream)
         e2e = {"value": world * flops_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}

@@ -1,0 +1,59 @@
+"""The N > 1 path of bench.py on CPU: replicas share no data, so the only
+cross-rank logic is the max-over-ranks timing and the whole-job value; two
+gloo ranks on 127.0.0.1 exercise it. The reference arm's non-zero ranks
+must exit without doing work."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out_path):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = [120.0, 250.0][rank]                 # rank 1 is the slow replica
+    slowest = bench.max_over_ranks(local_ms, world)
+    value = bench.whole_job_tflops(world, 1e12, 10, slowest)
+    dist.barrier()
+    with open(f"{out_path}.{rank}", "w") as f:
+        json.dump({"slowest": slowest, "value": value}, f)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_replica(tmp_path):
+    port = _free_port()
+    out = str(tmp_path / "r")
+    mp.start_processes(_rank, args=(2, port, out), nprocs=2, start_method="spawn", join=True)
+    res = [json.load(open(f"{out}.{r}")) for r in range(2)]
+    assert res[0] == res[1]
+    assert res[0]["slowest"] == 250.0
+    # 2 replicas x 10 steps x 1 TFLOP over 0.25 s
+    assert abs(res[0]["value"] - 80.0) < 1e-9
+
+
+def test_single_rank_needs_no_collective():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.whole_job_tflops(1, 2e12, 4, 1000.0) == 8.0
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
