@@ -575,15 +575,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (warp == 2 && lane == 0) {
-        for (int bx = 0; bx < C::kNBox; ++bx) {
-          tma_store_3d(&map_dv, stg_v + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
-          tma_store_3d(&map_dk, stg_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
-        }
-        tma_store_commit();
-        tma_store_wait_all0();
+    }
+    // all eight softmax-gradient warps meet here whether or not their waits
+    // succeeded; a warp that gave up has raised the abort flag: store nothing
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 2 && lane == 0) {
+      for (int bx = 0; bx < C::kNBox; ++bx) {
+        tma_store_3d(&map_dv, s_v + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+        tma_store_3d(&map_dk, s_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
       }
+      tma_store_commit();
+      tma_store_wait_all0();
     }
   }
 

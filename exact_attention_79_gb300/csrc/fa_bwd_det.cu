@@ -326,15 +326,17 @@ det_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       stage_half_bf16<D>(tbase + lane_off + C::kColDV + g * (D / 2), s_v, r, g * (D / 2), 1.0f);
       stage_half_bf16<D>(tbase + lane_off + C::kColDK + g * (D / 2), s_k, r, g * (D / 2), p.scale);
       fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (warp == 2 && lane == 0) {
-        for (int bx = 0; bx < C::kNBox; ++bx) {
-          tma_store_3d(&map_dv, s_v + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
-          tma_store_3d(&map_dk, s_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
-        }
-        tma_store_commit();
-        tma_store_wait_all0();
+    }
+    // all eight warps meet here whether or not their waits succeeded; a warp
+    // that gave up has raised the abort flag: store nothing
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 2 && lane == 0) {
+      for (int bx = 0; bx < C::kNBox; ++bx) {
+        tma_store_3d(&map_dv, s_v + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+        tma_store_3d(&map_dk, s_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
       }
+      tma_store_commit();
+      tma_store_wait_all0();
     }
   }
 
@@ -598,12 +600,12 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       // staging in the Q buffer (every MMA has completed)
       stage_half_bf16<D>(tbase + lane_off + C::kColDQ + g * (D / 2), s_q, r, g * (D / 2), p.scale);
       fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (warp == 2 && lane == 0) {
-        for (int bx = 0; bx < C::kNBox; ++bx) tma_store_3d(&map_dq, s_q + bx * kBoxBytes, bx * 64, it * kBM, bh);
-        tma_store_commit();
-        tma_store_wait_all0();
-      }
+    }
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 2 && lane == 0) {
+      for (int bx = 0; bx < C::kNBox; ++bx) tma_store_3d(&map_dq, s_q + bx * kBoxBytes, bx * 64, it * kBM, bh);
+      tma_store_commit();
+      tma_store_wait_all0();
     }
   }
 

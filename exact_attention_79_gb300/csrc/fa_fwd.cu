@@ -587,14 +587,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1 + g, 128);
-      if (warp == 2 + 4 * g && lane == 0) {
-        for (int bx = 0; bx < C::kNBox; ++bx)
-          tma_store_3d(&map_o, stage + bx * kBoxBytes, bx * C::kChunk, qt[g] * kBM, bh);
-        tma_store_commit();
-        tma_store_wait_all0();
-      }
       if (q_row < p.N) p.lse[static_cast<size_t>(bh) * p.N + q_row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+    // every warp of the group meets here whether or not its waits succeeded,
+    // so a timeout in one warp cannot leave the others stuck on the barrier;
+    // a warp that gave up has raised the abort flag, and then nothing is stored
+    named_bar_sync(1 + g, 128);
+    if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {
+      for (int bx = 0; bx < C::kNBox; ++bx)
+        tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * C::kChunk, qt[g] * kBM, bh);
+      tma_store_commit();
+      tma_store_wait_all0();
     }
   }
 
