@@ -75,6 +75,15 @@ unsigned long long wait_limit_ns() {
   return ns;
 }
 
+// FA_TEST_STALL=1 (read at every call): the tensor-core issuer first waits on
+// a barrier nothing ever arrives on, so the bounded wait runs out and the
+// call reports FA_ERR_TIMEOUT; for exercising failure detection without any
+// fault. Off unless set.
+int test_stall() {
+  const char* e = std::getenv("FA_TEST_STALL");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 3-D map over a dense [BH, N, d] tensor: dims (d, N, BH), one box = 128 rows
@@ -140,6 +149,7 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_limit_ns();
+  p.test_stall = test_stall();
   p.mask = mask;
   p.mask_sb = mask_sb;
   p.mask_sh = mask_sh;
@@ -206,6 +216,7 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   p->scale = scale;
   p->scale_log2 = scale * 1.4426950408889634f;
   p->timeout_ns = wait_limit_ns();
+  p->test_stall = test_stall();
   p->mask = mask;
   p->mask_sb = mask_sb;
   p->mask_sh = mask_sh;

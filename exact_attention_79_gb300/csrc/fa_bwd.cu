@@ -178,6 +178,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t bar_s_full = bars + 136, bar_dp_full = bars + 144, bar_p_ready = bars + 152;
   const uint32_t bar_ds_ready = bars + 160, bar_dq_full = bars + 168, bar_dq_free = bars + 176;
   const uint32_t bar_o_final = bars + 184;
+  const uint32_t bar_stall = bars + 208;                   // nothing arrives (timeout test)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 192);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 196);
 
@@ -221,6 +222,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 257);           // + the watcher: dO of the next step has landed
     mbar_init(bar_o_final, 1);
+    mbar_init(bar_stall, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -304,8 +306,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mma_commit(bar_dp_full);
       };
       // (a block-sparse key tile may have no step at all: dK = dV = 0)
-      bool ok = nsteps == 0 ||
-                (mbar_wait(bar_kv_full, 0, abort_flag, deadline) && mbar_wait(bar_q_full(0), 0, abort_flag, deadline));
+      bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
+      ok = ok && (nsteps == 0 ||
+                  (mbar_wait(bar_kv_full, 0, abort_flag, deadline) && mbar_wait(bar_q_full(0), 0, abort_flag, deadline)));
       if (ok && nsteps > 0) {
         tc_fence_after();
         issue_s(0);

@@ -167,6 +167,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   // block-sparse: the key tiles either query tile may see, ascending, after the
   // barriers; entry = tile | (visible to tile 0) << 14 | (visible to tile 1) << 15
   int* const list_count = reinterpret_cast<int*>(gbars + 480);       // [0] all, [1] group 0's prefix
+  const uint32_t bar_stall = bars + 472;                             // nothing arrives (timeout test)
   uint16_t* const tile_list = reinterpret_cast<uint16_t*>(gbars + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -206,6 +207,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(bar_kv_empty(s), 1);
     }
     mbar_init(bar_qk_ready, 128);
+    mbar_init(bar_stall, 1);
     fence_mbar_init();
   }
   if constexpr (kSparse) {
@@ -284,6 +286,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const uint32_t idesc_pv = make_idesc(C::kFmt, 128, D, 0, C::kTf32 ? 0 : 1);
       const uint32_t s_vt = s_q[1];                 // V^T buffer of the fp32 variant
       bool ok = true;
+      if (p.test_stall) ok = mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       for (int i = 0; i < 2 && ok; ++i)
         if (nkv[i] > 0) ok = mbar_wait(bar_q_full(i), 0, abort_flag, deadline);
       int c = 0;

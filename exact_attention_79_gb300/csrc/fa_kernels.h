@@ -21,6 +21,7 @@ struct FwdParams {
   const unsigned char* mask;
   long long mask_sb, mask_sh;
   int mask_nt;                     // tiles per row = ceil(N / 128)
+  int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
 };
 constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 
@@ -48,6 +49,7 @@ struct BwdParams {
   int mask_nt;
   int* ws_count;
   unsigned* ws_list;
+  int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;

@@ -34,8 +34,13 @@
  *   Errors: FA_ERR_INVALID_ARG for bad pointers or sizes, FA_ERR_UNSUPPORTED
  *     for a valid but unimplemented combination, FA_ERR_ARCH for a device that
  *     is not sm_103, FA_ERR_CUDA when a launch fails. Inside the kernels every
- *     wait is bounded; a wait that runs out sets the device status word,
- *     which fa_device_status reports as FA_ERR_TIMEOUT.
+ *     wait is bounded (2 s, or FA_WAIT_LIMIT_MS milliseconds from the
+ *     environment, read once per process); a wait that runs out makes its
+ *     block unwind, store nothing and set the device status word, which
+ *     fa_device_status reports as FA_ERR_TIMEOUT; the context stays usable.
+ *     FA_TEST_STALL=1 in the environment (read at every call) makes the
+ *     tensor-core issuer of fa_fwd* and of fa_bwd's dK/dV pass wait on a
+ *     barrier nothing arrives on, to exercise that path; unset in normal use.
  *   Threads: calls may come from several host threads; each call is
  *     independent.
  */

@@ -1,0 +1,63 @@
+"""Failure detection on the GPU without any fault: with FA_TEST_STALL=1 the
+tensor-core issuer first waits on a barrier nothing arrives on, so its
+bounded wait (FA_WAIT_LIMIT_MS, here 300 ms) runs out; every other role of
+the block sees the abort flag and unwinds, the block stores nothing and the
+call reports FA_ERR_TIMEOUT through fa_device_status. The next call on the
+same context must be correct. Runs in a child process because the wait
+limit is read once per process."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import ctypes, os, sys, time
+sys.path.insert(0, ROOT)
+import numpy as np, torch
+import exact_attention_79_gb300 as fa
+import oracle
+from exact_attention_79_gb300 import configs, inputs
+lib = fa.load()
+dev = torch.device("cuda:0")
+stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+t = inputs.make_inputs(1, 2, 2, 300, 128, "bf16", seed=1, with_grad=True)
+g = {n: x.to(dev) for n, x in t.items()}
+f = {n: inputs.to_f64(x) for n, x in t.items()}
+ro, rl, rdq, rdk, rdv = oracle.backward(f["q"], f["k"], f["v"], f["do"], True, 128 ** -0.5)
+
+def run(stall, what):
+    os.environ["FA_TEST_STALL"] = "1" if stall else "0"
+    t0 = time.time()
+    if what == "fwd":
+        out = fa.fwd(g["q"], g["k"], g["v"], causal=True)
+    else:
+        out = fa.bwd(g["q"], g["k"], g["v"], o_ok, lse_ok, g["do"], causal=True)
+    code = lib.fa_device_status(stream)
+    return out, code, time.time() - t0
+
+out, code, dt = run(True, "fwd")
+assert code == 5 and dt >= 0.25, (code, dt)                      # FA_ERR_TIMEOUT after the 300 ms limit
+(o_ok, lse_ok), code, _ = run(False, "fwd")
+assert code == 0
+assert np.abs(o_ok.float().cpu().numpy() - ro).max() <= configs.TOL_O_MAX
+out, code, dt = run(True, "bwd")
+assert code == 5 and dt >= 0.25, (code, dt)
+(dq, dk, dv), code, _ = run(False, "bwd")
+assert code == 0
+for a, r in zip((dq, dk, dv), (rdq, rdk, rdv)):
+    a = a.float().cpu().numpy()
+    assert np.linalg.norm(a - r) / np.linalg.norm(r) <= configs.TOL_GRAD_REL_FRO
+print("timeout-path-ok")
+'''
+
+
+def test_bounded_wait_runs_out_and_context_stays_usable():
+    env = dict(os.environ, FA_WAIT_LIMIT_MS="300", FA_TEST_STALL="0")
+    r = subprocess.run([sys.executable, "-c", "ROOT = %r\n" % ROOT + CHILD], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and "timeout-path-ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
