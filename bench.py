@@ -4,7 +4,8 @@
 One step = one pass of the whole path over one batch: fa_fwd, then the three
 backward phases (fa_bwd_preprocess, fa_bwd_dkdv, fa_bwd_dq), all through the
 C ABI. FLOPs are counted as 4 B Hq N^2 d for the forward (halved when causal)
-and 2.5x that for the backward. Prints one JSON line.
+and 2.5x that for the backward. Prints one JSON line. A workload without a
+backward (configs.Workload.backward false) times the forward call alone.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
 
@@ -44,6 +45,12 @@ def parse_args():
     ap.add_argument("--bwd", choices=["fused", "deterministic"], default="fused",
                     help="backward timed: fa_bwd's three phases (default) or fa_bwd_deterministic")
     return ap.parse_args()
+
+
+def metric_for(w):
+    if w.backward:
+        return METRIC
+    return f"attention TFLOPS fwd ({w.dtype}, d={w.d}) and % of GB300 dense BF16 peak"
 
 
 def peak_tflops():
@@ -107,22 +114,27 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle timing
 def oracle_rows_flops(rows, N, d, causal):
-    """Algorithmic fwd+bwd FLOPs of the given query rows: 14 d per visible key."""
+    """Algorithmic fwd+bwd FLOPs of the given query rows: 14 d per visible key
+    (4 d of them the forward's)."""
     import numpy as np
     keys = (np.asarray(rows) + 1) if causal else np.full(len(rows), N)
     return 14.0 * d * float(keys.sum())
 
 
 def oracle_slab_runner(w, seed=0):
-    """Returns (run(rows) -> flops, description): the oracle's full forward +
-    backward arithmetic for a slab of query rows of head (0, 0)."""
+    """Returns (run(rows) -> flops, np): the oracle's full forward + backward
+    arithmetic (the forward alone for a workload without a backward) for a
+    slab of query rows of head (0, 0)."""
     import numpy as np
     import oracle
     from exact_attention_79_gb300 import inputs
-    t = inputs.make_inputs(1, 1, 1, w.N, w.d, w.dtype, seed=seed, with_grad=True)
+    t = inputs.make_inputs(1, 1, 1, w.N, w.d, w.dtype, seed=seed, with_grad=w.backward)
     f = {k: inputs.to_f64(v) for k, v in t.items()}
 
     def run(rows):
+        if not w.backward:
+            oracle.forward_rows(f["q"], f["k"], f["v"], w.causal, w.scale, np.asarray(rows)[None, None])
+            return oracle_rows_flops(rows, w.N, w.d, w.causal) * 4.0 / 14.0
         oracle.backward_query_rows(f["q"], f["k"], f["v"], f["do"], w.causal, w.scale, 0, 0, rows)
         return oracle_rows_flops(rows, w.N, w.d, w.causal)
     return run, np
@@ -149,7 +161,8 @@ def cpu_baseline(w, budget_s):
         nrows += len(rows)
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{nrows} seeded query rows of head 0 (full fwd+bwd arithmetic per row, fp64), {dt:.1f} s"}
+            "sample": f"{nrows} seeded query rows of head 0 (full {'fwd+bwd' if w.backward else 'forward'} "
+                      f"arithmetic per row, fp64), {dt:.1f} s"}
 
 
 def reference_arm(args, w):
@@ -172,13 +185,14 @@ def reference_arm(args, w):
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
                    "sample_rows_per_step": R},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{R} seeded query rows of head 0 per step (full fwd+bwd arithmetic, fp64)"},
+                         "sample": f"{R} seeded query rows of head 0 per step (full "
+                                   f"{'fwd+bwd' if w.backward else 'forward'} arithmetic, fp64)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -246,14 +260,17 @@ def native_arm(args, w):
     dev = torch.device("cuda", local)
     lib = fa.load()
 
-    t = inputs.make_workload_inputs(w, with_grad=True)
-    q, k, v, do = (t[n].to(dev) for n in ("q", "k", "v", "do"))
+    fwd_only = not w.backward
+    t = inputs.make_workload_inputs(w, with_grad=not fwd_only)
+    q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
+    do = None if fwd_only else t["do"].to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = (None, None, None) if fwd_only else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     sparse = bool(w.block_window)
     kvlen = bool(w.Nk)
-    ws_bytes = (int(lib.fa_bwd_blocksparse_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)) if sparse
+    ws_bytes = (0 if fwd_only else
+                int(lib.fa_bwd_blocksparse_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)) if sparse
                 else fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d))
     mask = torch.tensor(w.block_mask(), dtype=torch.uint8, device=dev) if sparse else None
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -272,8 +289,17 @@ def native_arm(args, w):
     det = args.bwd == "deterministic"
     if (sparse or kvlen) and det:
         raise SystemExit("the deterministic backward has no block-sparse or unequal-length form")
+    if fwd_only and (sparse or kvlen or det):
+        raise SystemExit("forward-only workloads are dense with equal lengths")
+    fwd_name = "fa_fwd" if w.dtype == "bf16" else "fa_fwd_f32"
 
     def step(ev):
+        if fwd_only:
+            ev[0].record(stream)
+            check(fwd_name, getattr(lib, fwd_name)(P(q), P(k), P(v), P(o), P(lse), *dims, causal, scale, sptr))
+            for e in ev[1:]:
+                e.record(stream)
+            return
         if kvlen:
             # queries are the last N of Nk positions (fa_fwd_kv / fa_bwd_kv)
             ev[0].record(stream)
@@ -347,10 +373,14 @@ def native_arm(args, w):
     seg = [[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)]
     step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)]
     total_ms = max_over_ranks(sum(step_ms), world)
-    flops_step = w.flops_fwd + w.flops_bwd
+    flops_step = w.flops_fwd + (0.0 if fwd_only else w.flops_bwd)
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
-    names = ["fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    fwd_kernel = "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
+    fwd_src = "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
+    names = [fwd_kernel, "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    if fwd_only:
+        names = [fwd_kernel, "-", "-", "-"]
     if det:
         names = ["fwd_kernel", "bwd_deterministic (preprocess + det_dkdv_kernel + det_dq_kernel)", "-", "-"]
     if sparse:
@@ -363,7 +393,7 @@ def native_arm(args, w):
     dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
     achieved = dom_flops / (mean[dom] / 1e3) / 1e12
     traffic = None if ((det or sparse or kvlen) and dom != 0) else traffic_from_profile(
-        "fa_fwd.cu" if dom == 0 else "fa_bwd.cu", names[dom], w.name)
+        fwd_src if dom == 0 else "fa_bwd.cu", names[dom], w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
                 "algorithmic_flops_per_launch": dom_flops}
@@ -371,10 +401,10 @@ def native_arm(args, w):
     # ---- end to end: pinned host inputs -> device, the four calls, results -> host
     e2e = None
     if args.e2e_steps > 0:
-        host_in = [x.cpu().pin_memory() for x in (q, k, v, do)]
-        host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse, dq, dk, dv)]
-        dev_in = (q, k, v, do)
-        dev_out = (o, lse, dq, dk, dv)
+        dev_in = (q, k, v) if fwd_only else (q, k, v, do)
+        dev_out = (o, lse) if fwd_only else (o, lse, dq, dk, dv)
+        host_in = [x.cpu().pin_memory() for x in dev_in]
+        host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in dev_out]
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = sum(x.numel() * x.element_size() for x in host_out)
 
@@ -402,20 +432,22 @@ def native_arm(args, w):
         return
     clocks = sampler.summary(t0, t1)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU", "bwd_variant": args.bwd},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "bwd_variant": "none" if fwd_only else args.bwd},
         "frac_of_peak": value / world / peak,
         "fwd_tflops": w.flops_fwd / (mean[0] / 1e3) / 1e12,
         "fwd_frac_of_peak": w.flops_fwd / (mean[0] / 1e3) / 1e12 / peak,
-        "bwd_tflops": w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
+        "bwd_tflops": None if fwd_only else w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
         "kernel_ms": {n: m for n, m in zip(names, mean) if n != "-"},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": (5 if sparse else 4) * args.steps,   # fwd, preprocess, [block list], dK/dV, dQ convert
+        # fwd, preprocess, [block list], dK/dV, dQ convert
+        "gpu_launches": (1 if fwd_only else 5 if sparse else 4) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t1 - t0,
     }

@@ -86,11 +86,13 @@ WORKLOADS = {
     "bf16_h16_n8192_d128_causal_fwdbwd": Workload("bf16_h16_n8192_d128_causal_fwdbwd", "bf16", 1, 16, 16, 8192, 128, True, True),
     # long sequence forward + backward, 8 heads, N=65536, causal, 256 sampled rows per head
     "bf16_h8_n65536_d128_causal_fwdbwd": Workload("bf16_h8_n65536_d128_causal_fwdbwd", "bf16", 1, 8, 8, 65536, 128, True, True, sampled_rows=256),
-    # block-sparse local attention (a window of 16 key tiles = 2048 keys, causal), 16 heads, N=32768
     # chunked prefill: 4096 new queries at the end of 32768 positions, GQA 32 query heads on 8 KV heads, causal
     "bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd": Workload(
         "bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd", "bf16", 1, 32, 8, 4096, 128, True, True, Nk=32768),
+    # block-sparse local attention (a window of 16 key tiles = 2048 keys, causal), 16 heads, N=32768
     "bf16_h16_n32768_d128_local16_fwdbwd": Workload("bf16_h16_n32768_d128_local16_fwdbwd", "bf16", 1, 16, 16, 32768, 128, True, True, block_window=16),
+    # head dimension 256 (forward; the wide-head kernel), same N and heads as the d = 128 fwd+bwd case
+    "bf16_h16_n8192_d256_causal_fwd": Workload("bf16_h16_n8192_d256_causal_fwd", "bf16", 1, 16, 16, 8192, 256, True, False),
 }
 
 # Tolerances against the double-precision oracle on the same rounded inputs.

@@ -89,13 +89,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 3-D map over a dense [BH, N, d] tensor: dims (d, N, BH), one box = 128 rows
 // by 128 bytes with 128-byte swizzle. Rows past N read as zero and are not
 // written by stores.
-bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long long BH) {
+bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long long BH, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elt_bytes,
                                  static_cast<cuuint64_t>(d) * N * elt_bytes};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), 128, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(m, elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -107,16 +107,21 @@ bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long
 fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  // head dims up to 128 in steps of 8 (16-byte rows for TMA); the kernels are
-  // built for 64 and 128 and a smaller d runs in the next one up, the columns
-  // past d read as zeros and never written
-  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_INVALID_ARG;
+  // head dims up to 256 in steps of 8 (16-byte rows for TMA); the kernels are
+  // built for 64, 128, 192 and 256 and a smaller d runs in the next one up,
+  // the columns past d read as zeros and never written. The backward stops
+  // at 128 (bwd_dim).
+  if (d < 8 || d > 256 || d % 8 != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * Hq;
   const long long nq = (N + 127) / 128;
   if (BH > (1LL << 24) || ((nq + 1) / 2) * BH >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
+
+// The backward kernels hold dK, dV, S^T and dP^T of a 128-key tile in TMEM
+// (4 x d columns of 512): head dims above 128 are not built.
+fa_status bwd_dim(int d) { return d > 128 ? FA_ERR_UNSUPPORTED : FA_OK; }
 
 fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, int N, int d, int causal, float scale, void* stream,
@@ -129,13 +134,15 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   if (st != FA_OK) return st;
   if (Nk < 1) return FA_ERR_INVALID_ARG;
   if (elt == 4 && d != 64) return FA_ERR_UNSUPPORTED;
+  const bool wide = d > 128;                // one query tile per CTA, V in 64-key halves
+  if (wide && mask) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = device_state(&status);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
   if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, Nk, BHkv) ||
-      !make_map(&mv, v, elt, d, Nk, BHkv) || !make_map(&mo, o, elt, d, N, BHq))
+      !make_map(&mv, v, elt, d, Nk, BHkv, wide ? 64 : 128) || !make_map(&mo, o, elt, d, N, BHq))
     return FA_ERR_CUDA;
   fa::FwdParams p{};
   p.lse = lse;
@@ -154,7 +161,8 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   p.mask_sb = mask_sb;
   p.mask_sh = mask_sh;
   p.mask_nt = (N + 127) / 128;
-  const cudaError_t e = fa::launch_fwd(elt, d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = wide ? fa::launch_fwd_wide(d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream))
+                             : fa::launch_fwd(elt, d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -191,6 +199,8 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
   if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
+  st = bwd_dim(d);
+  if (st != FA_OK) return st;
   const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, N, d);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < (mask ? w.total_sparse : (lse_d_only ? w.off_dq : w.total)))
@@ -231,12 +241,13 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
 extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
-  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK) return 0;
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK || bwd_dim(d) != FA_OK) return 0;
   return bwd_workspace(B, Hq, Hkv, N, d).total;
 }
 
 size_t fa_bwd_blocksparse_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
-  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK || (N + 127) / 128 > fa::kMaskMaxTiles) return 0;
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK || bwd_dim(d) != FA_OK || (N + 127) / 128 > fa::kMaskMaxTiles)
+    return 0;
   return bwd_workspace(B, Hq, Hkv, N, d).total_sparse;
 }
 

@@ -29,6 +29,11 @@ constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 1
 cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
 
+// Head dims 136..256 (bf16, dense): one 128-row query tile per CTA; the V
+// map has 64-row boxes (the kernel stages V in 64-key halves).
+cudaError_t launch_fwd_wide(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const CUtensorMap& mo, const FwdParams& p, cudaStream_t stream);
+
 struct BwdParams {
   float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows
   float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows

@@ -25,8 +25,15 @@
  *     library never allocates or frees memory during a call and keeps no
  *     reference after it returns.
  *   Sizes: B, Hq, Hkv, N >= 1; Hq % Hkv == 0; d a multiple of 8 from 8 to
- *     128 (d other than 64 and 128 runs in the next larger kernel, the extra
- *     columns read as zeros and never written); scale finite and > 0.
+ *     256 (kernels are built for d = 64, 128, 192 and 256; any other d runs
+ *     in the next larger one, the extra columns read as zeros and never
+ *     written); scale finite and > 0. The forward calls take every such d
+ *     (fa_fwd_f32 and fa_fwd_blocksparse excepted, see there); the backward
+ *     calls stop at d = 128 and return FA_ERR_UNSUPPORTED for 136..256, since
+ *     the dK, dV, S^T and dP^T accumulators of a 128-key tile (4 d columns)
+ *     must fit the 512 TMEM columns. FlashAttention-2 raised the supported
+ *     head dimension from 128 to 256 ("Flash Attention-2", section
+ *     "Снижение накладных расходов").
  *   stream: a cudaStream_t (NULL = legacy default stream). Every call is
  *     asynchronous on it; argument errors are reported synchronously and
  *     launch nothing.
@@ -94,7 +101,7 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float*
  * causal, j <= i. Key tiles no query tile of a CTA sees are never loaded or
  * multiplied. A query row that sees no key gets O = 0 and lse = -inf.
  * FA_ERR_INVALID_ARG for a null mask or negative strides; FA_ERR_UNSUPPORTED
- * for N > 131072. */
+ * for N > 131072 or d > 128. */
 fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
                              const unsigned char* block_mask, long long mask_stride_b, long long mask_stride_h,
                              int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
