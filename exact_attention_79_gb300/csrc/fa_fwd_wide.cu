@@ -18,6 +18,17 @@
 //              32 KB slots, in the order the tensor core consumes them
 //   warp 1     tensor-core issuer (one thread) + TMEM owner
 //   warps 2-5  softmax, one thread per query row
+//   warp 6     ring watcher: waits for V_j to land and adds one arrival to
+//              the P-ready barrier of step j, so the issuing thread learns "P_j
+//              written and V_j resident" from one barrier instead of three
+//              (each poll costs it about as much as issuing two or three MMAs).
+//              K_{j+2} it still waits for itself, just before S_{j+2}: folding
+//              that load into P-ready too would hold P_j V_j back by the load
+//              latency, which the ring's depth does not cover.
+// The ring holds 160 KB against 128 KB of operands in use, so a load can only
+// start about one MMA group before it is needed. The producer therefore also
+// asks L2 for the pieces three items ahead (a prefetch needs no slot), which
+// turns most ring loads into L2 hits.
 // TMEM (512 columns x 128 lanes, fp32): O in columns [0, D), two S buffers at
 // 256 and 384, so S_{j+1} is computed while the softmax works on S_j.
 // Shared memory: Q [128 x D] (D/64 boxes of 128 rows x 128 bytes), then five
@@ -29,6 +40,8 @@
 // Tensor-core order: S_0, S_1, then per key tile j: P_j V_j, S_{j+2}. The
 // rescale of O (only when a row max grows by more than 2^8 in log2 units)
 // waits for the previous P V to complete, which the issuer signals per tile.
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_kernels.h"
 
@@ -42,7 +55,7 @@ struct WideCfg {
   static constexpr int kSlotBytes = 32768;
   static constexpr int kVBoxBytes = 64 * 128;             // 64 keys x 128 bytes
   static constexpr int kSlots = 5;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 256;
   static constexpr int kBarBytes = 256;
@@ -62,7 +75,7 @@ __device__ __forceinline__ int wide_item_k(int j) { return j == 0 ? 0 : 2 * j - 
 __device__ __forceinline__ int wide_item_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
 fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                 const FwdParams p) {
@@ -79,7 +92,12 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   auto bar_empty = [&](int s) { return bars + 40u + 8u * s; };              // kSlots
   const uint32_t bar_q_full = bars + 80;
   auto bar_s_full = [&](int i) { return bars + 88u + 8u * i; };             // 2
-  const uint32_t bar_p_ready = bars + 104;
+  // P-ready of step j is barrier j % 2. A softmax thread that has written P_j
+  // may already hold S_{j+1} (issued a step earlier) and write P_{j+1} before
+  // the slowest thread arrives for step j: with a single barrier that arrival
+  // would count toward step j. S_{j+2} is issued only after step j's barrier
+  // completes, so no thread gets two steps ahead on the same barrier.
+  auto bar_p_ready = [&](int j) { return (j & 1) ? bars + 144u : bars + 104u; };
   const uint32_t bar_pv_done = bars + 112;
   const uint32_t bar_o_final = bars + 120;
   const uint32_t bar_stall = bars + 128;                                    // nothing arrives (timeout test)
@@ -90,11 +108,16 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (query tile, batch*head), heaviest causal tiles first
+  // ---- work item: (query tile, batch*head). Heads go in groups of
+  // p.head_group whose K and V fit in part of L2; inside a group the
+  // heaviest causal tiles come first, so the last CTAs are light ones.
   const int lin = blockIdx.x;
   const int nq = (p.N + kBM - 1) / kBM;
-  const int qt = nq - 1 - lin / p.BH;
-  const int bh = lin % p.BH;
+  const int grp = lin / (nq * p.head_group);
+  const int gsize = min(p.head_group, p.BH - grp * p.head_group);
+  const int local = lin - grp * p.head_group * nq;
+  const int qt = nq - 1 - local / gsize;
+  const int bh = grp * p.head_group + local % gsize;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int nk = (p.Nk + kBN - 1) / kBN;
@@ -114,7 +137,8 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     mbar_init(bar_q_full, 1);
     mbar_init(bar_s_full(0), 1);
     mbar_init(bar_s_full(1), 1);
-    mbar_init(bar_p_ready, 128);
+    mbar_init(bar_p_ready(0), 129);                 // 128 softmax threads + the watcher
+    mbar_init(bar_p_ready(1), 129);
     mbar_init(bar_pv_done, 1);
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
@@ -148,6 +172,23 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         else if ((it & 1) && it <= 2 * n - 3) { is_v = false; j = (it + 1) >> 1; }
         else if (it & 1) { is_v = true; j = n - 1; }
         else { is_v = true; j = (it >> 1) - 1; }
+        if (it + 3 < 2 * n) {
+          // L2 prefetch of item it + 3 (the same decoding as below)
+          const int it3 = it + 3;
+          bool v3;
+          int j3;
+          if ((it3 & 1) && it3 <= 2 * n - 3) { v3 = false; j3 = (it3 + 1) >> 1; }
+          else if (it3 & 1) { v3 = true; j3 = n - 1; }
+          else { v3 = true; j3 = (it3 >> 1) - 1; }
+          for (int bx = 0; bx < C::kNBox; ++bx) {
+            if (v3) {
+              tma_prefetch_l2_3d(&map_v, bx * 64, j3 * kBN, bh_kv);
+              tma_prefetch_l2_3d(&map_v, bx * 64, j3 * kBN + 64, bh_kv);
+            } else {
+              tma_prefetch_l2_3d(&map_k, bx * 64, j3 * kBN, bh_kv);
+            }
+          }
+        }
         for (int pc = 0; pc < 2 && ok; ++pc) {
           const int ld = 2 * it + pc;
           const int slot = ld % C::kSlots;
@@ -178,51 +219,58 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       bool ok = true;
       if (p.test_stall) ok = mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       if (ok) ok = mbar_wait(bar_q_full, 0, abort_flag, deadline);
-      // waits for both slot loads of item `it`; returns their slots
-      auto take = [&](int it, int& s0, int& s1) -> bool {
-        const int l0 = 2 * it, l1 = 2 * it + 1;
-        s0 = l0 % C::kSlots;
-        s1 = l1 % C::kSlots;
-        return mbar_wait(bar_full(s0), (l0 / C::kSlots) & 1, abort_flag, deadline) &&
-               mbar_wait(bar_full(s1), (l1 / C::kSlots) & 1, abort_flag, deadline);
+      // the slots of item `it` (V residency comes folded into P-ready)
+      auto take = [&](int it, int& s0, int& s1) {
+        s0 = (2 * it) % C::kSlots;
+        s1 = (2 * it + 1) % C::kSlots;
       };
-      // S_j = Q K_j^T into S buffer j % 2, then hand the K slots back
+      // S_j = Q K_j^T into S buffer j % 2. Each K piece is waited for just
+      // before the MMAs that read it and handed back right after them, which
+      // gives the second piece's load half an S product more time.
       auto issue_s = [&](int j) -> bool {
+        const int it = wide_item_k(j);
         int s0, s1;
-        if (!take(wide_item_k(j), s0, s1)) return false;
-        tc_fence_after();
+        take(it, s0, s1);
         const uint32_t d_tmem = tbase + C::kColS0 + 128u * (j & 1);
-        const uint32_t kb0 = slot_addr(s0), kb1 = slot_addr(s1);
+        const uint64_t kd0 = smem_desc_sw128(slot_addr(s0), 16, 1024);
+        const uint64_t kd1 = smem_desc_sw128(slot_addr(s1), 16, 1024);
+        if (!mbar_wait(bar_full(s0), ((2 * it) / C::kSlots) & 1, abort_flag, deadline)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int bx = kk / 4;                       // box along d
           const uint32_t in_box = (kk % 4) * 32;       // 16 columns = 32 bytes
-          const uint32_t kaddr = ((bx < 2) ? kb0 : kb1) + (bx & 1) * kBoxBytes + in_box;
-          mma_bf16_ss(d_tmem, desc_add(qdesc, bx * kBoxBytes + in_box), smem_desc_sw128(kaddr, 16, 1024), idesc_qk,
-                      kk > 0);
+          if (kk == 8) {
+            mma_commit(bar_empty(s0));
+            if (!mbar_wait(bar_full(s1), ((2 * it + 1) / C::kSlots) & 1, abort_flag, deadline)) return false;
+            tc_fence_after();
+          }
+          const uint64_t kd = desc_add(bx < 2 ? kd0 : kd1, (bx & 1) * kBoxBytes + in_box);
+          mma_bf16_ss(d_tmem, desc_add(qdesc, bx * kBoxBytes + in_box), kd, idesc_qk, kk > 0);
         }
         mma_commit(bar_s_full(j & 1));
-        mma_commit(bar_empty(s0));
         mma_commit(bar_empty(s1));
         return true;
       };
       if (ok) ok = issue_s(0);
       if (ok && n > 1) ok = issue_s(1);
       for (int j = 0; j < n && ok; ++j) {
-        ok = mbar_wait(bar_p_ready, j & 1, abort_flag, deadline);
+        // P_j written and V_j resident
+        ok = mbar_wait(bar_p_ready(j), (j >> 1) & 1, abort_flag, deadline);
         int s0 = 0, s1 = 0;
-        if (ok) ok = take(wide_item_v(j, n), s0, s1);
+        take(wide_item_v(j, n), s0, s1);
         if (!ok) break;
         tc_fence_after();
         // O += P_j V_j: A = P_j (bf16 pairs in the S buffer), B = V_j, MN-major
         const uint32_t p_tmem = tbase + C::kColS0 + 128u * (j & 1);
+        const uint64_t vd0 = smem_desc_sw128(slot_addr(s0), C::kVBoxBytes, 1024);
+        const uint64_t vd1 = smem_desc_sw128(slot_addr(s1), C::kVBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t vaddr = slot_addr(kk < 4 ? s0 : s1) + (kk % 4) * 16 * 128;
-          mma_bf16_ts(tbase, p_tmem + kk * 8, smem_desc_sw128(vaddr, C::kVBoxBytes, 1024), idesc_pv,
+          mma_bf16_ts(tbase, p_tmem + kk * 8, desc_add(kk < 4 ? vd0 : vd1, (kk % 4) * 16 * 128), idesc_pv,
                       j > 0 || kk > 0);
+          if (kk == 3) mma_commit(bar_empty(s0));    // first 64 keys read
         }
-        mma_commit(bar_empty(s0));
         mma_commit(bar_empty(s1));
         mma_commit(bar_pv_done);
         // S_{j+2} overwrites P_j: issued after the P V that reads it, and one
@@ -230,6 +278,33 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (j + 2 < n) ok = issue_s(j + 2);
       }
       if (ok) mma_commit(bar_o_final);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ ring watcher
+    if (lane == 0 && n > 0) {
+      // A parity wait only tells phase k from phase k-1, so a waiter must know
+      // that the previous load into a slot has landed before it waits for the
+      // next one. The watcher observes every load in ring order; it waits for
+      // K_{j+2} only after its step-j arrival, so that load's latency never
+      // holds P_j V_j back. The issuer waits for the K loads alone: the load
+      // before one of them in the same slot was read by an MMA it issued after
+      // P-ready or after its own wait, so it had landed.
+      auto landed = [&](int it) -> bool {
+        const int l0 = 2 * it, l1 = 2 * it + 1;
+        return mbar_wait(bar_full(l0 % C::kSlots), (l0 / C::kSlots) & 1, abort_flag, deadline) &&
+               mbar_wait(bar_full(l1 % C::kSlots), (l1 / C::kSlots) & 1, abort_flag, deadline);
+      };
+      bool ok = landed(wide_item_k(0));
+      if (ok && n > 1) ok = landed(wide_item_k(1));
+      for (int j = 0; j < n && ok; ++j) {
+        ok = landed(wide_item_v(j, n));
+        // arrive for step j only once step j-2 (the previous phase of the
+        // same barrier) has completed
+        if (ok && j >= 2) ok = mbar_wait(bar_p_ready(j), ((j >> 1) - 1) & 1, abort_flag, deadline);
+        if (ok) mbar_arrive(bar_p_ready(j));
+        if (ok && j + 2 < n) ok = landed(wide_item_k(j + 2));
+      }
     }
     __syncwarp();
   } else {
@@ -321,7 +396,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p_ready);
+      mbar_arrive(bar_p_ready(j));
     }
     // ---------------------------------------------------------- epilogue
     // A query tile that sees no key tile (more queries than keys under the
@@ -395,7 +470,12 @@ static cudaError_t launch_wide(const CUtensorMap& mq, const CUtensorMap& mk, con
     configured = true;
   }
   const long long grid = static_cast<long long>((p.N + kBM - 1) / kBM) * p.BH;
-  fwd_wide_kernel<D><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  // heads per group: their K and V (2 Nk D bf16 each, counted per query head)
+  // within 64 MB, half of L2
+  FwdParams q = p;
+  const long long kv_bytes = 4LL * p.Nk * D;
+  q.head_group = static_cast<int>(std::max(1LL, std::min<long long>(p.BH, (64LL << 20) / kv_bytes)));
+  fwd_wide_kernel<D><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, q);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ struct FwdParams {
   long long mask_sb, mask_sh;
   int mask_nt;                     // tiles per row = ceil(N / 128)
   int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
+  int head_group;                  // wide-head forward: heads scheduled together (set by launch_fwd_wide)
 };
 constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 
