@@ -20,6 +20,9 @@ Sources (web pages on FlashAttention v1/v2/v3):
   * "Flash Attention V3技术解析" (mlqm.cn), section 2.1 ("掩码处理"): causal
     blocks where the key index exceeds the query index are skipped.
 
+`oracle.fp8` adds the FP8 (e4m3, block-scaled) quantiser and the attention of
+dequantised inputs, pinned by tests/test_oracle_fp8.py.
+
 Pins: every function here is checked by tests/test_oracle.py against things
 other than itself (torch float64 scaled-dot-product attention and autograd as
 an independent library routine, a pure-Python brute force, closed forms,
