@@ -40,6 +40,11 @@ SIGNATURES = {
     "fa_bwd_dkdv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_dq": (_I, [_VP, _VP, _SZ, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fp8_row_scales": (_SZ, [_I]),
+    "fa_fp8_vt_keys": (_SZ, [_I]),
+    "fa_fp8_quantize_rows": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
+    "fa_fp8_quantize_v": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
+    "fa_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_device_status": (_I, [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),
@@ -148,6 +153,56 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
         raise ValueError("dtype must be bfloat16 or float32")
     _check(fn, getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                 B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
+    return o, lse
+
+
+def quantize_fp8(q, k, v):
+    """Block-scaled e4m3 copies of bf16 q, k [B, H, N, d] and v (fa_fp8_quantize_rows,
+    fa_fp8_quantize_v): returns (q8, q_scale, k8, k_scale, vt8, v_scale) with
+    q8, k8 uint8 [B, H, N, d], scales fp32 [B, H, ceil(N/64)], vt8 uint8
+    [B, Hkv, d, NP] (V transposed, NP = N rounded up to 128) and v_scale
+    fp32 [B, Hkv, d]."""
+    import torch
+    lib = load()
+    for t in (q, k, v):
+        if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    nb, NP = int(lib.fa_fp8_row_scales(N)), int(lib.fa_fp8_vt_keys(N))
+    dev = q.device
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    vt8 = torch.empty((B, Hkv, d, NP), dtype=torch.uint8, device=dev)
+    qs = torch.empty((B, Hq, nb), dtype=torch.float32, device=dev)
+    ks = torch.empty((B, Hkv, nb), dtype=torch.float32, device=dev)
+    vs = torch.empty((B, Hkv, d), dtype=torch.float32, device=dev)
+    st = _stream(q)
+    _check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(_ptr(q), _ptr(q8), _ptr(qs), B * Hq, N, d, st))
+    _check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(_ptr(k), _ptr(k8), _ptr(ks), B * Hkv, N, d, st))
+    _check("fa_fp8_quantize_v", lib.fa_fp8_quantize_v(_ptr(v), _ptr(vt8), _ptr(vs), B * Hkv, N, d, st))
+    return q8, qs, k8, ks, vt8, vs
+
+
+def fwd_fp8(q8, q_scale, k8, k_scale, vt8, v_scale, causal=False, scale=None, out=None, lse=None):
+    """O (bf16), LSE = attention of block-scaled e4m3 inputs (fa_fwd_fp8), as
+    returned by quantize_fp8."""
+    import torch
+    lib = load()
+    B, Hq, N, d = q8.shape
+    Hkv = k8.shape[1]
+    for t in (q8, q_scale, k8, k_scale, vt8, v_scale):
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("fp8 inputs must be contiguous CUDA tensors")
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check("fa_fwd_fp8", lib.fa_fwd_fp8(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(vt8), _ptr(v_scale),
+                                        _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                        _stream(q8)))
     return o, lse
 
 

@@ -97,7 +97,10 @@ bool make_map(CUtensorMap* m, const void* ptr, int elt_bytes, int d, int N, long
                                  static_cast<cuuint64_t>(d) * N * elt_bytes};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+  const CUtensorMapDataType dt = elt_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUresult r = enc(m, dt, 3,
                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -409,6 +412,68 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq, int Hkv,
                      int N, int d, int causal, float scale, void* stream) {
   return fwd_common(4, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+size_t fa_fp8_row_scales(int N) { return N >= 1 ? static_cast<size_t>((N + 63) / 64) : 0; }
+
+size_t fa_fp8_vt_keys(int N) { return N >= 1 ? static_cast<size_t>((N + 127) / 128 * 128) : 0; }
+
+fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, int N, int d, void* stream) {
+  if (!x || !out || !scales || !aligned16(x) || !aligned16(out) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
+  if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  const fa_status st = device_state(&status);
+  if (st != FA_OK) return st;
+  return fa::launch_fp8_quant_rows(x, out, scales, BH, N, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int N, int d, void* stream) {
+  if (!v || !vt || !scales || !aligned16(v) || !aligned16(vt) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
+  if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  const fa_status st = device_state(&status);
+  if (st != FA_OK) return st;
+  return fa::launch_fp8_quant_v(v, vt, scales, BH, N, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                     const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                     float scale, void* stream) {
+  const void* ptrs[] = {q, q_scale, k, k_scale, vt, v_scale, o, lse};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = device_state(&status);
+  if (st != FA_OK) return st;
+  CUtensorMap mq, mk, mvt, mo;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  const int NP = (N + 127) / 128 * 128;
+  if (!make_map(&mq, q, 1, d, N, BHq) || !make_map(&mk, k, 1, d, N, BHkv) ||
+      !make_map(&mvt, vt, 1, NP, d, BHkv) || !make_map(&mo, o, 2, d, N, BHq))
+    return FA_ERR_CUDA;
+  fa::FwdParams p{};
+  p.lse = lse;
+  p.status = status;
+  p.N = N;
+  p.Nk = N;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.BH = static_cast<int>(BHq);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_limit_ns();
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  return fa::launch_fwd_fp8(mq, mk, mvt, mo, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                   : FA_ERR_CUDA;
 }
 
 fa_status fa_device_status(void* stream) {

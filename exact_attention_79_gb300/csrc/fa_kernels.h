@@ -23,6 +23,11 @@ struct FwdParams {
   int mask_nt;                     // tiles per row = ceil(N / 128)
   int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
   int head_group;                  // wide-head forward: heads scheduled together (set by launch_fwd_wide)
+  // FP8 forward: fp32 scales of the e4m3 inputs; Q and K one per 64-row block
+  // ([BH, ceil(N/64)], [BHkv, ceil(N/64)]), V one per column ([BHkv, d])
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
 };
 constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 
@@ -34,6 +39,18 @@ cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUte
 // map has 64-row boxes (the kernel stages V in 64-key halves).
 cudaError_t launch_fwd_wide(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mo, const FwdParams& p, cudaStream_t stream);
+
+// FP8 (e4m3) path, d = 128. Quantisers: rows of x [BH, N, d] bf16 -> codes
+// [BH, N, d] and one scale per 64-row block; V [BH, N, d] bf16 -> V^T codes
+// [BH, d, NP] (NP = N rounded up to 128, zero codes past N) and one scale per
+// column (`scales` doubles as scratch for the column maxima). The forward
+// reads Q, K codes (maps with 128-byte rows), V^T codes (map over [BH, d, NP])
+// and writes bf16 O and the LSE.
+cudaError_t launch_fp8_quant_rows(const void* x, void* out, float* scales, int BH, int N, int d,
+                                  cudaStream_t stream);
+cudaError_t launch_fp8_quant_v(const void* v, void* vt, float* scales, int BH, int N, int d, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mvt,
+                           const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
 
 struct BwdParams {
   float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows

@@ -112,6 +112,49 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                      int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/* FP8 forward (e4m3 inputs with block scales), d = 128 only.
+ * Source: "Flash Attention V3技术解析", section 1.3 (FP8 operands need the
+ * contracted dimension contiguous, so P V reads V transposed; block-wise
+ * quantisation) and section 3.2 (each block's scale from its largest
+ * magnitude); "4.3 FlashAttention-2与FlashAttention-3演进", FlashAttention-3
+ * section 2. Codes are e4m3 (largest finite value 448, no infinities);
+ * scale = max|block| / 448 in fp32 (1 for an all-zero block); code =
+ * e4m3(x / scale), division in fp32, rounded to nearest even, magnitudes
+ * past 448 held at 448. A value is code * scale.
+ *
+ * fa_fp8_row_scales(N): scales per head of a Q or K tensor, ceil(N / 64).
+ * fa_fp8_vt_keys(N): key columns of the transposed V codes, N rounded up to
+ * 128. Both 0 for N < 1.
+ *
+ * fa_fp8_quantize_rows: x bf16 [BH, N, d] -> out uint8 codes [BH, N, d] and
+ * scales fp32 [BH, fa_fp8_row_scales(N)], one per block of 64 rows over all d
+ * columns (used for Q and for K). */
+size_t fa_fp8_row_scales(int N);
+size_t fa_fp8_vt_keys(int N);
+fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, int N, int d, void* stream);
+
+/* fa_fp8_quantize_v: v bf16 [BH, N, d] -> vt uint8 codes [BH, d, NP]
+ * (NP = fa_fp8_vt_keys(N); row c holds column c of V, keys contiguous, codes
+ * 0 past N) and scales fp32 [BH, d], one per column over all N keys. The
+ * scales buffer is also the call's scratch (column maxima) until it returns
+ * on the stream. Three launches on `stream`. */
+fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int N, int d, void* stream);
+
+/* fa_fwd_fp8: attention of the dequantised inputs, the forward of fa_fwd:
+ * q codes [B, Hq, N, d] with q_scale [B, Hq, ceil(N/64)], k codes
+ * [B, Hkv, N, d] with k_scale [B, Hkv, ceil(N/64)], vt codes [B, Hkv, d, NP]
+ * with v_scale [B, Hkv, d] (as the two calls above write them); o bf16
+ * [B, Hq, N, d], lse fp32 [B, Hq, N]. The products run on e4m3 tensor cores
+ * with fp32 accumulation; the probabilities P (relative to the exact running
+ * row max, so P <= 1) are multiplied by 2^8 and rounded to e4m3 before the
+ * P V product, while the row sum and the LSE use the unrounded values. The
+ * result differs from the exact attention of the dequantised inputs by at
+ * most 2^-4 sum_j P_ij |V_jc| / l_i + 2^-18 sum_j |V_jc| per element, plus
+ * the bf16 rounding of O. FA_ERR_UNSUPPORTED for d != 128. */
+fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                     const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                     float scale, void* stream);
+
 /* Bytes of device workspace fa_bwd needs: fp32 LSE * log2(e) and fp32
  * D = rowsum(dO * O), each [B, Hq, ceil(N/128)*128], and the fp32 dQ
  * accumulator [B, Hq, N, d], each part 256-byte aligned. Returns 0 for invalid

@@ -1,0 +1,119 @@
+"""FP8 (e4m3, block-scaled) forward through the C ABI against the oracle.
+
+The quantisers are integer (byte) work decided in fp32 on both sides, so their
+codes and scales must match oracle/fp8.py bit for bit. The attention must
+match the exact attention of the dequantised inputs within the bound the
+rounding of P to e4m3 allows (oracle.fp8.p_rounding_bound, derived there),
+and the LSE within the dense path's 1e-3 (it uses unrounded probabilities)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8 as ofp8
+import exact_attention_79_gb300 as pkg
+from exact_attention_79_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def quantized(t):
+    g = {n: x.to(DEV) for n, x in t.items()}
+    return pkg.quantize_fp8(g["q"], g["k"], g["v"])
+
+
+def oracle_quant(t):
+    f = {n: inputs.to_f64(x) for n, x in t.items()}
+    qc, qs = ofp8.quantize_rows(f["q"])
+    kc, ks = ofp8.quantize_rows(f["k"])
+    vc, vs = ofp8.quantize_v_transposed(f["v"])
+    return qc, qs, kc, ks, vc, vs
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 2, 2, 128), (2, 3, 1, 333), (1, 4, 2, 1000), (1, 1, 1, 64), (1, 1, 1, 1)])
+def test_fp8_quantisers_bit_exact(fa, B, Hq, Hkv, N):
+    t = inputs.make_inputs(B, Hq, Hkv, N, 128, "bf16", seed=N + Hq)
+    t["q"][:, :, : min(N, 64)] = 0                                   # an all-zero block: scale 1, codes 0
+    got = [x.cpu().numpy() for x in quantized(t)]
+    fa.check_device_status()
+    ref = oracle_quant(t)
+    for name, a, r in zip(("q8", "q_scale", "k8", "k_scale", "vt8", "v_scale"), got, ref):
+        assert a.shape == r.shape, name
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              r.view(np.uint32) if r.dtype == np.float32 else r), name
+
+
+def check_against_bound(o, lse, q8, qs, k8, ks, vt8, vs, causal, scale):
+    deq_q = ofp8.dequantize_rows(q8, qs)
+    deq_k = ofp8.dequantize_rows(k8, ks)
+    deq_v = ofp8.dequantize_v_transposed(vt8, vs, k8.shape[-2])
+    ro, rl = oracle.forward(deq_q, deq_k, deq_v, causal, scale)
+    bound = ofp8.p_rounding_bound(deq_q, deq_k, deq_v, causal, scale, ro)
+    err = np.abs(o - ro)
+    assert (err <= bound).all(), (float(err.max()), float((err - bound).max()))
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.abs(lse[fin] - rl[fin]).max() <= configs.TOL_LSE_MAX
+    return float(err.max()), float(err.mean())
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 2, 2, 128), (2, 4, 2, 333), (1, 2, 1, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_within_rounding_bound(fa, B, Hq, Hkv, N, causal):
+    t = inputs.make_inputs(B, Hq, Hkv, N, 128, "bf16", seed=7 * N + causal)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    print(check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 128 ** -0.5))
+
+
+def test_fp8_forward_rescales_and_sharp_logits(fa):
+    """Keys growing along the sequence and Q x 4: the running max rises often
+    (every rise rescales the accumulator) and the softmax is sharp."""
+    N = 1300
+    t = inputs.make_inputs(1, 2, 2, N, 128, "bf16", seed=77, q_mult=4.0)
+    t["k"] = (t["k"].float() * torch.linspace(0.3, 3.0, N).view(1, 1, N, 1)).to(torch.bfloat16)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    for causal in (True, False):
+        o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+        fa.check_device_status()
+        check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 128 ** -0.5)
+
+
+def test_fp8_forward_full_size_sampled_rows(fa):
+    """16 heads, N = 8192, causal: the oracle computes 128 seeded query rows
+    per head of the dequantised attention and the bound for those rows."""
+    B, H, N, d = 1, 16, 8192, 128
+    t = inputs.make_inputs(B, H, H, N, d, "bf16", seed=8192)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True)
+    fa.check_device_status()
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    deq_q = ofp8.dequantize_rows(host[0], host[1])
+    deq_k = ofp8.dequantize_rows(host[2], host[3])
+    deq_v = ofp8.dequantize_v_transposed(host[4], host[5], N)
+    rows = inputs.sample_rows(B, H, N, 128, seed=4)
+    ro, rl = oracle.forward_rows(deq_q, deq_k, deq_v, True, d ** -0.5, rows)
+    wv, _ = oracle.forward_rows(deq_q, deq_k, np.abs(deq_v), True, d ** -0.5, rows)
+    bi = np.arange(B)[:, None, None]
+    hi = np.arange(H)[None, :, None]
+    # sum_j |V_jc| over the keys each sampled row sees (j <= row)
+    csum = np.cumsum(np.abs(deq_v), axis=2)
+    sum_abs = csum[bi, hi, rows]
+    bound = 2.0 ** -4 * wv + 2.0 ** -18 * sum_abs + 2.0 ** -8 * np.abs(ro) + 1e-6
+    err = np.abs(o[bi, hi, rows] - ro)
+    assert (err <= bound).all(), float((err - bound).max())
+    assert np.abs(lse[bi, hi, rows] - rl).max() <= configs.TOL_LSE_MAX
+
+
+def test_fp8_refuses_other_head_dims(fa):
+    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(pkg.FAError):
+        pkg.quantize_fp8(x, x, x)
+    fa.check_device_status()
