@@ -50,16 +50,22 @@ def parse_args():
 def metric_for(w):
     if w.backward:
         return METRIC
-    return f"attention TFLOPS fwd ({w.dtype}, d={w.d}) and % of GB300 dense BF16 peak"
+    peak = "FP8" if w.dtype == "fp8e4m3" else "BF16"
+    return f"attention TFLOPS fwd ({w.dtype}, d={w.d}) and % of GB300 dense {peak} peak"
 
 
-def peak_tflops():
+def peak_tflops(dtype="bf16"):
+    """Dense tensor peak for the workload's arithmetic: the measured bf16 burst
+    figure; e4m3 takes it times the nominal fp8 : bf16 dense ratio (4.5 : 2.25)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+            peak, src = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except Exception:
-        return FALLBACK_PEAK_TFLOPS, "fallback 1.9 PFLOP/s (MEASURED_PEAKS.json absent)"
+        peak, src = FALLBACK_PEAK_TFLOPS, "fallback 1.9 PFLOP/s (MEASURED_PEAKS.json absent)"
+    if dtype == "fp8e4m3":
+        return 2.0 * peak, src + " x 2 (nominal e4m3 / bf16 dense ratio)"
+    return peak, src
 
 
 # ------------------------------------------------------------------ clocks
@@ -128,8 +134,17 @@ def oracle_slab_runner(w, seed=0):
     import numpy as np
     import oracle
     from exact_attention_79_gb300 import inputs
-    t = inputs.make_inputs(1, 1, 1, w.N, w.d, w.dtype, seed=seed, with_grad=w.backward)
+    t = inputs.make_inputs(1, 1, 1, w.N, w.d, "bf16" if w.dtype == "fp8e4m3" else w.dtype, seed=seed,
+                           with_grad=w.backward)
     f = {k: inputs.to_f64(v) for k, v in t.items()}
+    if w.dtype == "fp8e4m3":
+        # the oracle's attention of the dequantised e4m3 inputs (quantised once, outside the timing)
+        from oracle import fp8 as ofp8
+        qc, qs = ofp8.quantize_rows(f["q"])
+        kc, ks = ofp8.quantize_rows(f["k"])
+        vc, vs = ofp8.quantize_v_transposed(f["v"])
+        f = {"q": ofp8.dequantize_rows(qc, qs), "k": ofp8.dequantize_rows(kc, ks),
+             "v": ofp8.dequantize_v_transposed(vc, vs, w.N)}
 
     def run(rows):
         if not w.backward:
@@ -292,55 +307,83 @@ def native_arm(args, w):
     if fwd_only and (sparse or kvlen or det):
         raise SystemExit("forward-only workloads are dense with equal lengths")
     fwd_name = "fa_fwd" if w.dtype == "bf16" else "fa_fwd_f32"
+    fp8 = w.dtype == "fp8e4m3"
+    if fp8:
+        # e4m3 codes and scales, resident before the timed region
+        q8, qs, k8, ks, vt8, vs = fa.quantize_fp8(q, k, v)
+        torch.cuda.synchronize(dev)
 
-    def step(ev):
+    class Bufs:
+        """Device tensors of one step of the path."""
+
+    main = Bufs()
+    main.__dict__.update(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+    if fp8:
+        main.__dict__.update(q8=q8, qs=qs, k8=k8, ks=ks, vt8=vt8, vs=vs)
+
+    def run(b, sp, mark, quantize=False):
+        """The path's library calls for one step on buffers b and stream sp;
+        mark(i) is called at the points the per-kernel events sit (0 before
+        the forward, 1 after it, 2-4 after the three backward phases)."""
+        def marks(first):
+            for i in range(first, 5):
+                mark(i)
+        if fp8:
+            if quantize:
+                # the user's whole job from bf16 inputs: quantise, then attention
+                check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(P(b.q), P(b.q8), P(b.qs), w.B * w.Hq, w.N,
+                                                                       w.d, sp))
+                check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(P(b.k), P(b.k8), P(b.ks), w.B * w.Hkv, w.N,
+                                                                       w.d, sp))
+                check("fa_fp8_quantize_v", lib.fa_fp8_quantize_v(P(b.v), P(b.vt8), P(b.vs), w.B * w.Hkv, w.N, w.d,
+                                                                 sp))
+            mark(0)
+            check("fa_fwd_fp8", lib.fa_fwd_fp8(P(b.q8), P(b.qs), P(b.k8), P(b.ks), P(b.vt8), P(b.vs), P(b.o),
+                                               P(b.lse), *dims, causal, scale, sp))
+            return marks(1)
         if fwd_only:
-            ev[0].record(stream)
-            check(fwd_name, getattr(lib, fwd_name)(P(q), P(k), P(v), P(o), P(lse), *dims, causal, scale, sptr))
-            for e in ev[1:]:
-                e.record(stream)
-            return
+            mark(0)
+            check(fwd_name, getattr(lib, fwd_name)(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
+            return marks(1)
         if kvlen:
             # queries are the last N of Nk positions (fa_fwd_kv / fa_bwd_kv)
-            ev[0].record(stream)
-            check("fa_fwd_kv", lib.fa_fwd_kv(P(q), P(k), P(v), P(o), P(lse), w.B, w.Hq, w.Hkv, w.N, w.Nk, w.d,
-                                             causal, scale, sptr))
-            ev[1].record(stream)
-            check("fa_bwd_kv", lib.fa_bwd_kv(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), P(ws),
-                                             ws_bytes, w.B, w.Hq, w.Hkv, w.N, w.Nk, w.d, causal, scale, sptr))
-            for e in ev[2:]:
-                e.record(stream)
-            return
+            mark(0)
+            check("fa_fwd_kv", lib.fa_fwd_kv(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), w.B, w.Hq, w.Hkv, w.N, w.Nk,
+                                             w.d, causal, scale, sp))
+            mark(1)
+            check("fa_bwd_kv", lib.fa_bwd_kv(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(b.do), P(b.dq), P(b.dk),
+                                             P(b.dv), P(ws), ws_bytes, w.B, w.Hq, w.Hkv, w.N, w.Nk, w.d, causal,
+                                             scale, sp))
+            return marks(2)
         if sparse:
             # the broadcast mask: byte strides 0 over batch and heads
-            ev[0].record(stream)
-            check("fa_fwd_blocksparse", lib.fa_fwd_blocksparse(P(q), P(k), P(v), P(o), P(lse), P(mask), 0, 0, *dims,
-                                                               causal, scale, sptr))
-            ev[1].record(stream)
-            check("fa_bwd_blocksparse", lib.fa_bwd_blocksparse(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk),
-                                                               P(dv), P(ws), ws_bytes, P(mask), 0, 0, *dims, causal,
-                                                               scale, sptr))
-            for e in ev[2:]:
-                e.record(stream)
-            return
-        ev[0].record(stream)
-        check("fa_fwd", lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), *dims, causal, scale, sptr))
-        ev[1].record(stream)
+            mark(0)
+            check("fa_fwd_blocksparse", lib.fa_fwd_blocksparse(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(mask), 0, 0,
+                                                               *dims, causal, scale, sp))
+            mark(1)
+            check("fa_bwd_blocksparse", lib.fa_bwd_blocksparse(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(b.do),
+                                                               P(b.dq), P(b.dk), P(b.dv), P(ws), ws_bytes, P(mask), 0,
+                                                               0, *dims, causal, scale, sp))
+            return marks(2)
+        mark(0)
+        check("fa_fwd", lib.fa_fwd(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
+        mark(1)
         if det:
             # one call: preprocess, dK/dV pass, dQ pass (no atomics)
-            check("fa_bwd_deterministic", lib.fa_bwd_deterministic(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq),
-                                                                   P(dk), P(dv), P(ws), ws_bytes, *dims, causal,
-                                                                   scale, sptr))
-            for e in ev[2:]:
-                e.record(stream)
-            return
-        check("fa_bwd_preprocess", lib.fa_bwd_preprocess(P(o), P(lse), P(do), P(ws), ws_bytes, *dims, sptr))
-        ev[2].record(stream)
-        check("fa_bwd_dkdv", lib.fa_bwd_dkdv(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes, *dims,
-                                             causal, scale, sptr))
-        ev[3].record(stream)
-        check("fa_bwd_dq", lib.fa_bwd_dq(P(dq), P(ws), ws_bytes, *dims, scale, sptr))
-        ev[4].record(stream)
+            check("fa_bwd_deterministic", lib.fa_bwd_deterministic(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(b.do),
+                                                                   P(b.dq), P(b.dk), P(b.dv), P(ws), ws_bytes, *dims,
+                                                                   causal, scale, sp))
+            return marks(2)
+        check("fa_bwd_preprocess", lib.fa_bwd_preprocess(P(b.o), P(b.lse), P(b.do), P(ws), ws_bytes, *dims, sp))
+        mark(2)
+        check("fa_bwd_dkdv", lib.fa_bwd_dkdv(P(b.q), P(b.k), P(b.v), P(b.do), P(b.dk), P(b.dv), P(ws), ws_bytes,
+                                             *dims, causal, scale, sp))
+        mark(3)
+        check("fa_bwd_dq", lib.fa_bwd_dq(P(b.dq), P(ws), ws_bytes, *dims, scale, sp))
+        mark(4)
+
+    def step(ev):
+        run(main, sptr, lambda i: ev[i].record(stream))
 
     def new_events():
         return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -376,8 +419,8 @@ def native_arm(args, w):
     flops_step = w.flops_fwd + (0.0 if fwd_only else w.flops_bwd)
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
-    fwd_kernel = "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
-    fwd_src = "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
+    fwd_kernel = "fwd_fp8_kernel" if fp8 else "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
+    fwd_src = "fa_fwd_fp8.cu" if fp8 else "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
     names = [fwd_kernel, "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
     if fwd_only:
         names = [fwd_kernel, "-", "-", "-"]
@@ -387,7 +430,7 @@ def native_arm(args, w):
         names = ["fwd_kernel (block-sparse)", "bwd_blocksparse (preprocess + block list + dkdv + dq convert)", "-", "-"]
     if kvlen:
         names = ["fwd_kernel (Nq != Nk)", "bwd_kv (preprocess + dkdv + dq convert)", "-", "-"]
-    peak, peak_src = peak_tflops()
+    peak, peak_src = peak_tflops(w.dtype)
     # dominant kernel of the step and its tensor roofline
     dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if (det or sparse or kvlen) else 2)
     dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
@@ -398,35 +441,69 @@ def native_arm(args, w):
                 "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
                 "algorithmic_flops_per_launch": dom_flops}
 
-    # ---- end to end: pinned host inputs -> device, the four calls, results -> host
+    # ---- end to end: pinned host inputs -> device, the path, results -> host,
+    # every step. Steps are pipelined the way a user would drive the library:
+    # the copy in of step i+1 and the copy out of step i-1 run on their own
+    # streams while step i computes, over two sets of device buffers.
     e2e = None
     if args.e2e_steps > 0:
-        dev_in = (q, k, v) if fwd_only else (q, k, v, do)
-        dev_out = (o, lse) if fwd_only else (o, lse, dq, dk, dv)
-        host_in = [x.cpu().pin_memory() for x in dev_in]
-        host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in dev_out]
+        names_in = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
+        names_out = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
+        host_in = [getattr(main, n).cpu().pin_memory() for n in names_in]
+        host_out = [[torch.empty(getattr(main, n).shape, dtype=getattr(main, n).dtype).pin_memory()
+                     for n in names_out] for _ in range(2)]
         h2d = sum(x.numel() * x.element_size() for x in host_in)
-        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        d2h = sum(x.numel() * x.element_size() for x in host_out[0])
+        sets = [main, Bufs()]
+        for n in names_in + names_out:
+            setattr(sets[1], n, torch.empty_like(getattr(main, n)))
+        if fp8:
+            for n in ("q8", "qs", "k8", "ks", "vt8", "vs"):
+                setattr(sets[1], n, torch.empty_like(getattr(main, n)))
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_comp = stream
+        done_in = [torch.cuda.Event() for _ in range(2)]
+        done_comp = [torch.cuda.Event() for _ in range(2)]
+        done_out = [torch.cuda.Event() for _ in range(2)]
+        started = [False, False]
 
-        def e2e_step():
-            for dst, src in zip(dev_in, host_in):
-                dst.copy_(src, non_blocking=True)
-            step(new_events())
-            for dst, src in zip(host_out, dev_out):
-                dst.copy_(src, non_blocking=True)
-        for _ in range(3):
-            e2e_step()
+        def e2e_step(i):
+            x = i % 2
+            b = sets[x]
+            with torch.cuda.stream(s_in):
+                if started[x]:
+                    s_in.wait_event(done_comp[x])       # step i-2 has finished reading set x
+                for n, src in zip(names_in, host_in):
+                    getattr(b, n).copy_(src, non_blocking=True)
+                done_in[x].record(s_in)
+            s_comp.wait_event(done_in[x])
+            if started[x]:
+                s_comp.wait_event(done_out[x])          # step i-2's results have left set x
+            run(b, s_comp.cuda_stream, lambda _i: None, quantize=True)
+            done_comp[x].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_comp[x])
+                for n, dst in zip(names_out, host_out[x]):
+                    dst.copy_(getattr(b, n), non_blocking=True)
+                done_out[x].record(s_out)
+            started[x] = True
+
+        for i in range(4):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record(stream)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        for x in range(2):
+            s_out.wait_event(done_out[x])
+        z.record(s_out)
         torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, world)
+        e2e_ms = max_over_ranks(a.elapsed_time(z) / args.e2e_steps, world)
         fa.check_device_status(stream.cuda_stream)
         e2e = {"value": world * flops_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "pipelining": "copy in, compute, copy out on three streams over two device buffer sets"}
 
     if rank != 0:
         return
@@ -447,7 +524,7 @@ def native_arm(args, w):
         "roofline": roofline,
         "e2e": e2e,
         # fwd, preprocess, [block list], dK/dV, dQ convert
-        "gpu_launches": (1 if fwd_only else 5 if sparse else 4) * args.steps,
+        "gpu_launches": (1 if (fwd_only or fp8) else 5 if sparse else 4) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t1 - t0,
     }

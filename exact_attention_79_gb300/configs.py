@@ -11,7 +11,8 @@ from dataclasses import dataclass
 @dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str          # "fp32" or "bf16": the element type of q, k, v, o (and grads)
+    dtype: str          # "fp32" or "bf16": the element type of q, k, v, o (and grads);
+    #                     "fp8e4m3": bf16 q, k, v quantised to block-scaled e4m3, bf16 o
     B: int
     Hq: int
     Hkv: int
@@ -91,6 +92,8 @@ WORKLOADS = {
         "bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd", "bf16", 1, 32, 8, 4096, 128, True, True, Nk=32768),
     # block-sparse local attention (a window of 16 key tiles = 2048 keys, causal), 16 heads, N=32768
     "bf16_h16_n32768_d128_local16_fwdbwd": Workload("bf16_h16_n32768_d128_local16_fwdbwd", "bf16", 1, 16, 16, 32768, 128, True, True, block_window=16),
+    # FP8 (e4m3, block-scaled) forward, same shape as the d = 128 fwd+bwd case; the bf16 inputs are quantised first
+    "fp8_h16_n8192_d128_causal_fwd": Workload("fp8_h16_n8192_d128_causal_fwd", "fp8e4m3", 1, 16, 16, 8192, 128, True, False),
     # head dimension 256 (forward; the wide-head kernel), same N and heads as the d = 128 fwd+bwd case
     "bf16_h16_n8192_d256_causal_fwd": Workload("bf16_h16_n8192_d256_causal_fwd", "bf16", 1, 16, 16, 8192, 256, True, False),
 }

@@ -42,7 +42,8 @@ def make_workload_inputs(w, seed=0, with_grad=None):
     """Inputs for a configs.Workload."""
     if with_grad is None:
         with_grad = w.backward
-    return make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.dtype, seed, w.q_mult, with_grad, Nk=(w.Nk or None))
+    storage = "bf16" if w.dtype == "fp8e4m3" else w.dtype      # fp8 inputs start as bf16 and are quantised
+    return make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, storage, seed, w.q_mult, with_grad, Nk=(w.Nk or None))
 
 
 def sample_rows(B, H, N, count, seed):
