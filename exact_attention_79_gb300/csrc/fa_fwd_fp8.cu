@@ -17,15 +17,22 @@
 // out of P V and are applied to the output columns. V is stored transposed,
 // [BH, d, NP] with NP = N rounded up to 128 and zero codes past N.
 //
-// Attention kernel: the bf16 forward's layout (two ping-ponged 128-row query
-// tiles per CTA, producer, issuer, two softmax groups of four warps, ring
-// watcher; TMEM S0 | S1 | O0 | O1) with kind::f8f6f4 MMAs, 16 KB tiles, and:
+// Attention kernel: two 128-row query tiles per CTA (producer, issuer, two
+// softmax groups of four warps, ring watcher; TMEM S0 | S1 | O0 | O1) with
+// kind::f8f6f4 MMAs on 16 KB tiles, and:
 //   * logits = S * scale * sq(row block) * sk(key block), the key scale
 //     changing at column 64 of each 128-key tile;
-//   * the running max is exact (a rescale whenever it grows), so P <= 1;
-//     P * 2^8 (the 2^8 folded into the exponent) is rounded to e4m3 and
-//     written over S, four codes per TMEM column, as the A operand of P V;
-//     the row sum uses the unrounded values;
+//   * the accumulator is rescaled only when a row max grows by more than
+//     2^4 (log2 units), so P <= 2^4 relative to the running max; 2^4 P (the
+//     2^4 folded into the exponent, at most 256 < 448) is rounded to e4m3
+//     into one of two shared-memory P buffers per tile, the A operand of P V;
+//     the row sum uses the unrounded values. A rescale waits for the previous
+//     P V, so an exact running max (a rescale on most early tiles) would put
+//     that wait on the softmax's path;
+//   * a softmax group signals "S consumed" as soon as S_j is in its registers,
+//     so S_{j+1} is computed while it works: at e4m3 rate the tensor work of a
+//     key tile is shorter than the softmax, and the chain S ready -> softmax ->
+//     P V -> next S would otherwise leave the tensor core idle;
 //   * O column c is multiplied by V's scale of column c and divided by l.
 #include "fa_common.cuh"
 #include "fa_kernels.h"
@@ -35,11 +42,11 @@ namespace {
 
 constexpr int kD = 128;                  // head dimension of this path
 constexpr int kTile = 128 * 128;         // 128 rows x 128 e4m3 codes: one TMA box
-constexpr int kQRegion = 2 * kTile;      // a query tile's region: its codes, later its bf16 O
-constexpr int kStages = 10;              // K / V^T ring slots
+constexpr int kQRegion = 2 * kTile;      // a query tile's region: its codes and P buffer 0, later its bf16 O
+constexpr int kStages = 8;               // K / V^T ring slots
 constexpr int kThreads = 352;
 constexpr int kBarBytes = 512;
-constexpr int kSmem = 2 * kQRegion + kStages * kTile + kBarBytes + 1024;
+constexpr int kSmem = 2 * kQRegion + 2 * kTile + kStages * kTile + kBarBytes + 1024;   // + P buffers 1
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 constexpr float kE4m3Max = 448.0f;
 constexpr int kRowBlock = 64;            // rows per Q / K scale
@@ -168,18 +175,28 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
 
+  // query region i: Q codes, then P buffer 0 of group i (later the bf16 O tile)
   const uint32_t s_q[2] = {base, base + kQRegion};
-  const uint32_t s_kv = base + 2 * kQRegion;
+  const uint32_t s_p1[2] = {base + 2 * kQRegion, base + 2 * kQRegion + kTile};     // P buffer 1 of group i
+  const uint32_t s_kv = base + 2 * kQRegion + 2 * kTile;
   const uint32_t bars = s_kv + kSt * kTile;
+  auto p_buf = [&](int i, int j) { return (j & 1) ? s_p1[i] : s_q[i] + kTile; };
   auto bar_q_full = [&](int i) { return bars + 8u * i; };
   auto bar_kv_full = [&](int s) { return bars + 16u + 8u * s; };
   auto bar_kv_empty = [&](int s) { return bars + 16u + 8u * (kSt + s); };
   auto bar_s_full = [&](int i) { return bars + 16u + 16u * kSt + 8u * i; };
-  auto bar_p_ready = [&](int i) { return bars + 32u + 16u * kSt + 8u * i; };
-  auto bar_o_final = [&](int i) { return bars + 48u + 16u * kSt + 8u * i; };
+  auto bar_s_cons = [&](int i) { return bars + 32u + 16u * kSt + 8u * i; };
+  // P-ready of tile i at step j is barrier (i, j % 2): a warp that holds S_{j+1}
+  // early may write P_{j+1} before a slower warp (or the watcher) arrived for
+  // step j, and that arrival must not count toward step j. No warp gets two
+  // steps ahead: S_{j+2} waits for S-consumed of step j+1, i.e. for every warp
+  // to be past step j, and for the watcher's step-j arrival before it.
+  auto bar_p_ready = [&](int i, int j) { return bars + 48u + 16u * kSt + 16u * i + 8u * (j & 1); };
+  auto bar_pv_done = [&](int i) { return bars + 80u + 16u * kSt + 8u * i; };
+  auto bar_o_final = [&](int i) { return bars + 96u + 16u * kSt + 8u * i; };
   uint8_t* const gbars = gbase + (bars - base);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 64 + 16 * kSt);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 68 + 16 * kSt);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 112 + 16 * kSt);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 116 + 16 * kSt);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -203,7 +220,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
       mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_p_ready(i), 129);                  // 128 softmax threads + the ring watcher
+      mbar_init(bar_s_cons(i), 129);                   // 128 softmax threads + the ring watcher
+      mbar_init(bar_p_ready(i, 0), 129);
+      mbar_init(bar_p_ready(i, 1), 129);
+      mbar_init(bar_pv_done(i), 1);
       mbar_init(bar_o_final(i), 1);
     }
     for (int s = 0; s < kSt; ++s) {
@@ -247,6 +267,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issuer
+    // Per key tile j: S_i(j+1) for each query tile as soon as its softmax has
+    // read S_i(j) out of TMEM (and K_{j+1} has landed), then P_i(j) V_j as
+    // soon as P_i(j) is in shared memory (and V_j has landed). Ring slots go
+    // back by commits after their last reader.
     if (lane == 0) {
       const uint32_t idesc = make_idesc(0, 128, 128, 0, 0);   // e4m3 x e4m3 -> f32, both K-major
       bool ok = true;
@@ -258,16 +282,14 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         for (int kk = 0; kk < kD / 32; ++kk)
           mma_fp8_ss(tbase + 128u * i, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc, kk > 0);
       };
-      auto issue_pv = [&](int i, uint32_t svt, bool acc) {
-        const uint64_t vd = smem_desc_sw128(svt, 16, 1024);
+      auto issue_pv = [&](int i, uint32_t sp, uint32_t svt, bool acc) {
+        const uint64_t pd = smem_desc_sw128(sp, 16, 1024), vd = smem_desc_sw128(svt, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
-          mma_fp8_ts(tbase + 256u + 128u * i, tbase + 128u * i + kk * 8, desc_add(vd, kk * 32), idesc, acc || kk > 0);
+          mma_fp8_ss(tbase + 256u + 128u * i, desc_add(pd, kk * 32), desc_add(vd, kk * 32), idesc, acc || kk > 0);
       };
-      int c = 0;
       if (ok && nmax > 0) {
-        ok = mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
-        c = 1;
+        ok = mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);     // K_0: only the issuer needs it first
         if (ok) {
           tc_fence_after();
           for (int i = 0; i < 2; ++i) {
@@ -275,59 +297,60 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             issue_qk(i, s_kv);
             mma_commit(bar_s_full(i));
           }
+          mma_commit(bar_kv_empty(0));
         }
       }
       for (int j = 0; j < nmax && ok; ++j) {
-        // residency of V_j and K_{j+1} is folded into the P-ready barriers
-        const uint32_t svt = s_kv + (c % kSt) * kTile;
-        ++c;
-        uint32_t sk_next = 0;
-        if (j + 1 < nmax) {
-          sk_next = s_kv + (c % kSt) * kTile;
-          ++c;
-        }
-        for (int i = 0; i < 2; ++i) {
-          if (j >= nkv[i]) continue;
-          if (!mbar_wait(bar_p_ready(i), j & 1, abort_flag, deadline)) { ok = false; break; }
+        const int slot_k = (2 * j + 2) % kSt, slot_v = (2 * j + 1) % kSt;
+        bool any_s = false;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j + 1 >= nkv[i]) continue;
+          ok = mbar_wait(bar_s_cons(i), j & 1, abort_flag, deadline);   // S_i(j) read out, K_{j+1} landed
+          if (!ok) break;
           tc_fence_after();
-          issue_pv(i, svt, j > 0);
-          if (j + 1 < nkv[i]) {
-            issue_qk(i, sk_next);
-            mma_commit(bar_s_full(i));
-          } else {
-            mma_commit(bar_o_final(i));
-          }
+          issue_qk(i, s_kv + slot_k * kTile);
+          mma_commit(bar_s_full(i));
+          any_s = true;
         }
+        if (!ok) break;
+        if (any_s) mma_commit(bar_kv_empty(slot_k));
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j >= nkv[i]) continue;
+          ok = mbar_wait(bar_p_ready(i, j), (j >> 1) & 1, abort_flag, deadline);  // P_i(j) written, V_j landed
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(i, p_buf(i, j), s_kv + slot_v * kTile, j > 0);
+          mma_commit(bar_pv_done(i));
+          if (j + 1 == nkv[i]) mma_commit(bar_o_final(i));
+        }
+        if (ok) mma_commit(bar_kv_empty(slot_v));
       }
     }
     __syncwarp();
   } else if (warp == 10) {
     // ------------------------------------------------------------ ring watcher
+    // Folds "V_j landed" into P-ready(i, j) and "K_{j+1} landed" into
+    // S-consumed(i, j). Parity waits only tell phase k from phase k-1, so it
+    // observes every load in ring order (K_0 included) and arrives for a
+    // phase only once the previous phase of that barrier has completed.
     if (lane == 0) {
-      // L: the group whose S MMAs are issued last in each step (group 1 unless absent)
-      const int L = (nkv[1] == nmax) ? 1 : 0;
-      // parity waits only tell phase k from phase k-1: observe every load in
-      // order, starting with K_0, which only the issuer needs
       bool ok = nmax == 0 || mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
-      auto hand_p = [&](int i, int j) {
-        if (j > 0) ok = mbar_wait(bar_p_ready(i), (j - 1) & 1, abort_flag, deadline);
-        if (ok) mbar_arrive(bar_p_ready(i));
-      };
       for (int j = 0; j < nmax && ok; ++j) {
         const int cv = 2 * j + 1;
         ok = mbar_wait(bar_kv_full(cv % kSt), (cv / kSt) & 1, abort_flag, deadline);
-        if (ok && j + 1 < nmax) {
-          const int ck = 2 * j + 2;
-          ok = mbar_wait(bar_kv_full(ck % kSt), (ck / kSt) & 1, abort_flag, deadline);
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j >= nkv[i]) continue;
+          if (j >= 2) ok = mbar_wait(bar_p_ready(i, j), ((j >> 1) - 1) & 1, abort_flag, deadline);
+          if (ok) mbar_arrive(bar_p_ready(i, j));
         }
-        if (ok && L == 1 && j < nkv[0]) hand_p(0, j);
-        // S_L(j) done: issued after every MMA that reads K_j or V_{j-1}
-        if (ok) ok = mbar_wait(bar_s_full(L), j & 1, abort_flag, deadline);
-        if (ok) {
-          mbar_arrive(bar_kv_empty((2 * j) % kSt));
-          if (j > 0) mbar_arrive(bar_kv_empty((2 * j - 1) % kSt));
+        if (!ok || j + 1 >= nmax) continue;
+        const int ck = 2 * j + 2;
+        ok = mbar_wait(bar_kv_full(ck % kSt), (ck / kSt) & 1, abort_flag, deadline);
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j + 1 >= nkv[i]) continue;
+          if (j > 0) ok = mbar_wait(bar_s_cons(i), (j - 1) & 1, abort_flag, deadline);
+          if (ok) mbar_arrive(bar_s_cons(i));
         }
-        if (ok) hand_p(L, j);
       }
     }
     __syncwarp();
@@ -345,8 +368,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const float sq = p.q_scale[static_cast<size_t>(bh) * nqb + min(q_row / kRowBlock, nqb - 1)];
     const float* ksc = p.k_scale + static_cast<size_t>(bh_kv) * nqb;
     const float csq = p.scale_log2 * sq;
-    float m = -INFINITY;                           // exact running max, log2 units
-    float l = 0.f;                                 // running sum of 2^8 P
+    float m = -INFINITY;                           // running max (up to 2^4 stale), log2 units
+    float l = 0.f;                                 // running sum of 2^4 P
     bool ok = n_kv > 0;
     for (int j = 0; j < n_kv && ok; ++j) {
       ok = mbar_wait(bar_s_full(g), j & 1, abort_flag, deadline);
@@ -359,6 +382,11 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tmem_wait_ld();
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+      if (j + 1 < n_kv) {
+        // S_j is in registers: the tensor core may write S_{j+1} over it
+        tc_fence_before();
+        mbar_arrive(bar_s_cons(g));
+      }
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -383,30 +411,45 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         mk[k] = fmaxf(a, v[31]);
       }
       const float mx = fmaxf(fmaxf(mk[0], mk[1]) * c0, fmaxf(mk[2], mk[3]) * c1);
-      const bool grow = mx > m;
+      const bool grow = mx > m + 4.0f;             // also true on the first tile (m = -inf)
       const float m_new = grow ? mx : m;
       const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
       m = m_new;
-      // 2^8 P = 2^(s c - m + 8); a row with no visible key yet keeps P = 0
-      const float off = (m == -INFINITY) ? 0.f : 8.0f - m;
+      // 2^4 P = 2^(s c - m + 4) <= 256; a row with no visible key yet keeps P = 0
+      const float off = (m == -INFINITY) ? 0.f : 4.0f - m;
       float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pr[32];
+      // P_j codes into shared memory buffer j % 2 (K-major, 128-byte swizzle),
+      // 16 codes per store; the P V that read this buffer two tiles ago has
+      // completed (it was issued before S_j)
+      const uint32_t pb = p_buf(g, j);
 #pragma unroll
-      for (int w = 0; w < 32; ++w) {
-        const float cm = (w < 16) ? c0 : c1;
-        float x0, x1, x2, x3;
-        fma2_bc(x0, x1, s[4 * w], s[4 * w + 1], cm, off);
-        fma2_bc(x2, x3, s[4 * w + 2], s[4 * w + 3], cm, off);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        add2_acc(sum0, sum1, p0, p1);
-        add2_acc(sum0, sum1, p2, p3);
-        pr[w] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+      for (int u = 0; u < 8; ++u) {
+        const float cm = (u < 4) ? c0 : c1;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 16 * u + 4 * e;
+          float x0, x1, x2, x3;
+          fma2_bc(x0, x1, s[c], s[c + 1], cm, off);
+          fma2_bc(x2, x3, s[c + 2], s[c + 3], cm, off);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          add2_acc(sum0, sum1, p0, p1);
+          add2_acc(sum0, sum1, p2, p3);
+          w[e] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(pb, row, u)),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
       }
-      tmem_st_32x32b_x32(t_s, pr);
       l = l * alpha + (sum0 + sum1);
-      // O <- alpha O before the next P V accumulates; the previous P V of this
-      // tile completed before the S MMA just waited for
+      // O <- alpha O before P_j V_j accumulates. P_{j-1} V_{j-1} may still be
+      // running (S_j was issued before it), so wait for it: phases of that
+      // barrier up to j-2 have completed and phase j cannot complete before
+      // this thread's P_j, so the parity wait is unambiguous.
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        bool w = mbar_wait(bar_pv_done(g), (j - 1) & 1, abort_flag, deadline);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < kD; cc += 32) {
           uint32_t o[32];
@@ -417,10 +460,11 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           tmem_st_32x32b_x32(t_o + cc, o);
         }
+        tmem_wait_st();
       }
-      tmem_wait_st();
+      fence_proxy_async_smem();                    // the P codes, for the tensor core
       tc_fence_before();
-      mbar_arrive(bar_p_ready(g));
+      mbar_arrive(bar_p_ready(g, j));
     }
     // ---------------------------------------------------------- epilogue
     const bool empty = has_tile[g] && n_kv == 0;
@@ -432,7 +476,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float* vsc = p.v_scale + static_cast<size_t>(bh_kv) * kD;
-      // bf16 O staged over this tile's region (its Q codes are no longer read)
+      // bf16 O staged over this tile's region (its Q codes and P buffer 0 are
+      // no longer read: every MMA of this tile has completed)
       const uint32_t stage = s_q[g];
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -461,9 +506,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         }
       }
       fence_proxy_async_smem();
-      // LSE = ln(sum_j e^{logit}) = (m + log2(l) - 8) ln 2, l holding 2^8 P
+      // LSE = ln(sum_j e^{logit}) = (m + log2(l) - 4) ln 2, l holding 2^4 P
       if (q_row < p.N)
-        p.lse[static_cast<size_t>(bh) * p.N + q_row] = l > 0.f ? (m + log2f(l) - 8.0f) * kLn2 : -INFINITY;
+        p.lse[static_cast<size_t>(bh) * p.N + q_row] = l > 0.f ? (m + log2f(l) - 4.0f) * kLn2 : -INFINITY;
     }
     named_bar_sync(1 + g, 128);
     if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {

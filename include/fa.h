@@ -145,12 +145,14 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
  * [B, Hkv, N, d] with k_scale [B, Hkv, ceil(N/64)], vt codes [B, Hkv, d, NP]
  * with v_scale [B, Hkv, d] (as the two calls above write them); o bf16
  * [B, Hq, N, d], lse fp32 [B, Hq, N]. The products run on e4m3 tensor cores
- * with fp32 accumulation; the probabilities P (relative to the exact running
- * row max, so P <= 1) are multiplied by 2^8 and rounded to e4m3 before the
- * P V product, while the row sum and the LSE use the unrounded values. The
- * result differs from the exact attention of the dequantised inputs by at
- * most 2^-4 sum_j P_ij |V_jc| / l_i + 2^-18 sum_j |V_jc| per element, plus
- * the bf16 rounding of O. FA_ERR_UNSUPPORTED for d != 128. */
+ * with fp32 accumulation; the probabilities P (relative to a running row max
+ * that may trail the true one by up to a factor 2^4, so P <= 2^4) are
+ * multiplied by 2^4 and rounded to e4m3 before the P V product, while the
+ * row sum and the LSE use the unrounded values. With P_ij = exp(s_ij - max_j
+ * s_ij) and l_i = sum_j P_ij, the result differs from the exact attention of
+ * the dequantised inputs by at most 2^-4 sum_j (P_ij / l_i)|V_jc| +
+ * 2^-14 sum_j |V_jc| / l_i per element (visible keys j), plus the bf16
+ * rounding of O. FA_ERR_UNSUPPORTED for d != 128. */
 fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
                      const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
                      float scale, void* stream);

@@ -30,9 +30,11 @@ Readings where the pages leave a step open (also listed in the design notes):
     all its keys; it multiplies column c of the output.
   * V is stored transposed, [B, Hkv, d, NP] with NP = N rounded up to 128 and
     zero codes past N, the K-contiguous layout the page asks for.
-  * P is rounded to e4m3 for the P V product after multiplying by 2^8, which
-    keeps probabilities down to 2^-17 representable (P <= 1 because the
-    running max is exact in this path); the row sum l uses the unrounded P.
+  * P is rounded to e4m3 for the P V product after multiplying by 2^4. The
+    running max is allowed to lag the true one by up to 2^4 (as the bf16
+    path lets it lag by 2^8) before the accumulator is rescaled, so
+    P <= 2^4 and 2^4 P <= 256 stays inside e4m3's range; the row sum l uses
+    the unrounded P.
 
 What the CUDA path must match: the quantiser bit for bit (an integer
 encoding decided in fp32 on both sides), and the attention of the dequantised
@@ -51,7 +53,7 @@ from .attention import forward
 E4M3_MAX = 448.0
 ROW_BLOCK = 64            # rows per Q / K scale block
 KEY_PAD = 128             # V^T rows are padded to a multiple of this many keys
-P_SCALE = 256.0           # P is rounded as e4m3(P * 2^8)
+P_SCALE = 16.0            # P (relative to a running max up to 2^4 stale) is rounded as e4m3(P * 2^4)
 
 
 def e4m3_decode(codes):
@@ -150,14 +152,35 @@ def forward_fp8(q_codes, q_scales, k_codes, k_scales, vt_codes, v_scales, causal
     return forward(q, k, v, causal, scale)
 
 
-def p_rounding_bound(q, k, v, causal, scale, o_ref):
+def p_rounding_bound(q, k, v, causal, scale, o_ref, rows=None):
     """Per-element bound on |O_fp8 - O| for dequantised inputs q, k, v
-    (float64) and the exact O: rounding P * 2^8 to e4m3 moves each normal
-    value by at most 2^-4 of itself and each subnormal one by at most 2^-10,
-    i.e. 2^-18 in P; with l >= 1 (the row max contributes 1) the output
-    moves by at most 2^-4 sum_j (P_j / l)|V_j| + 2^-18 sum_j |V_j|. Add the
-    bf16 rounding of the result (2^-9 relative, taken as 2^-8) and 1e-6."""
-    w_abs_v, _ = forward(q, k, np.abs(v), causal, scale)      # sum_j softmax_j |V_j|
-    G = q.shape[1] // k.shape[1]
-    sum_abs_v = np.repeat(np.abs(v).sum(axis=-2, keepdims=True), G, axis=1)
-    return 2.0 ** -4 * w_abs_v + 2.0 ** -18 * sum_abs_v + 2.0 ** -8 * np.abs(o_ref) + 1e-6
+    (float64) and the exact O (o_ref: [B, Hq, N, d], or [B, Hq, R, d] for
+    the query rows `rows` [B, Hq, R]).
+
+    Let P_j = exp(s_j - max s) and l = sum_j P_j (true units, l >= 1). The
+    kernel rounds P'_j * 2^4 to e4m3 where P'_j = P_j 2^(m - m') >= P_j is
+    relative to a running max m' that trails the true max m by at most 2^4
+    (log2 units). Where P_j 2^4 is a normal e4m3 value so is P'_j 2^4, and
+    the rounding moves it by at most 2^-4 of itself; elsewhere by at most
+    half a subnormal step, 2^-10 / 2^4 = 2^-14 in P' units, which is no more
+    in P units. Both the sum and l scale alike, so
+      |dO_c| <= 2^-4 sum_j (P_j / l)|V_jc| + 2^-14 sum_(visible j) |V_jc| / l.
+    Add the bf16 rounding of the result (2^-9 relative, taken as 2^-8) and
+    1e-6."""
+    B, Hq, N, d = q.shape
+    G = Hq // k.shape[1]
+    sub = 2.0 ** -10 / P_SCALE
+    out = np.empty_like(o_ref, dtype=np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            r = np.arange(N) if rows is None else np.asarray(rows[b, h])
+            kh, vh = k[b, h // G], v[b, h // G]
+            s = (q[b, h, r] @ kh.T) * scale
+            visible = np.ones(s.shape, bool) if not causal else (np.arange(kh.shape[0])[None, :] <= r[:, None])
+            s = np.where(visible, s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            l = p.sum(axis=1, keepdims=True)
+            av = np.abs(vh)
+            out[b, h] = (2.0 ** -4 * ((p / l) @ av) + sub * ((visible @ av) / l)
+                         + 2.0 ** -8 * np.abs(o_ref[b, h]) + 1e-6)
+    return out

@@ -71,7 +71,8 @@ def test_fp8_forward_within_rounding_bound(fa, B, Hq, Hkv, N, causal):
 
 def test_fp8_forward_rescales_and_sharp_logits(fa):
     """Keys growing along the sequence and Q x 4: the running max rises often
-    (every rise rescales the accumulator) and the softmax is sharp."""
+    by more than 2^4 several times, rescaling the accumulator, and the softmax
+    is sharp."""
     N = 1300
     t = inputs.make_inputs(1, 2, 2, N, 128, "bf16", seed=77, q_mult=4.0)
     t["k"] = (t["k"].float() * torch.linspace(0.3, 3.0, N).view(1, 1, N, 1)).to(torch.bfloat16)
@@ -100,13 +101,9 @@ def test_fp8_forward_full_size_sampled_rows(fa):
     deq_v = ofp8.dequantize_v_transposed(host[4], host[5], N)
     rows = inputs.sample_rows(B, H, N, 128, seed=4)
     ro, rl = oracle.forward_rows(deq_q, deq_k, deq_v, True, d ** -0.5, rows)
-    wv, _ = oracle.forward_rows(deq_q, deq_k, np.abs(deq_v), True, d ** -0.5, rows)
+    bound = ofp8.p_rounding_bound(deq_q, deq_k, deq_v, True, d ** -0.5, ro, rows=rows)
     bi = np.arange(B)[:, None, None]
     hi = np.arange(H)[None, :, None]
-    # sum_j |V_jc| over the keys each sampled row sees (j <= row)
-    csum = np.cumsum(np.abs(deq_v), axis=2)
-    sum_abs = csum[bi, hi, rows]
-    bound = 2.0 ** -4 * wv + 2.0 ** -18 * sum_abs + 2.0 ** -8 * np.abs(ro) + 1e-6
     err = np.abs(o[bi, hi, rows] - ro)
     assert (err <= bound).all(), float((err - bound).max())
     assert np.abs(lse[bi, hi, rows] - rl).max() <= configs.TOL_LSE_MAX

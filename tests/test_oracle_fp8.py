@@ -135,9 +135,10 @@ def test_forward_fp8_is_dense_oracle_of_dequantised_inputs():
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_p_rounding_bound_covers_rounded_probabilities(causal):
-    """Emulate the kernel's approximation directly: round P * 2^8 (P relative
-    to the exact row max) to e4m3, keep l unrounded, and check the result
-    stays within the bound."""
+    """Emulate the kernel's approximation directly: round P' * 2^4 to e4m3,
+    where P' is relative to a running max that trails the true one by a
+    random amount up to 2^4 per row (the kernel's lazy rescale), keep l
+    unrounded, and check the result stays within the bound."""
     rng = np.random.default_rng(10 + causal)
     N, d = 300, 128
     q = rng.normal(0, 1, (1, 1, N, d)) * 2.0
@@ -148,10 +149,15 @@ def test_p_rounding_bound_covers_rounded_probabilities(causal):
     s = (q[0, 0] @ k[0, 0].T) * scale
     if causal:
         s = np.where(np.tril(np.ones((N, N), bool)), s, -np.inf)
-    p = np.exp(s - s.max(axis=1, keepdims=True))
-    l = p.sum(axis=1, keepdims=True)
-    p_r = fp8.e4m3_decode(fp8.e4m3_encode((p * 256.0).astype(np.float32))) / 256.0
+    lag = rng.uniform(0, 4, (N, 1)) * np.log(2.0)               # m - m' in natural-log units
+    p_stale = np.exp(s - s.max(axis=1, keepdims=True) + lag)   # P' <= 2^4
+    l = p_stale.sum(axis=1, keepdims=True)
+    p_r = fp8.e4m3_decode(fp8.e4m3_encode((p_stale * fp8.P_SCALE).astype(np.float32))) / fp8.P_SCALE
     o_emul = (p_r @ v[0, 0]) / l
     bound = fp8.p_rounding_bound(q, k, v, causal, scale, o)[0, 0]
     assert (np.abs(o_emul - o[0, 0]) <= bound).all()
     assert np.abs(o_emul - o[0, 0]).max() > 1e-4            # the rounding is visible, so the check bites
+    # and the bound of a subset of rows is the same as the full one there
+    rows = np.array([[[0, 7, 150, 299]]])
+    sub = fp8.p_rounding_bound(q, k, v, causal, scale, o[:, :, rows[0, 0]], rows=rows)
+    assert np.allclose(sub[0, 0], bound[rows[0, 0]], rtol=1e-12, atol=0)
