@@ -114,3 +114,34 @@ def test_fp8_refuses_other_head_dims(fa):
     with pytest.raises(pkg.FAError):
         pkg.quantize_fp8(x, x, x)
     fa.check_device_status()
+
+
+@pytest.mark.parametrize("N,causal", [(1, True), (1, False), (64, True), (129, False)])
+def test_fp8_forward_degenerate_sizes(fa, N, causal):
+    """One query, one 64-row scale block, a ragged second key tile."""
+    t = inputs.make_inputs(1, 2, 1, N, 128, "bf16", seed=N + 5)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 128 ** -0.5)
+
+
+def test_fp8_forward_long_sequence_sampled_rows(fa):
+    """N = 65536 (512 key tiles per causal row at the end), 4 heads: the
+    eight-slot ring wraps over a hundred times; 64 seeded rows per head."""
+    B, H, N, d = 1, 4, 65536, 128
+    t = inputs.make_inputs(B, H, H, N, d, "bf16", seed=65536)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    deq = (ofp8.dequantize_rows(host[0], host[1]), ofp8.dequantize_rows(host[2], host[3]),
+           ofp8.dequantize_v_transposed(host[4], host[5], N))
+    rows = inputs.sample_rows(B, H, N, 64, seed=6)
+    ro, rl = oracle.forward_rows(*deq, True, d ** -0.5, rows)
+    bound = ofp8.p_rounding_bound(*deq, True, d ** -0.5, ro, rows=rows)
+    bi, hi = np.arange(B)[:, None, None], np.arange(H)[None, :, None]
+    err = np.abs(o[bi, hi, rows].float().cpu().numpy() - ro)
+    assert (err <= bound).all(), float((err - bound).max())
+    assert np.abs(lse[bi, hi, rows].cpu().numpy() - rl).max() <= configs.TOL_LSE_MAX

@@ -126,3 +126,19 @@ def test_wide_backward_and_block_mask_refused(fa):
         fa.fwd(q, q, q, causal=True, block_mask=torch.ones(1, 1, 2, 2, dtype=torch.bool, device=DEV))
     assert fa.bwd_workspace_bytes(1, 2, 2, 256, 256) == 0
     fa.check_device_status()
+
+
+def test_wide_fwd_long_sequence_sampled_rows(fa):
+    """d = 256, N = 32768, 4 heads, causal: 256 key tiles for the last rows,
+    the ring wraps about two hundred times and all four heads fit one head
+    group; 64 seeded rows per head against the oracle."""
+    B, H, N, d = 1, 4, 32768, 256
+    t = inputs.make_inputs(B, H, H, N, d, "bf16", seed=32768)
+    g = {n: x.to(DEV) for n, x in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=True)
+    fa.check_device_status()
+    rows = inputs.sample_rows(B, H, N, 64, seed=7)
+    f = {n: inputs.to_f64(x) for n, x in t.items()}
+    ro, rl = oracle.forward_rows(f["q"], f["k"], f["v"], True, d ** -0.5, rows)
+    bi, hi = np.arange(B)[:, None, None], np.arange(H)[None, :, None]
+    check_fwd(o[bi, hi, rows], lse[bi, hi, rows], ro, rl)
