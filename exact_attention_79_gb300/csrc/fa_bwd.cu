@@ -23,6 +23,8 @@
 //                        dQ_i = dS K               (TMEM -> shared -> TMA reduce-add into dQacc)
 //                      and finally dK *= scale; dK, dV stored once (deterministic).
 //  3. bwd_dq_kernel    dQ = scale * dQacc -> bf16.
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_kernels.h"
 
@@ -185,10 +187,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (key tile, batch * kv head); the key tiles with the most
-  // query tiles to visit (small index when causal) go first
-  const int jt = blockIdx.x / p.BHkv;
-  const int bhkv = blockIdx.x % p.BHkv;
+  // ---- work item: (key tile, batch * kv head). KV heads go in groups of
+  // p.head_group whose Q, dO and fp32 dQ accumulator fit in part of L2; in a
+  // group the key tiles with the most query tiles to visit (small index when
+  // causal) go first. `cta` is the item's logical index, key tile * BHkv +
+  // batch * Hkv + kv head (the block-sparse step lists are kept by it).
+  const int nkt = p.NKP / kBN;
+  const int grp = blockIdx.x / (nkt * p.head_group);
+  const int gsize = min(p.head_group, p.BHkv - grp * p.head_group);
+  const int local = blockIdx.x - grp * p.head_group * nkt;
+  const int jt = local / gsize;
+  const int bhkv = grp * p.head_group + local % gsize;
+  const int cta = jt * p.BHkv + bhkv;
   const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int nq = p.NQP / kBM;
@@ -199,8 +209,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int tiles_per_head = nq - it0;
   // block-sparse: only the (head, query tile) steps the mask lets see this key
   // tile, in the dense order, from the list bwd_blocklist_kernel compacted
-  const int nsteps = kSparse ? p.ws_count[blockIdx.x] : G * tiles_per_head;
-  const unsigned* const steps = kSparse ? p.ws_list + static_cast<size_t>(blockIdx.x) * G * nq : nullptr;
+  const int nsteps = kSparse ? p.ws_count[cta] : G * tiles_per_head;
+  const unsigned* const steps = kSparse ? p.ws_list + static_cast<size_t>(cta) * G * nq : nullptr;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -615,8 +625,13 @@ static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStrea
     configured = true;
   }
   const int grid = (p.NKP / kBN) * p.BHkv;
+  // KV heads per group: the group's Q and dO (bf16) and fp32 dQ accumulator,
+  // G query heads of N x d each, within 64 MB, half of L2
+  BwdParams q = p;
+  const long long per_kv_head = 8LL * (p.Hq / p.Hkv) * p.N * D;
+  q.head_group = static_cast<int>(std::max(1LL, std::min<long long>(p.BHkv, (64LL << 20) / per_kv_head)));
   bwd_dkdv_kernel<D, kSparse><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv,
-                                                                             m.dqacc, p);
+                                                                             m.dqacc, q);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,7 @@ struct BwdParams {
   int* ws_count;
   unsigned* ws_list;
   int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
+  int head_group;                  // dK/dV: KV heads scheduled together (set by launch_bwd_dkdv)
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;
