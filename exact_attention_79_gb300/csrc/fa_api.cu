@@ -372,7 +372,6 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // the two-pass kernels exist for 64 and 128 only
   fa::BwdParams p{};
   int num_sms = 0;
   fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, true);

@@ -646,8 +646,11 @@ static cudaError_t launch_det_d(const BwdMaps& m, const BwdParams& p, cudaStream
 }
 
 cudaError_t launch_bwd_deterministic(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_det_d<128>(m, p, stream);
-  if (d == 64) return launch_det_d<64>(m, p, stream);
+  // d < 128 runs in the kernel for the next size up: the tensor maps carry
+  // the true d, so the columns past it load as zeros (adding nothing to S,
+  // dP, dQ, dK or dV) and are skipped by the stores
+  if (d > 64 && d <= 128) return launch_det_d<128>(m, p, stream);
+  if (d >= 8 && d <= 64) return launch_det_d<64>(m, p, stream);
   return cudaErrorInvalidValue;
 }
 
