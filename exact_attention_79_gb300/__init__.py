@@ -45,6 +45,7 @@ SIGNATURES = {
     "fa_fp8_quantize_rows": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     "fa_fp8_quantize_v": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     "fa_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fwd_fp8_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_device_status": (_I, [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),
@@ -157,7 +158,7 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
 
 
 def quantize_fp8(q, k, v):
-    """Block-scaled e4m3 copies of bf16 q, k [B, H, N, d] and v (fa_fp8_quantize_rows,
+    """Block-scaled e4m3 copies of bf16 q [B, Hq, N, d], k and v [B, Hkv, Nk, d] (fa_fp8_quantize_rows,
     fa_fp8_quantize_v): returns (q8, q_scale, k8, k_scale, vt8, v_scale) with
     q8, k8 uint8 [B, H, N, d], scales fp32 [B, H, ceil(N/64)], vt8 uint8
     [B, Hkv, d, NP] (V transposed, NP = N rounded up to 128) and v_scale
@@ -168,21 +169,21 @@ def quantize_fp8(q, k, v):
         if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
             raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
     B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
-    nb, NP = int(lib.fa_fp8_row_scales(N)), int(lib.fa_fp8_vt_keys(N))
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    nb, nbk, NP = int(lib.fa_fp8_row_scales(N)), int(lib.fa_fp8_row_scales(Nk)), int(lib.fa_fp8_vt_keys(Nk))
     dev = q.device
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
     k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
     vt8 = torch.empty((B, Hkv, d, NP), dtype=torch.uint8, device=dev)
     qs = torch.empty((B, Hq, nb), dtype=torch.float32, device=dev)
-    ks = torch.empty((B, Hkv, nb), dtype=torch.float32, device=dev)
+    ks = torch.empty((B, Hkv, nbk), dtype=torch.float32, device=dev)
     vs = torch.empty((B, Hkv, d), dtype=torch.float32, device=dev)
     st = _stream(q)
     _check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(_ptr(q), _ptr(q8), _ptr(qs), B * Hq, N, d, st))
-    _check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(_ptr(k), _ptr(k8), _ptr(ks), B * Hkv, N, d, st))
-    _check("fa_fp8_quantize_v", lib.fa_fp8_quantize_v(_ptr(v), _ptr(vt8), _ptr(vs), B * Hkv, N, d, st))
+    _check("fa_fp8_quantize_rows", lib.fa_fp8_quantize_rows(_ptr(k), _ptr(k8), _ptr(ks), B * Hkv, Nk, d, st))
+    _check("fa_fp8_quantize_v", lib.fa_fp8_quantize_v(_ptr(v), _ptr(vt8), _ptr(vs), B * Hkv, Nk, d, st))
     return q8, qs, k8, ks, vt8, vs
 
 
@@ -200,6 +201,13 @@ def fwd_fp8(q8, q_scale, k8, k_scale, vt8, v_scale, causal=False, scale=None, ou
         scale = d ** -0.5
     o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    Nk = k8.shape[2]
+    if Nk != N:
+        # queries are the last N of Nk positions (fa_fwd_fp8_kv)
+        _check("fa_fwd_fp8_kv", lib.fa_fwd_fp8_kv(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(vt8),
+                                                  _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq, Hkv, N, Nk, d,
+                                                  int(bool(causal)), float(scale), _stream(q8)))
+        return o, lse
     _check("fa_fwd_fp8", lib.fa_fwd_fp8(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(vt8), _ptr(v_scale),
                                         _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                                         _stream(q8)))

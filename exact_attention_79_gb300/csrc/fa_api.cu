@@ -439,29 +439,34 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
              ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
-                     const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
-                     float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                         const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int Nk, int d,
+                         int causal, float scale, void* stream) {
   const void* ptrs[] = {q, q_scale, k, k_scale, vt, v_scale, o, lse};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
+  if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
   if (d != 128) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = device_state(&status);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mvt, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-  const int NP = (N + 127) / 128 * 128;
-  if (!make_map(&mq, q, 1, d, N, BHq) || !make_map(&mk, k, 1, d, N, BHkv) ||
+  const int NP = (Nk + 127) / 128 * 128;
+  if (!make_map(&mq, q, 1, d, N, BHq) || !make_map(&mk, k, 1, d, Nk, BHkv) ||
       !make_map(&mvt, vt, 1, NP, d, BHkv) || !make_map(&mo, o, 2, d, N, BHq))
     return FA_ERR_CUDA;
   fa::FwdParams p{};
   p.lse = lse;
   p.status = status;
   p.N = N;
-  p.Nk = N;
+  p.Nk = Nk;
+  p.causal_off = Nk - N;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.BH = static_cast<int>(BHq);
@@ -473,6 +478,21 @@ fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const f
   p.v_scale = v_scale;
   return fa::launch_fwd_fp8(mq, mk, mvt, mo, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                                    : FA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                     const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                     float scale, void* stream) {
+  return fwd_fp8_common(q, q_scale, k, k_scale, vt, v_scale, o, lse, B, Hq, Hkv, N, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_fp8_kv(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                        const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        int causal, float scale, void* stream) {
+  return fwd_fp8_common(q, q_scale, k, k_scale, vt, v_scale, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
 }
 
 fa_status fa_device_status(void* stream) {

@@ -208,9 +208,15 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int nq = (p.N + kBM - 1) / kBM;
-  const int nk = nq;
+  const int nk = (p.Nk + kBN - 1) / kBN;
   const int qt[2] = {2 * pair, 2 * pair + 1};
-  auto reach = [&](int t) { return p.causal ? min(nk, t + 1) : nk; };
+  // key tiles a query tile reaches: causal (bottom-right: key <= row + Nk - N),
+  // up to the one holding key (last row + Nk - N), none if that is negative
+  auto reach = [&](int t) {
+    if (!p.causal) return nk;
+    const int last = t * kBM + kBM - 1 + p.causal_off;
+    return last < 0 ? 0 : min(nk, last / kBN + 1);
+  };
   const bool has_tile[2] = {true, qt[1] < nq};
   const int nkv[2] = {reach(qt[0]), has_tile[1] ? reach(qt[1]) : 0};
   const int nmax = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
@@ -366,7 +372,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int q_row = qt[g] * kBM + row;
     const int nqb = (p.N + kRowBlock - 1) / kRowBlock;
     const float sq = p.q_scale[static_cast<size_t>(bh) * nqb + min(q_row / kRowBlock, nqb - 1)];
-    const float* ksc = p.k_scale + static_cast<size_t>(bh_kv) * nqb;
+    const int nkb = (p.Nk + kRowBlock - 1) / kRowBlock;
+    const float* ksc = p.k_scale + static_cast<size_t>(bh_kv) * nkb;
     const float csq = p.scale_log2 * sq;
     float m = -INFINITY;                           // running max (up to 2^4 stale), log2 units
     float l = 0.f;                                 // running sum of 2^4 P
@@ -392,15 +399,15 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
       const int kv0 = j * kBN;
       int lim = kBN;
-      if (p.causal) lim = min(lim, q_row - kv0 + 1);
-      if (kv0 + kBN > p.N) lim = min(lim, p.N - kv0);
+      if (p.causal) lim = min(lim, q_row + p.causal_off - kv0 + 1);
+      if (kv0 + kBN > p.Nk) lim = min(lim, p.Nk - kv0);
       if (lim < kBN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
       // per-half multipliers: scale * log2(e) * sq * sk (key blocks of 64)
-      const float c0 = csq * ksc[min(2 * j, nqb - 1)];
-      const float c1 = csq * ksc[min(2 * j + 1, nqb - 1)];
+      const float c0 = csq * ksc[min(2 * j, nkb - 1)];
+      const float c1 = csq * ksc[min(2 * j + 1, nkb - 1)];
       float mk[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {

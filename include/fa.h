@@ -157,6 +157,17 @@ fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const f
                      const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
                      float scale, void* stream);
 
+/* fa_fwd_fp8 with keys of another length than the queries, as fa_fwd_kv:
+ * q codes [B, Hq, Nq, d] and q_scale [B, Hq, ceil(Nq/64)]; k codes
+ * [B, Hkv, Nk, d], k_scale [B, Hkv, ceil(Nk/64)], vt codes [B, Hkv, d, NPk]
+ * (NPk = fa_fp8_vt_keys(Nk)) and v_scale [B, Hkv, d] (quantised with N = Nk);
+ * o [B, Hq, Nq, d], lse [B, Hq, Nq]. The queries are the last Nq of Nk
+ * positions: when causal, key j is visible to query i iff j <= i + (Nk - Nq);
+ * rows that see no key get O = 0, lse = -inf. Same bound as fa_fwd_fp8. */
+fa_status fa_fwd_fp8_kv(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
+                        const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        int causal, float scale, void* stream);
+
 /* Bytes of device workspace fa_bwd needs: fp32 LSE * log2(e) and fp32
  * D = rowsum(dO * O), each [B, Hq, ceil(N/128)*128], and the fp32 dQ
  * accumulator [B, Hq, N, d], each part 256-byte aligned. Returns 0 for invalid

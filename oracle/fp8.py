@@ -176,10 +176,13 @@ def p_rounding_bound(q, k, v, causal, scale, o_ref, rows=None):
             r = np.arange(N) if rows is None else np.asarray(rows[b, h])
             kh, vh = k[b, h // G], v[b, h // G]
             s = (q[b, h, r] @ kh.T) * scale
-            visible = np.ones(s.shape, bool) if not causal else (np.arange(kh.shape[0])[None, :] <= r[:, None])
+            off = kh.shape[0] - N                      # keys Nk vs queries N: bottom-right causal
+            visible = np.ones(s.shape, bool) if not causal else (np.arange(kh.shape[0])[None, :] <= r[:, None] + off)
             s = np.where(visible, s, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            l = p.sum(axis=1, keepdims=True)
+            mx = s.max(axis=1, keepdims=True)
+            seen = np.isfinite(mx)                     # rows that see no key: O = 0 exactly, bound 1e-6
+            p = np.where(seen, np.exp(s - np.where(seen, mx, 0.0)), 0.0)
+            l = np.where(seen, p.sum(axis=1, keepdims=True), 1.0)
             av = np.abs(vh)
             out[b, h] = (2.0 ** -4 * ((p / l) @ av) + sub * ((visible @ av) / l)
                          + 2.0 ** -8 * np.abs(o_ref[b, h]) + 1e-6)

@@ -145,3 +145,30 @@ def test_fp8_forward_long_sequence_sampled_rows(fa):
     err = np.abs(o[bi, hi, rows].float().cpu().numpy() - ro)
     assert (err <= bound).all(), float((err - bound).max())
     assert np.abs(lse[bi, hi, rows].cpu().numpy() - rl).max() <= configs.TOL_LSE_MAX
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(200, 700, True), (500, 130, True), (1, 777, True), (300, 1000, False),
+                                          (1000, 1000, True)])
+def test_fp8_forward_kv_lengths(fa, Nq, Nk, causal):
+    """Queries are the last Nq of Nk positions (fa_fwd_fp8_kv, bottom-right
+    causal); with Nq > Nk the first rows see nothing: O = 0, LSE = -inf.
+    Equal lengths through the same path agree bit for bit with fa_fwd_fp8."""
+    B, Hq, Hkv, d = 1, 4, 2, 128
+    t = inputs.make_inputs(B, Hq, Hkv, Nq, d, "bf16", seed=Nq + 3 * Nk, Nk=Nk)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    ref = oracle_quant(t)
+    assert all(np.array_equal(a, r) for a, r in zip(host, ref))
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    o_np, lse_np = o.float().cpu().numpy(), lse.cpu().numpy()
+    check_against_bound(o_np, lse_np, *host, causal, d ** -0.5)
+    if Nq == Nk:
+        lib = pkg.load()
+        o2 = torch.empty_like(o)
+        l2 = torch.empty_like(lse)
+        P = pkg._ptr
+        assert lib.fa_fwd_fp8_kv(P(q8), P(qs), P(k8), P(ks), P(vt8), P(vs), P(o2), P(l2), B, Hq, Hkv, Nq, Nk, d,
+                                 int(causal), d ** -0.5, pkg._stream(q8)) == 0
+        fa.check_device_status()
+        assert torch.equal(o, o2) and torch.equal(lse, l2)
