@@ -473,6 +473,7 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_limit_ns();
+  p.test_stall = test_stall();
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;

@@ -197,6 +197,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   uint8_t* const gbars = gbase + (bars - base);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 112 + 16 * kSt);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 116 + 16 * kSt);
+  const uint32_t bar_stall = bars + 120u + 16u * kSt;                     // nothing arrives (timeout test)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -236,6 +237,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
+    mbar_init(bar_stall, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -280,6 +282,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc = make_idesc(0, 128, 128, 0, 0);   // e4m3 x e4m3 -> f32, both K-major
       bool ok = true;
+      if (p.test_stall) ok = mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       for (int i = 0; i < 2 && ok; ++i)
         if (nkv[i] > 0) ok = mbar_wait(bar_q_full(i), 0, abort_flag, deadline);
       auto issue_qk = [&](int i, uint32_t sk) {

@@ -46,8 +46,9 @@
  *     block unwind, store nothing and set the device status word, which
  *     fa_device_status reports as FA_ERR_TIMEOUT; the context stays usable.
  *     FA_TEST_STALL=1 in the environment (read at every call) makes the
- *     tensor-core issuer of fa_fwd* and of fa_bwd's dK/dV pass wait on a
- *     barrier nothing arrives on, to exercise that path; unset in normal use.
+ *     tensor-core issuer of every fa_fwd* call (fa_fwd_fp8* included) and of
+ *     fa_bwd's dK/dV pass wait on a barrier nothing arrives on, to exercise
+ *     that path; unset in normal use.
  *   Threads: calls may come from several host threads; each call is
  *     independent.
  */
