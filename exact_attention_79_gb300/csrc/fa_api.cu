@@ -526,6 +526,6 @@ const char* fa_status_string(fa_status s) {
   return "unknown status";
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 }  // extern "C"
