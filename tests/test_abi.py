@@ -61,3 +61,29 @@ def test_invalid_arguments_rejected_without_device(lib):
     args = [fake] * 9
     assert lib.fa_bwd(*args, null, 1 << 30, 1, 1, 1, 128, 128, 1, 0.1, null) == 6
     assert lib.fa_bwd(*([null] + [fake] * 8), fake, 1 << 30, 1, 1, 1, 128, 128, 1, 0.1, null) == 1
+
+
+def test_head_dim_and_fp8_rules_without_device(lib):
+    """Head dims 8..256 for the forward, 8..128 for every backward, 128 for
+    FP8: the host checks answer before any device work."""
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 264, 0, 0.125, null) == 1    # past 256
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 252, 0, 0.125, null) == 1    # not a multiple of 8
+    args = [fake] * 9
+    # backward above 128: unsupported, before the workspace is looked at
+    assert lib.fa_bwd(*args, null, 0, 1, 1, 1, 128, 256, 1, 0.1, null) == 2
+    assert lib.fa_bwd_deterministic(*args, null, 0, 1, 1, 1, 128, 192, 1, 0.1, null) == 2
+    assert lib.fa_bwd_noalloc(*args, 1, 1, 1, 128, 136, 1, 0.1, null) == 2
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 256) == 0
+    assert lib.fa_bwd_blocksparse_workspace_bytes(1, 2, 2, 128, 192) == 0
+    # FP8: d = 128 only; other sizes are valid arguments but not built
+    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 64, 0, 0.1, null) == 2
+    assert lib.fa_fwd_fp8_kv(*([fake] * 8), 1, 1, 1, 128, 300, 256, 0, 0.1, null) == 2
+    assert lib.fa_fwd_fp8(*([fake] * 7 + [null]), 1, 1, 1, 128, 128, 0, 0.1, null) == 1
+    assert lib.fa_fp8_quantize_rows(fake, fake, fake, 4, 100, 64, null) == 2
+    assert lib.fa_fp8_quantize_v(fake, fake, fake, 0, 100, 128, null) == 1
+    # scale-array and padded-key helpers
+    assert lib.fa_fp8_row_scales(1) == 1 and lib.fa_fp8_row_scales(64) == 1 and lib.fa_fp8_row_scales(65) == 2
+    assert lib.fa_fp8_vt_keys(1) == 128 and lib.fa_fp8_vt_keys(128) == 128 and lib.fa_fp8_vt_keys(129) == 256
+    assert lib.fa_fp8_row_scales(0) == 0 and lib.fa_fp8_vt_keys(0) == 0
