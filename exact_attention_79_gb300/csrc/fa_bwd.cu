@@ -677,13 +677,19 @@ cudaError_t launch_bwd_blocklist(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The two streaming kernels (grid-stride loops, 256 threads per CTA): eight
+// CTAs per SM fill its 2048 thread slots, which keeps enough 16-byte loads in
+// flight to cover the memory latency (four per SM left them latency-bound).
+constexpr int kStreamCtasPerSm = 8;
+
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* lse, const BwdParams& p, int num_sms,
                            cudaStream_t stream) {
   const auto* o16 = static_cast<const __nv_bfloat16*>(o);
   const auto* do16 = static_cast<const __nv_bfloat16*>(dO);
-  if (d == 128) bwd_pre_kernel<128><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
-  else if (d == 64) bwd_pre_kernel<64><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
-  else if (d >= 8 && d <= 128 && d % 8 == 0) bwd_pre_kernel<0><<<num_sms * 4, 256, 0, stream>>>(o16, do16, lse, p, d);
+  const int grid = num_sms * kStreamCtasPerSm;
+  if (d == 128) bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
+  else if (d == 64) bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
+  else if (d >= 8 && d <= 128 && d % 8 == 0) bwd_pre_kernel<0><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
@@ -698,7 +704,7 @@ cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStr
 
 cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream) {
   auto* dq16 = static_cast<__nv_bfloat16*>(dq);
-  if (d >= 8 && d <= 128 && d % 8 == 0) bwd_dq_kernel<<<num_sms * 4, 256, 0, stream>>>(dq16, p, d);
+  if (d >= 8 && d <= 128 && d % 8 == 0) bwd_dq_kernel<<<num_sms * kStreamCtasPerSm, 256, 0, stream>>>(dq16, p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
