@@ -420,7 +420,7 @@ size_t fa_fp8_vt_keys(int N) { return N >= 1 ? static_cast<size_t>((N + 127) / 1
 fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, int N, int d, void* stream) {
   if (!x || !out || !scales || !aligned16(x) || !aligned16(out) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
   unsigned* status = nullptr;
   const fa_status st = device_state(&status);
   if (st != FA_OK) return st;
@@ -431,7 +431,7 @@ fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, 
 fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int N, int d, void* stream) {
   if (!v || !vt || !scales || !aligned16(v) || !aligned16(vt) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
   unsigned* status = nullptr;
   const fa_status st = device_state(&status);
   if (st != FA_OK) return st;
@@ -451,7 +451,7 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
   if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
   unsigned* status = nullptr;
   st = device_state(&status);
   if (st != FA_OK) return st;
@@ -474,6 +474,7 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_limit_ns();
   p.test_stall = test_stall();
+  p.head_dim = d;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;

@@ -40,7 +40,7 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;                  // head dimension of this path
+constexpr int kD = 128;                  // head dimension of the kernel (d = 64 runs in it, zero-filled)
 constexpr int kTile = 128 * 128;         // 128 rows x 128 e4m3 codes: one TMA box
 constexpr int kQRegion = 2 * kTile;      // a query tile's region: its codes and P buffer 0, later its bf16 O
 constexpr int kStages = 8;               // K / V^T ring slots
@@ -485,7 +485,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (ok || empty) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      const float* vsc = p.v_scale + static_cast<size_t>(bh_kv) * kD;
+      // V's scales: one per column of the head's d (columns past d hold zeros)
+      const float* vsc = p.v_scale + static_cast<size_t>(bh_kv) * p.head_dim;
+      auto vscale = [&](int c) { return c < p.head_dim ? __ldg(vsc + c) : 0.f; };
       // bf16 O staged over this tile's region (its Q codes and P buffer 0 are
       // no longer read: every MMA of this tile has completed)
       const uint32_t stage = s_q[g];
@@ -508,8 +510,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 8 * u + 2 * e;
-            w[e] = pack_bf16x2(__uint_as_float(o[c]) * (__ldg(vsc + c0 + c) * inv_l),
-                               __uint_as_float(o[c + 1]) * (__ldg(vsc + c0 + c + 1) * inv_l));
+            w[e] = pack_bf16x2(__uint_as_float(o[c]) * (vscale(c0 + c) * inv_l),
+                               __uint_as_float(o[c + 1]) * (vscale(c0 + c + 1) * inv_l));
           }
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, row, u0 + u)),
                        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
@@ -522,7 +524,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     named_bar_sync(1 + g, 128);
     if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {
-      for (int bx = 0; bx < 2; ++bx) tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * 64, qt[g] * kBM, bh);
+      // 64-column boxes; one that would start at or past d (d = 64) is skipped
+      for (int bx = 0; bx < 2; ++bx)
+        if (bx * 64 < p.head_dim) tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * 64, qt[g] * kBM, bh);
       tma_store_commit();
       tma_store_wait_all0();
     }

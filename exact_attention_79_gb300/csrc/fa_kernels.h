@@ -28,6 +28,7 @@ struct FwdParams {
   const float* q_scale;
   const float* k_scale;
   const float* v_scale;
+  int head_dim;                    // FP8 forward: d (64 runs in the d = 128 kernel, columns past d zero)
 };
 constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 

@@ -77,11 +77,11 @@ def test_head_dim_and_fp8_rules_without_device(lib):
     assert lib.fa_bwd_noalloc(*args, 1, 1, 1, 128, 136, 1, 0.1, null) == 2
     assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 256) == 0
     assert lib.fa_bwd_blocksparse_workspace_bytes(1, 2, 2, 128, 192) == 0
-    # FP8: d = 128 only; other sizes are valid arguments but not built
-    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 64, 0, 0.1, null) == 2
+    # FP8: d = 64 or 128; other sizes are valid arguments but not built
+    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 96, 0, 0.1, null) == 2
     assert lib.fa_fwd_fp8_kv(*([fake] * 8), 1, 1, 1, 128, 300, 256, 0, 0.1, null) == 2
     assert lib.fa_fwd_fp8(*([fake] * 7 + [null]), 1, 1, 1, 128, 128, 0, 0.1, null) == 1
-    assert lib.fa_fp8_quantize_rows(fake, fake, fake, 4, 100, 64, null) == 2
+    assert lib.fa_fp8_quantize_rows(fake, fake, fake, 4, 100, 32, null) == 2
     assert lib.fa_fp8_quantize_v(fake, fake, fake, 0, 100, 128, null) == 1
     # scale-array and padded-key helpers
     assert lib.fa_fp8_row_scales(1) == 1 and lib.fa_fp8_row_scales(64) == 1 and lib.fa_fp8_row_scales(65) == 2

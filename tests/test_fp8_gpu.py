@@ -109,8 +109,21 @@ def test_fp8_forward_full_size_sampled_rows(fa):
     assert np.abs(lse[bi, hi, rows] - rl).max() <= configs.TOL_LSE_MAX
 
 
+@pytest.mark.parametrize("N,causal", [(333, True), (1000, False)])
+def test_fp8_head_dim_64(fa, N, causal):
+    """d = 64 runs in the d = 128 kernel: Q, K and V^T read zeros past d,
+    V's scales exist only for the 64 columns and the store clips."""
+    t = inputs.make_inputs(2, 4, 2, N, 64, "bf16", seed=N + 64)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    assert all(np.array_equal(a, r) for a, r in zip(host, oracle_quant(t)))
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 64 ** -0.5)
+
+
 def test_fp8_refuses_other_head_dims(fa):
-    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros(1, 1, 128, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(pkg.FAError):
         pkg.quantize_fp8(x, x, x)
     fa.check_device_status()
