@@ -617,13 +617,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 template <int D, bool kSparse>
 static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([] {
+    return cudaFuncSetAttribute(bwd_dkdv_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemAlloc);
+  });
+  if (e != cudaSuccess) return e;
   const int grid = (p.NKP / kBN) * p.BHkv;
   // KV heads per group: the group's Q and dO (bf16) and fp32 dQ accumulator,
   // G query heads of N x d each, within 64 MB, half of L2

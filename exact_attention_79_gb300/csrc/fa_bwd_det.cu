@@ -621,20 +621,17 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ launch
-template <typename Kern>
-static cudaError_t set_smem(Kern k, int bytes, bool& done) {
-  if (done) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done = true;
-  return e;
-}
-
 template <int D>
 static cudaError_t launch_det_d(const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-  static bool cfg_a = false, cfg_b = false;
-  cudaError_t e = set_smem(det_dkdv_kernel<D>, DetDkdvCfg<D>::kSmemBytes, cfg_a);
+  static PerDeviceOnce attr_a, attr_b;
+  cudaError_t e = attr_a.run([] {
+    return cudaFuncSetAttribute(det_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                DetDkdvCfg<D>::kSmemBytes);
+  });
   if (e != cudaSuccess) return e;
-  e = set_smem(det_dq_kernel<D>, DetDqCfg<D>::kSmemBytes, cfg_b);
+  e = attr_b.run([] {
+    return cudaFuncSetAttribute(det_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DetDqCfg<D>::kSmemBytes);
+  });
   if (e != cudaSuccess) return e;
   det_dkdv_kernel<D><<<(p.NQP / kBN) * p.BHkv, DetDkdvCfg<D>::kThreads, DetDkdvCfg<D>::kSmemBytes, stream>>>(
       m.q, m.k, m.v, m.dO, m.dk, m.dv, p);

@@ -1,6 +1,7 @@
 // Shared definitions for the attention kernels (device side).
 #pragma once
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -37,5 +38,22 @@ __device__ __forceinline__ void abort_grace_period() {
 __device__ __forceinline__ uint32_t swz128(uint32_t box_base, int r, int u) {
   return box_base + r * 128 + ((u ^ (r & 7)) << 4);
 }
+
+// Host side: a kernel's dynamic shared-memory limit is an attribute of each
+// device's copy of the kernel, so it is set once per device (and per launcher,
+// each holding its own PerDeviceOnce), safely from several host threads.
+struct PerDeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::once_flag flag[kMaxDevices];
+  cudaError_t result[kMaxDevices] = {};
+  template <typename Fn>
+  cudaError_t run(Fn fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { result[dev] = fn(); });
+    return result[dev];
+  }
+};
 
 }  // namespace fa

@@ -622,12 +622,11 @@ static cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   // the block-sparse variant: one ring slot fewer, the tile list after the barriers
   constexpr int kSmem = kSparse ? C::kSmemBytes - C::kTileBytes + 2 * kMaskMaxTiles : C::kSmemBytes;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([] {
+    return cudaFuncSetAttribute(fwd_kernel<T, D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e != cudaSuccess) return e;
   fwd_kernel<T, D, kSparse><<<grid, C::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }

@@ -567,12 +567,11 @@ cudaError_t launch_fp8_quant_v(const void* v, void* vt, float* scales, int BH, i
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mvt,
                            const CUtensorMap& mo, FwdParams p, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([] {
+    return cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e != cudaSuccess) return e;
   const int nq = (p.N + kBM - 1) / kBM;
   p.num_pairs = (nq + 1) / 2;
   fwd_fp8_kernel<<<p.num_pairs * p.BH, kThreads, kSmem, stream>>>(mq, mk, mvt, mo, p);

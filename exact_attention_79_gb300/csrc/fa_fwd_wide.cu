@@ -462,13 +462,11 @@ template <int D>
 static cudaError_t launch_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mo, const FwdParams& p, cudaStream_t stream) {
   using C = WideCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([] {
+    return cudaFuncSetAttribute(fwd_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((p.N + kBM - 1) / kBM) * p.BH;
   // heads per group: their K and V (2 Nk D bf16 each, counted per query head)
   // within 64 MB, half of L2
