@@ -419,8 +419,12 @@ def native_arm(args, w):
     flops_step = w.flops_fwd + (0.0 if fwd_only else w.flops_bwd)
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     mean = [sum(s[j] for s in seg) / args.steps for j in range(4)]
-    fwd_kernel = "fwd_fp8_kernel" if fp8 else "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
-    fwd_src = "fa_fwd_fp8.cu" if fp8 else "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
+    if fp8:
+        fwd_kernel = "fwd_fp8_wide_kernel" if w.d > 128 else "fwd_fp8_kernel"
+        fwd_src = "fa_fwd_fp8_wide.cu" if w.d > 128 else "fa_fwd_fp8.cu"
+    else:
+        fwd_kernel = "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
+        fwd_src = "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
     names = [fwd_kernel, "bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
     if fwd_only:
         names = [fwd_kernel, "-", "-", "-"]

@@ -86,6 +86,10 @@ int test_stall() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// FP8 head dimensions: the quantisers move V in 64-column passes, and the
+// attention kernels are built for 128 (64 runs in it) and 256 (192 runs in it)
+bool fp8_dim(int d) { return d == 64 || d == 128 || d == 192 || d == 256; }
+
 // 3-D map over a dense [BH, N, d] tensor: dims (d, N, BH), one box = 128 rows
 // by 128 bytes with 128-byte swizzle. Rows past N read as zero and are not
 // written by stores.
@@ -420,7 +424,7 @@ size_t fa_fp8_vt_keys(int N) { return N >= 1 ? static_cast<size_t>((N + 127) / 1
 fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, int N, int d, void* stream) {
   if (!x || !out || !scales || !aligned16(x) || !aligned16(out) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
+  if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   const fa_status st = device_state(&status);
   if (st != FA_OK) return st;
@@ -431,7 +435,7 @@ fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, 
 fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int N, int d, void* stream) {
   if (!v || !vt || !scales || !aligned16(v) || !aligned16(vt) || !aligned16(scales)) return FA_ERR_INVALID_ARG;
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
+  if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   const fa_status st = device_state(&status);
   if (st != FA_OK) return st;
@@ -451,7 +455,7 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
   if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;      // d = 64 runs in the d = 128 kernel
+  if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = device_state(&status);
   if (st != FA_OK) return st;
@@ -478,8 +482,9 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  return fa::launch_fwd_fp8(mq, mk, mvt, mo, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
-                                                                                                   : FA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d <= 128 ? fa::launch_fwd_fp8(mq, mk, mvt, mo, p, s) : fa::launch_fwd_fp8_wide(mq, mk, mvt, mo, p, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 }  // namespace
 

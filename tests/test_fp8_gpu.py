@@ -122,8 +122,9 @@ def test_fp8_head_dim_64(fa, N, causal):
     check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 64 ** -0.5)
 
 
-def test_fp8_refuses_other_head_dims(fa):
-    x = torch.zeros(1, 1, 128, 96, dtype=torch.bfloat16, device=DEV)
+@pytest.mark.parametrize("d", [96, 160])
+def test_fp8_refuses_other_head_dims(fa, d):
+    x = torch.zeros(1, 1, 128, d, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(pkg.FAError):
         pkg.quantize_fp8(x, x, x)
     fa.check_device_status()
@@ -185,3 +186,73 @@ def test_fp8_forward_kv_lengths(fa, Nq, Nk, causal):
                                  int(causal), d ** -0.5, pkg._stream(q8)) == 0
         fa.check_device_status()
         assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+# ---- d = 192 and 256: the one-tile-per-CTA kernel (csrc/fa_fwd_fp8_wide.cu)
+
+@pytest.mark.parametrize("d,B,Hq,Hkv,N", [(256, 1, 2, 2, 128), (192, 2, 3, 1, 333), (256, 1, 2, 1, 1000)])
+def test_fp8_wide_quantisers_bit_exact(fa, d, B, Hq, Hkv, N):
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=N + d)
+    got = [x.cpu().numpy() for x in quantized(t)]
+    fa.check_device_status()
+    for name, a, r in zip(("q8", "q_scale", "k8", "k_scale", "vt8", "v_scale"), got, oracle_quant(t)):
+        assert a.shape == r.shape, name
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              r.view(np.uint32) if r.dtype == np.float32 else r), name
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 2, 2, 128), (2, 4, 2, 333), (1, 2, 1, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_wide_forward_within_rounding_bound(fa, d, B, Hq, Hkv, N, causal):
+    """Six-slot ring (wraps after three key tiles at N = 333 and 1000), the
+    last 64-column box of d = 192 past d, ragged key and query tails."""
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=11 * N + d + causal)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    print(check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, d ** -0.5))
+
+
+def test_fp8_wide_forward_rescales_and_sharp_logits(fa):
+    N, d = 1300, 256
+    t = inputs.make_inputs(1, 2, 2, N, d, "bf16", seed=78, q_mult=4.0)
+    t["k"] = (t["k"].float() * torch.linspace(0.3, 3.0, N).view(1, 1, N, 1)).to(torch.bfloat16)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    for causal in (True, False):
+        o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+        fa.check_device_status()
+        check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, d ** -0.5)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal,d", [(200, 700, True, 256), (500, 130, True, 192), (1, 777, True, 256),
+                                            (1, 1, False, 192), (300, 1000, False, 256)])
+def test_fp8_wide_forward_kv_lengths_and_degenerate(fa, Nq, Nk, causal, d):
+    t = inputs.make_inputs(1, 4, 2, Nq, d, "bf16", seed=Nq + 5 * Nk + d, Nk=Nk)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, d ** -0.5)
+
+
+def test_fp8_wide_forward_full_size_sampled_rows(fa):
+    """16 heads, N = 8192, d = 256, causal (the size the benchmark times at
+    d = 128): 64 seeded rows per head against the oracle and the bound."""
+    B, H, N, d = 1, 16, 8192, 256
+    t = inputs.make_inputs(B, H, H, N, d, "bf16", seed=8256)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    deq = (ofp8.dequantize_rows(host[0], host[1]), ofp8.dequantize_rows(host[2], host[3]),
+           ofp8.dequantize_v_transposed(host[4], host[5], N))
+    rows = inputs.sample_rows(B, H, N, 64, seed=9)
+    ro, rl = oracle.forward_rows(*deq, True, d ** -0.5, rows)
+    bound = ofp8.p_rounding_bound(*deq, True, d ** -0.5, ro, rows=rows)
+    bi, hi = np.arange(B)[:, None, None], np.arange(H)[None, :, None]
+    err = np.abs(o[bi, hi, rows].float().cpu().numpy() - ro)
+    assert (err <= bound).all(), float((err - bound).max())
+    assert np.abs(lse[bi, hi, rows].cpu().numpy() - rl).max() <= configs.TOL_LSE_MAX

@@ -1,5 +1,6 @@
 """Failure detection on the GPU without any fault: with FA_TEST_STALL=1 the
-tensor-core issuer (of the forward kernels: d <= 128, wide-head, FP8; and of
+tensor-core issuer (of the forward kernels: d <= 128, wide-head, FP8 at d = 128
+and 256; and of
 the backward's dK/dV pass) first waits on a barrier nothing arrives on, so its
 bounded wait (FA_WAIT_LIMIT_MS, here 300 ms) runs out; every other role of
 the block sees the abort flag and unwinds, the block stores nothing and the
@@ -54,16 +55,19 @@ for a, r in zip((dq, dk, dv), (rdq, rdk, rdv)):
     a = a.float().cpu().numpy()
     assert np.linalg.norm(a - r) / np.linalg.norm(r) <= configs.TOL_GRAD_REL_FRO
 
-# the wide-head forward (d = 256) and the FP8 forward take the same path
+# the wide-head forward (d = 256) and the FP8 forwards (d = 128, 256) take the same path
 tw = inputs.make_inputs(1, 2, 2, 300, 256, "bf16", seed=2)
 gw = {n: x.to(dev) for n, x in tw.items()}
 q8, qs, k8, ks, vt8, vs = fa.quantize_fp8(g["q"], g["k"], g["v"])
+w8 = fa.quantize_fp8(gw["q"], gw["k"], gw["v"])
 os.environ["FA_TEST_STALL"] = "0"
-ref_w = fa.fwd(gw["q"], gw["k"], gw["v"], causal=True)
-ref_8 = fa.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True)
+refs = {"wide": fa.fwd(gw["q"], gw["k"], gw["v"], causal=True),
+        "fp8": fa.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True),
+        "fp8_wide": fa.fwd_fp8(*w8, causal=True)}
 assert lib.fa_device_status(stream) == 0
 for name, call in (("wide", lambda: fa.fwd(gw["q"], gw["k"], gw["v"], causal=True)),
-                   ("fp8", lambda: fa.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True))):
+                   ("fp8", lambda: fa.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=True)),
+                   ("fp8_wide", lambda: fa.fwd_fp8(*w8, causal=True))):
     os.environ["FA_TEST_STALL"] = "1"
     t0 = time.time()
     call()
@@ -72,7 +76,7 @@ for name, call in (("wide", lambda: fa.fwd(gw["q"], gw["k"], gw["v"], causal=Tru
     os.environ["FA_TEST_STALL"] = "0"
     again = call()
     assert lib.fa_device_status(stream) == 0, name
-    ref = ref_w if name == "wide" else ref_8
+    ref = refs[name]
     assert torch.equal(again[0], ref[0]) and torch.equal(again[1], ref[1]), name
 print("timeout-path-ok")
 '''

@@ -68,9 +68,12 @@ def item_v(j, n):
 
 
 def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watcher_gate=True,
-             issuer_waits_k=True):
-    """Errors seen in one run of n key tiles. The keyword switches take
-    pieces of the protocol out, to show what each one guards against."""
+             issuer_waits_k=True, pieces=2):
+    """Errors seen in one run of n key tiles. `pieces` is the number of slot
+    loads per K or V tile: two in the bf16 kernel, one in the FP8 kernel
+    (csrc/fa_fwd_fp8_wide.cu, six slots of 32 KB, whose protocol is
+    otherwise the same). The other keyword switches take parts of the
+    protocol out, to show what each one guards against."""
     rng = random.Random(seed)
     SLOTS = slots  # noqa: N806
     errors = []
@@ -121,8 +124,8 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
 
     def producer():
         for it in range(2 * n):
-            for pc in range(2):
-                load = 2 * it + pc
+            for pc in range(pieces):
+                load = pieces * it + pc
                 slot = load % SLOTS
                 yield ("wait", lambda s=slot, p=((load // SLOTS) & 1) ^ 1: empty[s].passes(p))
                 if in_flight[slot] is not None:
@@ -139,15 +142,15 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
     def issuer():
         def issue_s(j):
             it = item_k(j)
-            for pc in range(2):
-                load = 2 * it + pc
+            for pc in range(pieces):
+                load = pieces * it + pc
                 if issuer_waits_k:
                     yield from wait_full(load % SLOTS, load, "issuer")
                 pipe.append(("S", j, load % SLOTS, load))
-                if pc == 0:
+                if pc < pieces - 1:
                     pipe.append(("commit", empty[load % SLOTS]))
             pipe.append(("commit", s_full[j & 1]))
-            pipe.append(("commit", empty[(2 * it + 1) % SLOTS]))
+            pipe.append(("commit", empty[(pieces * it + pieces - 1) % SLOTS]))
 
         yield from issue_s(0)
         if n > 1:
@@ -155,8 +158,8 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
         for j in range(n):
             yield ("wait", lambda j=j: pr(j).passes(pr_parity(j)))
             it = item_v(j, n)
-            for pc in range(2):
-                load = 2 * it + pc
+            for pc in range(pieces):
+                load = pieces * it + pc
                 pipe.append(("PV", j, load % SLOTS, load))
                 pipe.append(("commit", empty[load % SLOTS]))
             pipe.append(("commit", pv_done))
@@ -166,8 +169,8 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
 
     def watcher():
         def item(it):
-            for pc in range(2):
-                load = 2 * it + pc
+            for pc in range(pieces):
+                load = pieces * it + pc
                 yield from wait_full(load % SLOTS, load, "watcher")
 
         yield from item(item_k(0))
@@ -234,10 +237,10 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 12])
 @pytest.mark.parametrize("softmax_cycles", [(300, 1500), (100, 5000)])
-@pytest.mark.parametrize("slots", [SLOTS, 12])
-def test_wide_forward_protocol_holds(n, softmax_cycles, slots):
+@pytest.mark.parametrize("slots,pieces", [(SLOTS, 2), (12, 2), (6, 1)])
+def test_wide_forward_protocol_holds(n, softmax_cycles, slots, pieces):
     for seed in range(25):
-        errs = simulate(n, seed, softmax_cycles=softmax_cycles, slots=slots)
+        errs = simulate(n, seed, softmax_cycles=softmax_cycles, slots=slots, pieces=pieces)
         assert not errs, (n, seed, errs[:3])
 
 
@@ -252,6 +255,16 @@ def test_single_p_ready_barrier_races():
 
 def test_issuer_must_wait_for_k():
     assert count_bad(issuer_waits_k=False) > 0
+
+
+def test_fp8_ring_needs_split_p_ready_and_watcher_gate():
+    """One load per tile in six slots (the FP8 kernel): the single-barrier
+    protocol, an issuer that leaves the K wait to the ring, and a watcher that
+    arrives without waiting for the previous phase all break. Unlike the
+    five-slot bf16 ring, this ring lets V_{j+2} land before step j completes."""
+    assert count_bad(split=False, slots=6, pieces=1) > 0
+    assert count_bad(issuer_waits_k=False, slots=6, pieces=1) > 0
+    assert count_bad(watcher_gate=False, slots=6, pieces=1) > 0
 
 
 def test_watcher_gate_needed_with_a_deeper_ring():
