@@ -68,19 +68,27 @@ def item_v(j, n):
 
 
 def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watcher_gate=True,
-             issuer_waits_k=True, pieces=2):
+             issuer_waits_k=True, pieces=2, paired=False, xchg_buffers=2):
     """Errors seen in one run of n key tiles. `pieces` is the number of slot
     loads per K or V tile: two in the bf16 kernel, one in the FP8 kernel
     (csrc/fa_fwd_fp8_wide.cu, six slots of 32 KB, whose protocol is
-    otherwise the same). The other keyword switches take parts of the
-    protocol out, to show what each one guards against."""
+    otherwise the same). `paired` gives each row two softmax warps (one per
+    64-key half, as in the FP8 kernel) that exchange their partial row maxima
+    every step through a per-quarter barrier and a buffer per step parity
+    (`xchg_buffers`). The other keyword switches take parts of the protocol
+    out, to show what each one guards against."""
     rng = random.Random(seed)
     SLOTS = slots  # noqa: N806
     errors = []
     full = [Barrier(1) for _ in range(SLOTS)]
     empty = [Barrier(1) for _ in range(SLOTS)]
+    warps = 2 * SOFTMAX_WARPS if paired else SOFTMAX_WARPS
     s_full = [Barrier(1), Barrier(1)]
-    p_ready = [Barrier(SOFTMAX_WARPS + 1) for _ in range(2 if split else 1)]
+    p_ready = [Barrier(warps + 1) for _ in range(2 if split else 1)]
+    # row-max exchange: barrier per (lane quarter, step parity), two warps each;
+    # xbuf[(buffer, half, quarter)] = the step whose maximum it holds
+    xchg = [[Barrier(2) for _ in range(2)] for _ in range(SOFTMAX_WARPS)]
+    xbuf = {}
     pv_done, o_final = Barrier(1), Barrier(1)
 
     def pr(j):
@@ -93,7 +101,7 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
     in_flight = [None] * SLOTS
     s_buffer = [None, None]           # what a TMEM S buffer holds: ("S", j) or ("P", j)
     p_written = {}
-    warp_done = [-1] * SOFTMAX_WARPS
+    warp_done = [-1] * warps
     pipe = []
     clock = [0.0]
     events = []
@@ -114,7 +122,7 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
             kind, j, slot, load = op
             if landed[slot] != load or in_flight[slot] is not None:
                 errors.append(f"{kind}({j}) read slot {slot} holding {landed[slot]}, wanted load {load}")
-            if kind == "PV" and (p_written.get(j) != set(range(SOFTMAX_WARPS)) or s_buffer[j & 1] != ("P", j)):
+            if kind == "PV" and (p_written.get(j) != set(range(warps)) or s_buffer[j & 1] != ("P", j)):
                 errors.append(f"PV({j}) started before every warp wrote P_{j}")
             if kind == "S" and j >= 2 and min(warp_done) < j - 2:
                 errors.append(f"S({j}) overwrote P_{j - 2} while a warp still worked on it")
@@ -187,19 +195,34 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
                 yield from item(item_k(j + 2))
 
     def softmax(w):
+        quarter, half = w % SOFTMAX_WARPS, w // SOFTMAX_WARPS
         for j in range(n):
             yield ("wait", lambda j=j: s_full[j & 1].passes((j >> 1) & 1))
             if s_buffer[j & 1] != ("S", j) and s_buffer[j & 1] != ("P", j):
                 errors.append(f"warp {w} read {s_buffer[j & 1]} at step {j}")
+            if paired:
+                yield ("delay", rng.uniform(20, 300))          # S out of TMEM, this half's maximum
+                buf = j % xchg_buffers
+                xbuf[(buf, half, quarter)] = j
+                bar = xchg[quarter][j & 1]
+                bar.arrive()
+                yield ("wait", lambda b=bar, j=j: b.passes((j >> 1) & 1))
+                if bar.done < (j >> 1) + 1:
+                    errors.append(f"warp {w}: exchange wait for step {j} passed on an older phase")
+                # the read may trail the wait, now and then by a long time
+                yield ("delay", rng.uniform(0, 3000) if rng.random() < 0.2 else rng.uniform(0, 200))
+                got = xbuf.get((buf, 1 - half, quarter))
+                if got != j:
+                    errors.append(f"warp {w} read its partner's maximum of step {got} at step {j}")
             yield ("delay", rng.uniform(*softmax_cycles))
             p_written.setdefault(j, set()).add(w)
-            if p_written[j] == set(range(SOFTMAX_WARPS)):
+            if p_written[j] == set(range(warps)):
                 s_buffer[j & 1] = ("P", j)
             warp_done[w] = j
             pr(j).arrive()
         yield ("wait", lambda: o_final.passes(0))
 
-    roles = [tensor_core(), producer(), issuer(), watcher()] + [softmax(w) for w in range(SOFTMAX_WARPS)]
+    roles = [tensor_core(), producer(), issuer(), watcher()] + [softmax(w) for w in range(warps)]
     waiting = {}
     finished = set()
     for i in range(len(roles)):
@@ -237,10 +260,10 @@ def simulate(n, seed, split=True, softmax_cycles=(300, 1500), slots=SLOTS, watch
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 12])
 @pytest.mark.parametrize("softmax_cycles", [(300, 1500), (100, 5000)])
-@pytest.mark.parametrize("slots,pieces", [(SLOTS, 2), (12, 2), (6, 1)])
-def test_wide_forward_protocol_holds(n, softmax_cycles, slots, pieces):
+@pytest.mark.parametrize("slots,pieces,paired", [(SLOTS, 2, False), (12, 2, False), (6, 1, True), (12, 1, True)])
+def test_wide_forward_protocol_holds(n, softmax_cycles, slots, pieces, paired):
     for seed in range(25):
-        errs = simulate(n, seed, softmax_cycles=softmax_cycles, slots=slots, pieces=pieces)
+        errs = simulate(n, seed, softmax_cycles=softmax_cycles, slots=slots, pieces=pieces, paired=paired)
         assert not errs, (n, seed, errs[:3])
 
 
@@ -265,6 +288,13 @@ def test_fp8_ring_needs_split_p_ready_and_watcher_gate():
     assert count_bad(split=False, slots=6, pieces=1) > 0
     assert count_bad(issuer_waits_k=False, slots=6, pieces=1) > 0
     assert count_bad(watcher_gate=False, slots=6, pieces=1) > 0
+
+
+def test_fp8_row_max_exchange_needs_two_buffers():
+    """With one exchange buffer a warp can overwrite its maximum for step
+    j+1 before its partner has read the one of step j."""
+    assert count_bad(slots=6, pieces=1, paired=True) == 0
+    assert count_bad(slots=6, pieces=1, paired=True, xchg_buffers=1) > 0
 
 
 def test_watcher_gate_needed_with_a_deeper_ring():
