@@ -532,6 +532,6 @@ const char* fa_status_string(fa_status s) {
   return "unknown status";
 }
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 300; }
 
 }  // extern "C"
