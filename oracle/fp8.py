@@ -165,8 +165,8 @@ def p_rounding_bound(q, k, v, causal, scale, o_ref, rows=None):
     half a subnormal step, 2^-10 / 2^4 = 2^-14 in P' units, which is no more
     in P units. Both the sum and l scale alike, so
       |dO_c| <= 2^-4 sum_j (P_j / l)|V_jc| + 2^-14 sum_(visible j) |V_jc| / l.
-    Add the bf16 rounding of the result (2^-9 relative, taken as 2^-8) and
-    1e-6."""
+    Add the bf16 rounding of the result (at most 2^-8 of it: bf16 keeps an
+    8-bit significand) and 1e-6."""
     B, Hq, N, d = q.shape
     G = Hq // k.shape[1]
     sub = 2.0 ** -10 / P_SCALE
