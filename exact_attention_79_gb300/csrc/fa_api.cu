@@ -86,9 +86,11 @@ int test_stall() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// FP8 head dimensions: the quantisers move V in 64-column passes, and the
-// attention kernels are built for 128 (64 runs in it) and 256 (192 runs in it)
-bool fp8_dim(int d) { return d == 64 || d == 128 || d == 192 || d == 256; }
+// FP8 head dimensions: multiples of 16 up to 256 (a row of one-byte codes
+// must be a multiple of 16 bytes for TMA). The attention kernels are built
+// for 128 and 256; a smaller d runs in the next one up, its columns past d
+// read as zeros and never stored.
+bool fp8_dim(int d) { return d >= 16 && d <= 256 && d % 16 == 0; }
 
 // 3-D map over a dense [BH, N, d] tensor: dims (d, N, BH), one box = 128 rows
 // by 128 bytes with 128-byte swizzle. Rows past N read as zero and are not

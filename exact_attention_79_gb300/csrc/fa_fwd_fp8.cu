@@ -40,7 +40,7 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;                  // head dimension of the kernel (d = 64 runs in it, zero-filled)
+constexpr int kD = 128;                  // head dimension of the kernel (a smaller d runs in it, zero-filled)
 constexpr int kTile = 128 * 128;         // 128 rows x 128 e4m3 codes: one TMA box
 constexpr int kQRegion = 2 * kTile;      // a query tile's region: its codes and P buffer 0, later its bf16 O
 constexpr int kStages = 8;               // K / V^T ring slots
@@ -120,7 +120,8 @@ __global__ void fp8_v_amax_kernel(const __nv_bfloat16* __restrict__ v, unsigned*
 
 // V, pass 2: a 128-key chunk, 64 columns at a time, through shared memory into
 // V^T rows (keys contiguous), each column with its own scale; keys past N get
-// code 0. One CTA per (128-key chunk, head).
+// code 0. The last pass may hold fewer than 64 columns (d a multiple of 16):
+// columns past d are neither read nor written. One CTA per (128-key chunk, head).
 __global__ void __launch_bounds__(256) fp8_v_quant_kernel(const __nv_bfloat16* __restrict__ v,
                                                           const unsigned* __restrict__ amax_bits,
                                                           uint8_t* __restrict__ vt, int N, int NP, int d) {
@@ -132,13 +133,15 @@ __global__ void __launch_bounds__(256) fp8_v_quant_kernel(const __nv_bfloat16* _
     for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
       const int r = i >> 3, u = i & 7;
       uint4 val = make_uint4(0, 0, 0, 0);
-      if (k0 + r < N) val = *reinterpret_cast<const uint4*>(v + (static_cast<size_t>(bh) * N + k0 + r) * d + c0 + 8 * u);
+      if (k0 + r < N && c0 + 8 * u < d)
+        val = *reinterpret_cast<const uint4*>(v + (static_cast<size_t>(bh) * N + k0 + r) * d + c0 + 8 * u);
       *reinterpret_cast<uint4*>(&tile[r][8 * u]) = val;
     }
     __syncthreads();
     // 64 V^T rows x 128 keys: 512 chunks of sixteen codes; lanes take consecutive columns
     for (int i = threadIdx.x; i < 512; i += blockDim.x) {
       const int c = i & 63, u = i >> 6;              // column, 16-key group
+      if (c0 + c >= d) continue;
       const float s = block_scale(__uint_as_float(amax_bits[static_cast<size_t>(bh) * d + c0 + c]));
       uint32_t q[4];
 #pragma unroll
@@ -524,7 +527,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     named_bar_sync(1 + g, 128);
     if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {
-      // 64-column boxes; one that would start at or past d (d = 64) is skipped
+      // 64-column boxes; one that would start at or past d (d <= 64) is skipped
       for (int bx = 0; bx < 2; ++bx)
         if (bx * 64 < p.head_dim) tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * 64, qt[g] * kBM, bh);
       tma_store_commit();

@@ -1,5 +1,6 @@
 // FP8 (e4m3) forward with one 128-row query tile per CTA, for head dimensions
-// 192 and 256 (192 runs in the D = 256 kernel, zero-filled): the inputs of
+// above 128 (multiples of 16 up to 256, all in the D = 256 kernel, the columns
+// past d zero-filled): the inputs of
 // fa_fwd_fp8.cu's quantisers (Q, K with one scale per 64-row block, V
 // transposed with one scale per column), the same arithmetic (logits scaled
 // per row and key block, a running max that may trail by 2^4, 2^4 P rounded to

@@ -41,7 +41,7 @@ cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUte
 cudaError_t launch_fwd_wide(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mo, const FwdParams& p, cudaStream_t stream);
 
-// FP8 (e4m3) path, d = 64 and 128. Quantisers: rows of x [BH, N, d] bf16 -> codes
+// FP8 (e4m3) path, d a multiple of 16 up to 256. Quantisers: rows of x [BH, N, d] bf16 -> codes
 // [BH, N, d] and one scale per 64-row block; V [BH, N, d] bf16 -> V^T codes
 // [BH, d, NP] (NP = N rounded up to 128, zero codes past N) and one scale per
 // column (`scales` doubles as scratch for the column maxima). The forward
@@ -52,7 +52,7 @@ cudaError_t launch_fp8_quant_rows(const void* x, void* out, float* scales, int B
 cudaError_t launch_fp8_quant_v(const void* v, void* vt, float* scales, int BH, int N, int d, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mvt,
                            const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
-// The same computation for d = 192 and 256: one 128-row query tile per CTA,
+// The same computation for d in (128, 256]: one 128-row query tile per CTA,
 // Q / K maps with 128-byte boxes read at x = 0 and 128, the V^T map's 128-row
 // boxes at y = 0 and 128 (rows past d read as zeros).
 cudaError_t launch_fwd_fp8_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mvt,

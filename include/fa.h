@@ -113,10 +113,11 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                      int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
 
-/* FP8 forward (e4m3 inputs with block scales), d = 64, 128, 192 or 256 (64
- * runs in the d = 128 kernel and 192 in the d = 256 one, the columns past d
- * read as zeros); other head dimensions return FA_ERR_UNSUPPORTED, from the
- * quantisers and the forwards alike.
+/* FP8 forward (e4m3 inputs with block scales), d a multiple of 16 from 16 to
+ * 256 (a row of one-byte codes must be a multiple of 16 bytes for TMA; d up to
+ * 128 runs in the d = 128 kernel and above it in the d = 256 one, the columns
+ * past d read as zeros); other head dimensions return FA_ERR_UNSUPPORTED, from
+ * the quantisers and the forwards alike.
  * Source: "Flash Attention V3技术解析", section 1.3 (FP8 operands need the
  * contracted dimension contiguous, so P V reads V transposed; block-wise
  * quantisation) and section 3.2 (each block's scale from its largest
@@ -156,7 +157,7 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
  * s_ij) and l_i = sum_j P_ij, the result differs from the exact attention of
  * the dequantised inputs by at most 2^-4 sum_j (P_ij / l_i)|V_jc| +
  * 2^-14 sum_j |V_jc| / l_i per element (visible keys j), plus the bf16
- * rounding of O. FA_ERR_UNSUPPORTED for d other than 64, 128, 192 or 256. */
+ * rounding of O. FA_ERR_UNSUPPORTED for d not a multiple of 16. */
 fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
                      const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
                      float scale, void* stream);

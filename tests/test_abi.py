@@ -64,8 +64,8 @@ def test_invalid_arguments_rejected_without_device(lib):
 
 
 def test_head_dim_and_fp8_rules_without_device(lib):
-    """Head dims 8..256 for the forward, 8..128 for every backward, 64, 128,
-    192 and 256 for FP8: the host checks answer before any device work."""
+    """Head dims 8..256 for the forward, 8..128 for every backward, multiples
+    of 16 up to 256 for FP8: the host checks answer before any device work."""
     null = ctypes.c_void_p(0)
     fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
     assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 264, 0, 0.125, null) == 1    # past 256
@@ -77,13 +77,14 @@ def test_head_dim_and_fp8_rules_without_device(lib):
     assert lib.fa_bwd_noalloc(*args, 1, 1, 1, 128, 136, 1, 0.1, null) == 2
     assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 256) == 0
     assert lib.fa_bwd_blocksparse_workspace_bytes(1, 2, 2, 128, 192) == 0
-    # FP8: d = 64, 128, 192, 256; other sizes are valid arguments but not built
-    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 96, 0, 0.1, null) == 2
-    assert lib.fa_fwd_fp8_kv(*([fake] * 8), 1, 1, 1, 128, 300, 160, 0, 0.1, null) == 2
-    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 224, 0, 0.1, null) == 2
+    # FP8: multiples of 16 up to 256; other multiples of 8 are valid arguments
+    # but not built (a row of codes must be a multiple of 16 bytes for TMA)
+    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 8, 0, 0.1, null) == 2
+    assert lib.fa_fwd_fp8_kv(*([fake] * 8), 1, 1, 1, 128, 300, 152, 0, 0.1, null) == 2
+    assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 264, 0, 0.1, null) == 1
     assert lib.fa_fp8_quantize_v(fake, fake, fake, 4, 100, 200, null) == 2
     assert lib.fa_fwd_fp8(*([fake] * 7 + [null]), 1, 1, 1, 128, 128, 0, 0.1, null) == 1
-    assert lib.fa_fp8_quantize_rows(fake, fake, fake, 4, 100, 32, null) == 2
+    assert lib.fa_fp8_quantize_rows(fake, fake, fake, 4, 100, 40, null) == 2
     assert lib.fa_fp8_quantize_v(fake, fake, fake, 0, 100, 128, null) == 1
     # scale-array and padded-key helpers
     assert lib.fa_fp8_row_scales(1) == 1 and lib.fa_fp8_row_scales(64) == 1 and lib.fa_fp8_row_scales(65) == 2

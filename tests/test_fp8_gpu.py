@@ -122,7 +122,7 @@ def test_fp8_head_dim_64(fa, N, causal):
     check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, 64 ** -0.5)
 
 
-@pytest.mark.parametrize("d", [96, 160])
+@pytest.mark.parametrize("d", [24, 40, 136])
 def test_fp8_refuses_other_head_dims(fa, d):
     x = torch.zeros(1, 1, 128, d, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(pkg.FAError):
@@ -256,3 +256,28 @@ def test_fp8_wide_forward_full_size_sampled_rows(fa):
     err = np.abs(o[bi, hi, rows].float().cpu().numpy() - ro)
     assert (err <= bound).all(), float((err - bound).max())
     assert np.abs(lse[bi, hi, rows].cpu().numpy() - rl).max() <= configs.TOL_LSE_MAX
+
+
+# ---- head dimensions between the built ones: multiples of 16, zero-filled in the next kernel up
+
+@pytest.mark.parametrize("d,N", [(16, 200), (48, 333), (96, 129), (160, 300), (224, 1000)])
+def test_fp8_ragged_head_dim_quantisers_bit_exact(fa, d, N):
+    """The V quantiser's last 64-column pass holds d % 64 columns."""
+    t = inputs.make_inputs(2, 2, 1, N, d, "bf16", seed=3 * N + d)
+    got = [x.cpu().numpy() for x in quantized(t)]
+    fa.check_device_status()
+    for name, a, r in zip(("q8", "q_scale", "k8", "k_scale", "vt8", "v_scale"), got, oracle_quant(t)):
+        assert a.shape == r.shape, name
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              r.view(np.uint32) if r.dtype == np.float32 else r), name
+
+
+@pytest.mark.parametrize("d", [32, 96, 160, 224])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_ragged_head_dim_forward_within_rounding_bound(fa, d, causal):
+    t = inputs.make_inputs(1, 4, 2, 700, d, "bf16", seed=17 * d + causal)
+    q8, qs, k8, ks, vt8, vs = quantized(t)
+    o, lse = pkg.fwd_fp8(q8, qs, k8, ks, vt8, vs, causal=causal)
+    fa.check_device_status()
+    host = [x.cpu().numpy() for x in (q8, qs, k8, ks, vt8, vs)]
+    check_against_bound(o.float().cpu().numpy(), lse.cpu().numpy(), *host, causal, d ** -0.5)
