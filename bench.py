@@ -237,6 +237,31 @@ def traffic_from_profile(kernel_file, kernel_name, workload):
         return None
 
 
+# ------------------------------------------------------------------ exponential ceiling, step spread
+def exp_roofline(w, ex2_per_cycle_per_sm, n_sms, sm_mhz, fwd_ms, kernel):
+    """The forward kernel against the exponential unit: one ex2 per visible
+    (query, key) pair, flops_fwd / (4 d) of them, over the ex2 rate measured
+    on this GPU (fa_ex2_throughput) at the SM clock sampled under load. None
+    when the clock or the rate is unknown."""
+    if not sm_mhz or not ex2_per_cycle_per_sm or ex2_per_cycle_per_sm <= 0 or fwd_ms <= 0:
+        return None
+    exps = w.flops_fwd / (4.0 * w.d)
+    peak = ex2_per_cycle_per_sm * n_sms * sm_mhz * 1e6 / 1e9
+    achieved = exps / (fwd_ms / 1e3) / 1e9
+    return {"bound": "exp", "achieved": achieved, "peak": peak, "unit": "Gexp/s", "frac": achieved / peak,
+            "kernel": kernel, "exps_per_launch": exps, "ex2_per_cycle_per_sm": ex2_per_cycle_per_sm,
+            "n_sms": n_sms, "sm_mhz": sm_mhz}
+
+
+def percentiles(xs):
+    """p10, p50, p90 of a list of step times (nearest rank)."""
+    v = sorted(xs)
+    if not v:
+        return None
+    pick = lambda q: v[min(len(v) - 1, int(round(q * (len(v) - 1))))]  # noqa: E731
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9)}
+
+
 # ------------------------------------------------------------------ replicas across ranks
 def max_over_ranks(x, world):
     """The largest of every rank's x (one float); x itself on a single rank.
@@ -392,6 +417,8 @@ def native_arm(args, w):
         flush.zero_()
         step(new_events())
     fa.check_device_status(stream.cuda_stream)
+    # the exponential unit's rate on this GPU (a half-millisecond probe, before the timed region)
+    ex2_rate = fa.ex2_throughput(stream.cuda_stream)
 
     gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if world > 1 or \
         "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
@@ -512,6 +539,7 @@ def native_arm(args, w):
     if rank != 0:
         return
     clocks = sampler.summary(t0, t1)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     line = {
         "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -526,6 +554,8 @@ def native_arm(args, w):
         "bwd_tflops": None if fwd_only else w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
         "kernel_ms": {n: m for n, m in zip(names, mean) if n != "-"},
         "roofline": roofline,
+        "exp_roofline": exp_roofline(w, ex2_rate, n_sms, clocks.get("sm_mhz"), mean[0], names[0]),
+        "step_ms_percentiles": percentiles(step_ms),
         "e2e": e2e,
         # fwd, preprocess, [block list], dK/dV, dQ convert
         "gpu_launches": (1 if (fwd_only or fp8) else 5 if sparse else 4) * args.steps,

@@ -46,6 +46,7 @@ SIGNATURES = {
     "fa_fp8_quantize_v": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     "fa_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_fp8_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_ex2_throughput": (_I, [ctypes.POINTER(ctypes.c_double), _VP]),
     "fa_device_status": (_I, [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),
@@ -261,6 +262,16 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
                                     B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(q)))
     return dq, dk, dv
+
+
+def ex2_throughput(stream=None):
+    """ex2 results per SM clock cycle on the current device (fa_ex2_throughput):
+    the rate behind the forward's exponential ceiling."""
+    import torch
+    s = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    out = ctypes.c_double(0.0)
+    _check("fa_ex2_throughput", load().fa_ex2_throughput(ctypes.byref(out), s))
+    return out.value
 
 
 def check_device_status(stream=None):

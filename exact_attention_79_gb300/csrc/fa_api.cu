@@ -504,6 +504,17 @@ fa_status fa_fwd_fp8_kv(const void* q, const float* q_scale, const void* k, cons
   return fwd_fp8_common(q, q_scale, k, k_scale, vt, v_scale, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
 }
 
+fa_status fa_ex2_throughput(double* per_sm_per_cycle, void* stream) {
+  if (!per_sm_per_cycle) return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int num_sms = 0;
+  const fa_status st = device_state(&status, &num_sms);
+  if (st != FA_OK) return st;
+  if (num_sms > fa::kEx2MaxSms) return FA_ERR_UNSUPPORTED;
+  return fa::measure_ex2_rate(num_sms, 4096, per_sm_per_cycle, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_device_status(void* stream) {
   unsigned* status = nullptr;
   fa_status st = device_state(&status);

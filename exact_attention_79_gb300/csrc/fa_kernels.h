@@ -58,6 +58,13 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& mq, const CUtensorMap& mk, const C
 cudaError_t launch_fwd_fp8_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mvt,
                                 const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
 
+// Exponential-unit probe: one CTA of kEx2Threads per SM, eight ex2 chains
+// per thread for `iters` steps; returns ex2 results per SM clock (mean over
+// SMs). Synchronises the stream.
+constexpr int kEx2Threads = 512;
+constexpr int kEx2MaxSms = 1024;
+cudaError_t measure_ex2_rate(int num_sms, int iters, double* per_sm_per_cycle, cudaStream_t stream);
+
 struct BwdParams {
   float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows
   float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows

@@ -267,6 +267,19 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * reported an error). */
 fa_status fa_device_status(void* stream);
 
+/* Diagnostic: throughput of the exponential instruction the softmax uses
+ * (ex2.approx), measured on the current device, for the exponential ceiling
+ * of the forward (one exponential per 4 d floating-point operations).
+ * Source: "4.3 FlashAttention-2与FlashAttention-3演进", FlashAttention-3
+ * section 1 (the exponential unit is much slower than the tensor cores).
+ * Every SM runs 512 threads of eight independent ex2 chains for 4096 steps
+ * (about half a millisecond); *per_sm_per_cycle receives the mean over SMs
+ * of ex2 results per SM clock cycle. Synchronises `stream`. Allocates
+ * nothing: the per-SM cycle counts go to a static device array, so calls that
+ * overlap on the GPU race. FA_ERR_INVALID_ARG for a null pointer,
+ * FA_ERR_UNSUPPORTED for more than 1024 SMs. */
+fa_status fa_ex2_throughput(double* per_sm_per_cycle, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 

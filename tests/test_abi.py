@@ -39,6 +39,10 @@ def test_status_strings_and_version(lib):
     assert lib.fa_version() >= 100
 
 
+def test_ex2_probe_rejects_a_null_result_pointer(lib):
+    assert lib.fa_ex2_throughput(None, None) == 1
+
+
 def test_workspace_size_formula(lib):
     # lse2 + D: B*Hq*ceil(N/128)*128 floats each; dQ accumulator: B*Hq*N*d floats
     assert lib.fa_bwd_workspace_bytes(1, 16, 16, 8192, 128) == 2 * 16 * 8192 * 4 + 16 * 8192 * 128 * 4

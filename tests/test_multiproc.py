@@ -57,3 +57,23 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_exp_roofline_and_percentiles_arithmetic():
+    """The exponential ceiling counts one ex2 per visible (query, key) pair,
+    flops_fwd / (4 d) of them (4 d floating-point operations per pair); the
+    step spread is nearest-rank."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from exact_attention_79_gb300 import configs
+    w = configs.WORKLOADS["bf16_h16_n8192_d128_causal_fwdbwd"]
+    r = bench.exp_roofline(w, 8.0, 152, 2000.0, 0.5, "fwd_kernel")
+    exps = w.flops_fwd / (4 * 128)
+    assert abs(r["exps_per_launch"] - exps) < 1e-6 * exps
+    assert abs(r["peak"] - 8.0 * 152 * 2000e6 / 1e9) < 1e-9
+    assert abs(r["achieved"] - exps / 0.5e-3 / 1e9) < 1e-6 * r["achieved"]
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    assert bench.exp_roofline(w, 8.0, 152, None, 0.5, "fwd_kernel") is None
+    p = bench.percentiles([5.0, 1.0, 3.0, 2.0, 4.0, 6.0, 7.0, 8.0, 9.0, 10.0, 11.0])
+    assert p == {"p10": 2.0, "p50": 6.0, "p90": 10.0}
+    assert bench.percentiles([]) is None
