@@ -80,9 +80,10 @@ def test_encode_ties_and_saturation():
         e(np.array([np.inf], np.float32))
 
 
-def test_quantize_rows_properties():
-    rng = np.random.default_rng(7)
-    x = torch.from_numpy(rng.normal(0, 2, (2, 3, 200, 128)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+@pytest.mark.parametrize("d", [16, 96, 128])
+def test_quantize_rows_properties(d):
+    rng = np.random.default_rng(7 + d)
+    x = torch.from_numpy(rng.normal(0, 2, (2, 3, 200, d)).astype(np.float32)).to(torch.bfloat16).float().numpy()
     x[0, 0, 64:128] = 0.0                                            # an all-zero block
     codes, scales = fp8.quantize_rows(x)
     assert codes.shape == x.shape and scales.shape == (2, 3, 4)
@@ -101,14 +102,15 @@ def test_quantize_rows_properties():
     assert (err <= np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * blk_scale) * (1 + 1e-6)).all()
 
 
-def test_quantize_v_transposed_layout():
-    rng = np.random.default_rng(8)
-    v = rng.normal(0, 1, (1, 2, 150, 128)).astype(np.float32)
+@pytest.mark.parametrize("d", [16, 48, 128, 224])
+def test_quantize_v_transposed_layout(d):
+    rng = np.random.default_rng(8 + d)
+    v = rng.normal(0, 1, (1, 2, 150, d)).astype(np.float32)
     codes, scales = fp8.quantize_v_transposed(v)
-    assert codes.shape == (1, 2, 128, 256) and scales.shape == (1, 2, 128)
+    assert codes.shape == (1, 2, d, 256) and scales.shape == (1, 2, d)
     assert (codes[..., 150:] == 0).all()
     # column c of V is row c of V^T, quantised with its own scale
-    c = 17
+    c = min(17, d - 1)
     s = np.float32(np.abs(v[0, 1, :, c]).max() / np.float32(448.0))
     assert scales[0, 1, c] == s
     assert np.array_equal(codes[0, 1, c, :150], fp8.e4m3_encode((v[0, 1, :, c] / s).astype(np.float32)))
