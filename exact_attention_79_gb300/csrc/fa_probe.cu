@@ -1,9 +1,10 @@
 // Throughput of the exponential instruction the softmax runs (ex2.approx),
 // measured on the device at hand: the second ceiling of the forward besides
 // the tensor cores. The forward takes one exponential per 4 d of its
-// floating-point operations ("4.3 FlashAttention-2与FlashAttention-3演进",
-// FlashAttention-3 section 1: the exponential unit is far slower than the
-// tensor cores), so at small d the exponentials can bound it.
+// floating-point operations, and work off the matrix units runs at a small
+// fraction of their rate ("FlashAttention v2相比于v1有哪些更新", sections 2
+// and 3, "CUDA Core vs. Tensor Core": up to 16 times lower), so at small d
+// the exponentials can bound it.
 //
 // One CTA per SM, 512 threads (four warps per scheduler), each running eight
 // independent chains x <- 2^-x, which stay in (0, 1]. Every CTA records the

@@ -270,8 +270,9 @@ fa_status fa_device_status(void* stream);
 /* Diagnostic: throughput of the exponential instruction the softmax uses
  * (ex2.approx), measured on the current device, for the exponential ceiling
  * of the forward (one exponential per 4 d floating-point operations).
- * Source: "4.3 FlashAttention-2与FlashAttention-3演进", FlashAttention-3
- * section 1 (the exponential unit is much slower than the tensor cores).
+ * Source: "FlashAttention v2相比于v1有哪些更新", sections 2 and 3 ("CUDA
+ * Core vs. Tensor Core": work off the matrix units runs up to 16 times
+ * slower than on them).
  * Every SM runs 512 threads of eight independent ex2 chains for 4096 steps
  * (about half a millisecond); *per_sm_per_cycle receives the mean over SMs
  * of ex2 results per SM clock cycle. Synchronises `stream`. Allocates
