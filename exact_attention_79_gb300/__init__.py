@@ -94,8 +94,26 @@ def _ptr(t):
 
 
 def _shape(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D: [B, H, N, d]")
     B, Hq, N, d = q.shape
     return B, Hq, k.shape[1], N, d
+
+
+def _require(device, *specs):
+    """Refuse, before any launch, a tensor the kernels would read or write past
+    its end. specs: (tensor, name, dtype, shape). Every dtype and shape is
+    checked before any placement (contiguous, CUDA, on the device of q), so
+    the shape rules hold for CPU tensors too."""
+    for t, name, dtype, shape in specs:
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: expected {dtype} of shape {tuple(shape)}, "
+                             f"got {t.dtype} of shape {tuple(t.shape)}")
+    for t, name, _, _ in specs:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda or t.device != device:
+            raise ValueError(f"{name} must be a CUDA tensor on {device}")
 
 
 def _mask_args(block_mask, B, Hq, N, device):
@@ -130,12 +148,14 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, block_mask=None):
     B, Hq, Hkv, N, d = _shape(q, k)
     if scale is None:
         scale = d ** -0.5
-    for t in (q, k, v):
-        if not t.is_contiguous() or not t.is_cuda or t.dtype != q.dtype:
-            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    Nk = k.shape[2]
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must be bf16 or fp32")
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    Nk = k.shape[2]
+    _require(q.device, (q, "q", q.dtype, (B, Hq, N, d)), (k, "k", q.dtype, (B, Hkv, Nk, d)),
+             (v, "v", q.dtype, (B, Hkv, Nk, d)), (o, "out", q.dtype, (B, Hq, N, d)),
+             (lse, "lse", torch.float32, (B, Hq, N)))
     if Nk != N:
         if q.dtype != torch.bfloat16 or block_mask is not None:
             raise ValueError("keys of another length need bf16 inputs and no block mask")
@@ -193,16 +213,18 @@ def fwd_fp8(q8, q_scale, k8, k_scale, vt8, v_scale, causal=False, scale=None, ou
     returned by quantize_fp8."""
     import torch
     lib = load()
-    B, Hq, N, d = q8.shape
-    Hkv = k8.shape[1]
-    for t in (q8, q_scale, k8, k_scale, vt8, v_scale):
-        if not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("fp8 inputs must be contiguous CUDA tensors")
+    B, Hq, Hkv, N, d = _shape(q8, k8)
+    Nk = k8.shape[2]
+    dev = q8.device
     if scale is None:
         scale = d ** -0.5
-    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
-    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device) if lse is None else lse
-    Nk = k8.shape[2]
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev) if lse is None else lse
+    f32, u8 = torch.float32, torch.uint8
+    _require(dev, (q8, "q8", u8, (B, Hq, N, d)), (q_scale, "q_scale", f32, (B, Hq, int(lib.fa_fp8_row_scales(N)))),
+             (k8, "k8", u8, (B, Hkv, Nk, d)), (k_scale, "k_scale", f32, (B, Hkv, int(lib.fa_fp8_row_scales(Nk)))),
+             (vt8, "vt8", u8, (B, Hkv, d, int(lib.fa_fp8_vt_keys(Nk)))), (v_scale, "v_scale", f32, (B, Hkv, d)),
+             (o, "out", torch.bfloat16, (B, Hq, N, d)), (lse, "lse", f32, (B, Hq, N)))
     if Nk != N:
         # queries are the last N of Nk positions (fa_fwd_fp8_kv)
         _check("fa_fwd_fp8_kv", lib.fa_fwd_fp8_kv(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(vt8),
@@ -230,12 +252,11 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     B, Hq, Hkv, N, d = _shape(q, k)
     if scale is None:
         scale = d ** -0.5
-    for t in (q, k, v, o, do):
-        if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
-            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
+    Nk = k.shape[2]
+    dev = q.device
+    bf16 = torch.bfloat16
     if block_mask is not None and deterministic:
         raise ValueError("the deterministic backward has no block-sparse form")
-    Nk = k.shape[2]
     if Nk != N and (deterministic or block_mask is not None):
         raise ValueError("keys of another length: only the default backward")
     nbytes = (int(lib.fa_bwd_blocksparse_workspace_bytes(B, Hq, Hkv, N, d)) if block_mask is not None
@@ -245,6 +266,11 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    # the workspace's byte count is passed on; the library refuses one that is too small
+    _require(dev, (q, "q", bf16, (B, Hq, N, d)), (k, "k", bf16, (B, Hkv, Nk, d)), (v, "v", bf16, (B, Hkv, Nk, d)),
+             (o, "o", bf16, (B, Hq, N, d)), (lse, "lse", torch.float32, (B, Hq, N)), (do, "do", bf16, (B, Hq, N, d)),
+             (workspace, "workspace", torch.uint8, (workspace.numel(),)), (dq, "dq", bf16, (B, Hq, N, d)),
+             (dk, "dk", bf16, (B, Hkv, Nk, d)), (dv, "dv", bf16, (B, Hkv, Nk, d)))
     if Nk != N:
         _check("fa_bwd_kv", lib.fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
                                           _ptr(dv), _ptr(workspace), workspace.numel(), B, Hq, Hkv, N, Nk, d,

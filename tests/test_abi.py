@@ -94,3 +94,39 @@ def test_head_dim_and_fp8_rules_without_device(lib):
     assert lib.fa_fp8_row_scales(1) == 1 and lib.fa_fp8_row_scales(64) == 1 and lib.fa_fp8_row_scales(65) == 2
     assert lib.fa_fp8_vt_keys(1) == 128 and lib.fa_fp8_vt_keys(128) == 128 and lib.fa_fp8_vt_keys(129) == 256
     assert lib.fa_fp8_row_scales(0) == 0 and lib.fa_fp8_vt_keys(0) == 0
+
+
+def test_binding_refuses_mismatched_tensors_before_any_launch(lib):
+    """Shapes and dtypes are checked for every tensor before placement, so CPU
+    tensors show it: a wrong output, gradient, workspace or FP8 scale buffer
+    never reaches a kernel that would write or read past its end."""
+    import torch
+    import exact_attention_79_gb300 as fa
+    bf = torch.bfloat16
+    q = torch.zeros(1, 2, 64, 64, dtype=bf)
+    k = torch.zeros(1, 1, 64, 64, dtype=bf)
+    lse = torch.zeros(1, 2, 64)
+    with pytest.raises(ValueError, match="^v:"):
+        fa.fwd(q, k, torch.zeros(1, 1, 64, 32, dtype=bf))
+    with pytest.raises(ValueError, match="^out:"):
+        fa.fwd(q, k, k, out=torch.zeros(1, 2, 64, 64))
+    with pytest.raises(ValueError, match="^lse:"):
+        fa.fwd(q, k, k, lse=torch.zeros(1, 2, 63))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fa.fwd(q, k, k)
+    with pytest.raises(ValueError, match="^do:"):
+        fa.bwd(q, k, k, q, lse, torch.zeros(1, 2, 64, 32, dtype=bf))
+    with pytest.raises(ValueError, match="^dk:"):
+        fa.bwd(q, k, k, q, lse, q, workspace=torch.zeros(16, dtype=torch.uint8), dk=torch.zeros(1, 2, 64, 64, dtype=bf))
+    with pytest.raises(ValueError, match="^workspace:"):
+        fa.bwd(q, k, k, q, lse, q, workspace=torch.zeros(16, dtype=torch.float32))
+    u8 = torch.uint8
+    q8, k8 = torch.zeros(1, 2, 64, 64, dtype=u8), torch.zeros(1, 1, 64, 64, dtype=u8)
+    qs, ks = torch.zeros(1, 2, 1), torch.zeros(1, 1, 1)
+    vt8, vs = torch.zeros(1, 1, 64, 128, dtype=u8), torch.zeros(1, 1, 64)
+    with pytest.raises(ValueError, match="^v_scale:"):
+        fa.fwd_fp8(q8, qs, k8, ks, vt8, torch.zeros(1, 1, 64, dtype=bf))
+    with pytest.raises(ValueError, match="^vt8:"):
+        fa.fwd_fp8(q8, qs, k8, ks, torch.zeros(1, 1, 64, 64, dtype=u8), vs)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fa.fwd_fp8(q8, qs, k8, ks, vt8, vs)
