@@ -186,13 +186,10 @@ def quantize_fp8(q, k, v):
     fp32 [B, Hkv, d]."""
     import torch
     lib = load()
-    for t in (q, k, v):
-        if not t.is_contiguous() or not t.is_cuda or t.dtype != torch.bfloat16:
-            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
-    B, Hq, N, d = q.shape
-    Hkv, Nk = k.shape[1], k.shape[2]
-    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    B, Hq, Hkv, N, d = _shape(q, k)
+    Nk = k.shape[2]
+    bf16 = torch.bfloat16
+    _require(q.device, (q, "q", bf16, (B, Hq, N, d)), (k, "k", bf16, (B, Hkv, Nk, d)), (v, "v", bf16, (B, Hkv, Nk, d)))
     nb, nbk, NP = int(lib.fa_fp8_row_scales(N)), int(lib.fa_fp8_row_scales(Nk)), int(lib.fa_fp8_vt_keys(Nk))
     dev = q.device
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)

@@ -130,3 +130,5 @@ def test_binding_refuses_mismatched_tensors_before_any_launch(lib):
         fa.fwd_fp8(q8, qs, k8, ks, torch.zeros(1, 1, 64, 64, dtype=u8), vs)
     with pytest.raises(ValueError, match="CUDA tensor"):
         fa.fwd_fp8(q8, qs, k8, ks, vt8, vs)
+    with pytest.raises(ValueError, match="^v:"):
+        fa.quantize_fp8(q, k, torch.zeros(1, 1, 64, 64))
