@@ -391,10 +391,16 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   auto bar_s_full = [&](int x) { return bars + 8u + 16u * C::kStages + 8u * x; };  // 2
   const uint32_t bar_dp_full = bars + 24 + 16 * C::kStages;
   const uint32_t bar_dp_read = bars + 32 + 16 * C::kStages;
-  const uint32_t bar_ds_ready = bars + 40 + 16 * C::kStages;
-  const uint32_t bar_dq_final = bars + 48 + 16 * C::kStages;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 56 + 16 * C::kStages);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 60 + 16 * C::kStages);
+  // dS-ready of key tile j is barrier j % 2. A warp that has written dS_j may
+  // already hold S_{j+1} (issued before the dP-read wait) and dP_{j+1} (issued
+  // once every warp has read dP_j) and arrive for tile j+1 while a slower warp
+  // is still writing dS_j: with one barrier that arrival would complete tile
+  // j's phase early. No warp gets two tiles ahead: dP_{j+2} waits for every
+  // warp to read dP_{j+1}, which each does after its tile-j arrival.
+  auto bar_ds_ready = [&](int j) { return bars + 40u + 16u * C::kStages + 8u * (j & 1); };
+  const uint32_t bar_dq_final = bars + 56 + 16 * C::kStages;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 64 + 16 * C::kStages);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 68 + 16 * C::kStages);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -418,7 +424,8 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     mbar_init(bar_s_full(1), 1);
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_dp_read, 256);
-    mbar_init(bar_ds_ready, 256);
+    mbar_init(bar_ds_ready(0), 256);
+    mbar_init(bar_ds_ready(1), 256);
     mbar_init(bar_dq_final, 1);
     fence_mbar_init();
   }
@@ -520,7 +527,7 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           mma_commit(bar_dp_full);
           mma_commit(bar_kv_empty(vslot));
         }
-        if (!mbar_wait(bar_ds_ready, j & 1, abort_flag, deadline)) { ok = false; break; }
+        if (!mbar_wait(bar_ds_ready(j), (j >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
         // dQ += dS_j K_j  (K = 128 keys; dS of key k sits in column S_x + 64*(k/64) + (k%64)/2)
         const uint64_t km = slot_mn(kslot_j);
@@ -588,7 +595,7 @@ det_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tmem_st_32x32b_x32(tbase + lane_off + scol + 64 * g, dd);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ds_ready);
+      mbar_arrive(bar_ds_ready(j));
     }
     // ---------------------------------------------------------- dQ epilogue
     if (ok) {
