@@ -273,3 +273,222 @@ def test_slots_go_back_after_the_last_issued_s():
 
 def test_slots_go_back_only_after_s_completes():
     assert bad_runs(release_after_s=False) > 0
+
+
+# ---------------------------------------------------------------- fp32 (tf32) variant
+def simulate_tf32(n, seed, *, slots=3, vt_wait_s=True, issuer_waits_p=True, warp_cycles=(300, 1500)):
+    """The fp32 instantiation: one query tile, a three-slot ring, no watcher.
+    The issuer waits for every load itself; besides the softmax, the four
+    warps of the tile split Q and K_0 into tf32 high and low parts (the low
+    parts in their own buffers, signalled by Q-K-ready), transpose V_j into a
+    V^T buffer (the second Q region) and split K_{j+1}, each warp its own
+    rows, before arriving on P-ready. Those buffers are rewritten at step j+1
+    only after S_{j+1} has completed, which follows P(j) V^T. With
+    vt_wait_s=False the warps write V^T_{j+1} as soon as V_{j+1} lands."""
+    rng = random.Random(seed)
+    errors = []
+    full = [Barrier(1) for _ in range(slots)]
+    empty = [Barrier(1) for _ in range(slots)]
+    q_full, s_full, o_final = Barrier(1), Barrier(1), Barrier(1)
+    p_ready, qk_ready = Barrier(WARPS), Barrier(WARPS)
+    landed = [None] * slots
+    in_flight = [None] * slots
+    split_rows = {}                            # load of a K tile -> warps that split it (hi in place, lo buffer)
+    k_lo = [None]                              # (load, warps) whose low part the lo buffer holds
+    vt = [None]                                # (j, warps) whose V^T the V^T buffer holds
+    q_landed = [False]
+    tmem_s = [None]
+    p_written = {}
+    done = {"S": -1, "PV": -1}
+    pipe = []
+    clock = [0.0]
+    events = []
+
+    def wait(bar, parity, who, phase=None):
+        yield ("wait", lambda: bar.passes(parity))
+        if phase is not None and bar.done < phase + 1:
+            errors.append(f"{who}: parity wait for phase {phase} passed on an older phase")
+
+    def tensor_core():
+        while True:
+            while not pipe:
+                yield ("wait", lambda: bool(pipe))
+            op = pipe.pop(0)
+            if op[0] == "commit":
+                op[1].arrive()
+                continue
+            kind, j, load = op
+            if kind == "S":
+                if landed[load % slots] != load:
+                    errors.append(f"S({j}) read slot {load % slots} holding {landed[load % slots]}")
+                if k_lo[0] != (load, WARPS) or len(split_rows.get(load, ())) < WARPS:
+                    errors.append(f"S({j}) read K low parts {k_lo[0]}, wanted every row of load {load}")
+                if j > 0 and done["PV"] < j - 1:
+                    errors.append(f"S({j}) overwrote P({j - 1}) before P V read it")
+            else:
+                if vt[0] != (j, WARPS):
+                    errors.append(f"PV({j}) read V^T buffer holding {vt[0]}")
+                if tmem_s[0] != ("P", j):
+                    errors.append(f"PV({j}) read TMEM holding {tmem_s[0]}")
+            yield ("delay", rng.uniform(200, 300))
+            done[kind] = j
+            if kind == "S":
+                tmem_s[0] = ("S", j)
+
+    def producer():
+        q_full.expect_tx(1)
+        q_full.arrive()
+
+        def land_q():
+            q_landed[0] = True
+            q_full.complete_tx(1)
+        heapq.heappush(events, (clock[0] + rng.uniform(300, 3000), rng.random(), ("call", land_q)))
+        for c in range(2 * n):
+            slot = c % slots
+            yield from wait(empty[slot], ((c // slots) & 1) ^ 1, "producer")
+            if in_flight[slot] is not None:
+                errors.append(f"load {c} issued into slot {slot} with a load in flight")
+            prev = c - slots
+            if prev >= 0 and prev % 2 == 0 and done["S"] < prev // 2:
+                errors.append(f"load {c} overwrote K load {prev} before S read it")
+            full[slot].expect_tx(1)
+            full[slot].arrive()
+            in_flight[slot], landed[slot] = c, None
+
+            def land(s=slot, ld=c):
+                in_flight[s], landed[s] = None, ld
+                full[s].complete_tx(1)
+            heapq.heappush(events, (clock[0] + rng.uniform(300, 3000), rng.random(), ("call", land)))
+
+    def issuer():
+        if n == 0:
+            return
+        c = [0]
+
+        def take():
+            ld = c[0]
+            c[0] += 1
+            yield from wait(full[ld % slots], (ld // slots) & 1, "issuer", ld // slots)
+            return ld
+
+        yield from wait(q_full, 0, "issuer q", 0)
+        k = yield from take()
+        yield from wait(qk_ready, 0, "issuer qk", 0)
+        pipe.extend([("S", 0, k), ("commit", s_full), ("commit", empty[k % slots])])
+        for j in range(n):
+            v = yield from take()
+            kn = (yield from take()) if j + 1 < n else None
+            if issuer_waits_p:
+                yield from wait(p_ready, j & 1, "issuer p_ready", j)
+            pipe.append(("PV", j, v))
+            if kn is not None:
+                pipe.extend([("S", j + 1, kn), ("commit", s_full)])
+            else:
+                pipe.append(("commit", o_final))
+            pipe.append(("commit", empty[v % slots]))
+            if kn is not None:
+                pipe.append(("commit", empty[kn % slots]))
+
+    def split_k(w, load):
+        """This warp's rows of K tile `load`: high part in place, low part into the lo buffer."""
+        if k_lo[0] is None or k_lo[0][0] != load:
+            k_lo[0] = (load, 0)
+        split_rows.setdefault(load, set()).add(w)
+        k_lo[0] = (load, len(split_rows[load]))
+
+    def warp(w):
+        if n == 0:
+            return
+        yield from wait(q_full, 0, f"warp {w} q", 0)
+        yield from wait(full[0], 0, f"warp {w} K_0", 0)
+        if landed[0] != 0:
+            errors.append(f"warp {w} split K_0 from slot 0 holding {landed[0]}")
+        split_k(w, 0)
+        qk_ready.arrive()
+        for j in range(n):
+            yield from wait(s_full, j & 1, f"warp {w} s_full", j)
+            if tmem_s[0] != ("S", j) and not (tmem_s[0] == ("P", j) and w not in p_written.get(j, ())):
+                errors.append(f"warp {w} read S({j}) from TMEM holding {tmem_s[0]}")
+            yield ("delay", rng.uniform(*warp_cycles))
+            p_written.setdefault(j, set()).add(w)
+            if len(p_written[j]) == WARPS:
+                tmem_s[0] = ("P", j)
+            # V_j into the V^T buffer, this warp's key rows
+            cv = 2 * j + 1
+            yield from wait(full[cv % slots], (cv // slots) & 1, f"warp {w} V", cv // slots)
+            if landed[cv % slots] != cv:
+                errors.append(f"warp {w} transposed V_{j} from slot {cv % slots} holding {landed[cv % slots]}")
+            if j > 0 and done["PV"] < j - 1:
+                errors.append(f"warp {w} wrote V^T_{j} while P V({j - 1}) still read V^T_{j - 1}")
+            if vt[0] is None or vt[0][0] != j:
+                vt[0] = (j, 0)
+            vt[0] = (j, vt[0][1] + 1)
+            if j + 1 < n:
+                ck = 2 * j + 2
+                yield from wait(full[ck % slots], (ck // slots) & 1, f"warp {w} K", ck // slots)
+                if landed[ck % slots] != ck:
+                    errors.append(f"warp {w} split K_{j + 1} from slot {ck % slots} holding {landed[ck % slots]}")
+                if done["S"] < j:
+                    errors.append(f"warp {w} rewrote the K low parts while S({j}) still read them")
+                split_k(w, ck)
+            if j > 0 and rng.random() < 0.3 and done["PV"] < j - 1:
+                errors.append(f"warp {w} rescaled O while P V({j - 1}) was pending")
+            p_ready.arrive()
+            if not vt_wait_s and j + 1 < n:
+                # planted: the next V^T as soon as V_{j+1} lands, without waiting for S_{j+1}
+                cv2 = 2 * j + 3
+                yield from wait(full[cv2 % slots], (cv2 // slots) & 1, f"warp {w} V early")
+                if done["PV"] < j:
+                    errors.append(f"warp {w} wrote V^T_{j + 1} while P V({j}) still read V^T_{j}")
+        yield from wait(o_final, 0, f"warp {w} epilogue", 0)
+
+    roles = [tensor_core(), producer(), issuer()] + [warp(w) for w in range(WARPS)]
+    waiting, finished = {}, set()
+    for i in range(len(roles)):
+        heapq.heappush(events, (0.0, rng.random(), ("run", i)))
+    horizon = 20000.0 * (n + 4)
+    while events and clock[0] < horizon:
+        clock[0], _, (what, arg) = heapq.heappop(events)
+        if what == "call":
+            arg()
+            continue
+        r = arg
+        if r in finished:
+            continue
+        try:
+            y = waiting.pop(r) if r in waiting else next(roles[r])
+            while True:
+                if y[0] == "delay":
+                    heapq.heappush(events, (clock[0] + y[1], rng.random(), ("run", r)))
+                    break
+                if y[1]():
+                    y = next(roles[r])
+                    continue
+                waiting[r] = y
+                heapq.heappush(events, (clock[0] + rng.uniform(20, 200), rng.random(), ("run", r)))
+                break
+        except StopIteration:
+            finished.add(r)
+        if finished == set(range(1, len(roles))) and not pipe:
+            break
+    if finished != set(range(1, len(roles))):
+        errors.append(f"deadlock: roles {sorted(set(range(1, len(roles))) - finished)} never finished")
+    return errors
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 5, 10])
+@pytest.mark.parametrize("warp_cycles", [(300, 1500), (100, 5000)])
+def test_tf32_forward_protocol_holds(n, warp_cycles):
+    for seed in range(15):
+        errs = simulate_tf32(n, seed, warp_cycles=warp_cycles)
+        assert not errs, (n, seed, errs[:3])
+
+
+def test_tf32_vt_rewrite_must_wait_for_s():
+    assert sum(bool(simulate_tf32(n, seed, warp_cycles=(100, 5000), vt_wait_s=False))
+               for n in (3, 5, 10) for seed in range(15)) > 0
+
+
+def test_tf32_issuer_must_wait_for_p_ready():
+    assert sum(bool(simulate_tf32(n, seed, warp_cycles=(100, 5000), issuer_waits_p=False))
+               for n in (3, 5, 10) for seed in range(15)) > 0
