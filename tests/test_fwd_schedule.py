@@ -231,13 +231,15 @@ def simulate(nkv, seed, *, slots=SLOTS, watcher_first_wait=True, last_tile_rule=
     return errors
 
 
-# causal pairs see n or n+1 key tiles per tile; an odd tail has no second tile
-CASES = [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (7, 7), (11, 12), (6, 0)]
+# causal pairs see n or n+1 key tiles per tile; an odd tail has no second tile;
+# block-sparse lists give the first tile any prefix of the second's list
+# (0 included) and the ring one slot fewer
+CASES = [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (7, 7), (11, 12), (6, 0), (0, 3), (2, 5), (1, 7), (0, 0)]
 
 
 @pytest.mark.parametrize("nkv", CASES)
 @pytest.mark.parametrize("softmax_cycles", [(300, 1500), (100, 5000)])
-@pytest.mark.parametrize("slots", [SLOTS, 12])
+@pytest.mark.parametrize("slots", [SLOTS - 1, SLOTS, 12])
 def test_forward_protocol_holds(nkv, softmax_cycles, slots):
     for seed in range(15):
         errs = simulate(nkv, seed, slots=slots, softmax_cycles=softmax_cycles)
