@@ -150,14 +150,18 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
  * [B, Hkv, N, d] with k_scale [B, Hkv, ceil(N/64)], vt codes [B, Hkv, d, NP]
  * with v_scale [B, Hkv, d] (as the two calls above write them); o bf16
  * [B, Hq, N, d], lse fp32 [B, Hq, N]. The products run on e4m3 tensor cores
- * with fp32 accumulation; the probabilities P (relative to a running row max
- * that may trail the true one by up to a factor 2^4, so P <= 2^4) are
- * multiplied by 2^4 and rounded to e4m3 before the P V product, while the
- * row sum and the LSE use the unrounded values. With P_ij = exp(s_ij - max_j
- * s_ij) and l_i = sum_j P_ij, the result differs from the exact attention of
- * the dequantised inputs by at most 2^-4 sum_j (P_ij / l_i)|V_jc| +
- * 2^-14 sum_j |V_jc| / l_i per element (visible keys j), plus the bf16
- * rounding of O. FA_ERR_UNSUPPORTED for d not a multiple of 16. */
+ * with fp32 accumulation. Contract on the probabilities: each P_ij is taken
+ * relative to a reference no larger than the row's true running maximum
+ * (this build lets it trail by up to a factor 2^4), scaled by a power of two
+ * >= 1 (this build: 2^4) and rounded to the nearest e4m3 value below 448
+ * before the P V product; the row sum and the LSE use the unrounded values.
+ * With P_ij = exp(s_ij - max_j s_ij) and l_i = sum_j P_ij, the result then
+ * differs from the exact attention of the dequantised inputs by at most
+ * 2^-4 sum_j (P_ij / l_i)|V_jc| + 2^-10 sum_j |V_jc| / l_i per element
+ * (visible keys j; e4m3's relative and subnormal rounding), plus the bf16
+ * rounding of O, and the errors are unbiased to first order (round to
+ * nearest). The tests also hold the mean error to its expectation under
+ * independent roundings. FA_ERR_UNSUPPORTED for d not a multiple of 16. */
 fa_status fa_fwd_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* vt,
                      const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
                      float scale, void* stream);

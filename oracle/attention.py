@@ -11,8 +11,9 @@ Query head h reads key/value head h // G (grouped-query attention; the
 Llama-2-70B-shaped workload maps 64 query heads onto 8 KV heads this way).
 
 Causal convention: key j is visible to query i iff j <= i (the pages skip the
-blocks whose key index exceeds the query index). `forward`, `backward` and
-`forward_rows` also take keys of another length Nk than the Nq queries
+blocks whose key index exceeds the query index). Every function but
+`backward_query_rows` and `tiled_forward` also takes keys of another length Nk
+than the Nq queries
 (k, v: [B, Hkv, Nk, d]); the queries are then the last Nq positions of the Nk
 (bottom-right alignment): key j is visible to query i iff j <= i + (Nk - Nq),
 so with Nq > Nk the first Nq - Nk query rows see no key.
@@ -185,17 +186,49 @@ def forward_rows(q, k, v, causal, scale, rows, block_mask=None):
     return o, lse
 
 
-def row_statistics(q, k, v, do, causal, scale, block=1024, threads=None):
+def _slab_keys(rows, Nk, causal, off, bm_bh):
+    """Keys that at least one of the given query rows may see: under the
+    causal rule none past (last row + off); under a block mask only the key
+    tiles some row's query tile may see. Every other key is masked for every
+    row of the slab (exp(-inf) = 0), so leaving it out changes no result."""
+    keys = np.arange(Nk)
+    if causal:
+        keys = keys[keys <= rows[-1] + off]
+    if bm_bh is not None:
+        tiles = np.asarray(bm_bh, dtype=bool)[np.unique(rows // BLOCK)].any(axis=0)
+        keys = keys[tiles[keys // BLOCK]]
+    return keys
+
+
+def _scores_on(qh, kh, scale, causal, row_index, key_index, block_mask_bh=None, off=0):
+    """As _scores, for the keys `key_index` only (absolute indices into kh)."""
+    s = scale * (qh @ kh[key_index].T)
+    if causal:
+        s = np.where(key_index[None, :] <= row_index[:, None] + off, s, -np.inf)
+    if block_mask_bh is not None:
+        allowed = np.asarray(block_mask_bh, dtype=bool)[row_index[:, None] // BLOCK, key_index[None, :] // BLOCK]
+        s = np.where(allowed, s, -np.inf)
+    return s
+
+
+def row_statistics(q, k, v, do, causal, scale, block=1024, threads=None, block_mask=None):
     """LSE_i and D_i = dO_i . O_i for EVERY query row, in double.
 
     Needed to check sampled key rows of dK/dV at lengths where the full score
     matrix does not fit: a key row's gradient sums over all query rows that
     see it, each weighted by that row's own LSE and D. The values come from
     this oracle alone, never from the GPU. Whole rows are computed together in
-    batches of `block`; no row is split.
+    batches of `block`; no row is split. Keys may be longer than queries
+    (k, v: [B, Hkv, Nk, d]; bottom-right causal rule, as in `forward`), and
+    block_mask is as in `forward` (Nq == Nk). A row that sees no key has
+    LSE = -inf and D = 0 (its O is 0).
     Returns (lse [B,Hq,N], D [B,Hq,N]).
     """
-    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    B, Hq, Hkv, N, Nk, d, G = _check_qk(q, k, v)
+    if block_mask is not None and Nk != N:
+        raise ValueError("block masks need Nq == Nk")
+    bm = _block_mask_bh(block_mask, B, Hq, N)
+    off = Nk - N
     lse = np.empty((B, Hq, N))
     D = np.empty((B, Hq, N))
     jobs = [(b, h, r0) for b in range(B) for h in range(Hq) for r0 in range(0, N, block)]
@@ -204,10 +237,15 @@ def row_statistics(q, k, v, do, causal, scale, block=1024, threads=None):
         b, h, r0 = job
         hk = h // G
         r = np.arange(r0, min(r0 + block, N))
-        kmax = (r[-1] + 1) if causal else N      # keys past the last row are all masked
-        s = _scores(q[b, h, r], k[b, hk, :kmax], scale, causal, r)
+        bmh = None if bm is None else bm[b, h]
+        keys = _slab_keys(r, Nk, causal, off, bmh)
+        if keys.size == 0:
+            lse[b, h, r] = -np.inf
+            D[b, h, r] = 0.0
+            return
+        s = _scores_on(q[b, h, r], k[b, hk], scale, causal, r, keys, bmh, off)
         p, lse_r = _softmax_rows(s)
-        o_r = p @ v[b, hk, :kmax]
+        o_r = p @ v[b, hk, keys]
         lse[b, h, r] = lse_r
         D[b, h, r] = (do[b, h, r] * o_r).sum(axis=1)
 
@@ -216,7 +254,7 @@ def row_statistics(q, k, v, do, causal, scale, block=1024, threads=None):
     return lse, D
 
 
-def backward_rows(q, k, v, do, causal, scale, q_rows, k_rows, lse, D):
+def backward_rows(q, k, v, do, causal, scale, q_rows, k_rows, lse, D, block_mask=None):
     """dQ for selected query rows and dK, dV for selected key rows.
 
     q_rows: [B, Hq, R] query indices; k_rows: [B, Hkv, R2] key indices.
@@ -225,29 +263,40 @@ def backward_rows(q, k, v, do, causal, scale, q_rows, k_rows, lse, D):
         dQ_i = scale sum_j P_ij (dP_ij - D_i) K_j
         dK_j = scale sum_{h in group} sum_i P_ij (dP_ij - D_i) Q_i
         dV_j = sum_{h in group} sum_i P_ij dO_i
-    with P_ij = exp(S_ij - LSE_i) and dP_ij = dO_i . V_j (see `backward`).
+    with P_ij = exp(S_ij - LSE_i) over the visible (i, j) and 0 elsewhere, and
+    dP_ij = dO_i . V_j (see `backward`). Keys may be longer than queries
+    (bottom-right causal rule) and block_mask is as in `forward`; a query row
+    that sees no key (LSE = -inf) has dQ = 0 and adds nothing to dK, dV.
     Returns (dq [B,Hq,R,d], dk [B,Hkv,R2,d], dv [B,Hkv,R2,d]).
     """
-    B, Hq, Hkv, N, d, G = _check(q, k, v)
+    B, Hq, Hkv, N, Nk, d, G = _check_qk(q, k, v)
+    if block_mask is not None and Nk != N:
+        raise ValueError("block masks need Nq == Nk")
+    bm = _block_mask_bh(block_mask, B, Hq, N)
+    off = Nk - N
     all_rows = np.arange(N)
     dq = np.empty((B, Hq, q_rows.shape[2], d))
     dk = np.zeros((B, Hkv, k_rows.shape[2], d))
     dv = np.zeros((B, Hkv, k_rows.shape[2], d))
+
+    def probs(s, lse_rows):
+        seen = np.isfinite(lse_rows)
+        return np.where(seen[:, None], np.exp(s - np.where(seen, lse_rows, 0.0)[:, None]), 0.0)
+
     for b in range(B):
         for h in range(Hq):
             hk = h // G
+            bmh = None if bm is None else bm[b, h]
             r = q_rows[b, h]
-            s = _scores(q[b, h, r], k[b, hk], scale, causal, r)
-            p = np.exp(s - lse[b, h, r][:, None])
+            s = _scores(q[b, h, r], k[b, hk], scale, causal, r, bmh, off)
+            p = probs(s, lse[b, h, r])
             dp = do[b, h, r] @ v[b, hk].T
             dq[b, h] = scale * ((p * (dp - D[b, h, r][:, None])) @ k[b, hk])
 
             c = k_rows[b, hk]
             # scores of every query row against the selected keys: [N, R2]
-            st = scale * (q[b, h] @ k[b, hk, c].T)
-            if causal:
-                st = np.where(c[None, :] <= all_rows[:, None], st, -np.inf)
-            pt = np.exp(st - lse[b, h][:, None])
+            st = _scores_on(q[b, h], k[b, hk], scale, causal, all_rows, c, bmh, off)
+            pt = probs(st, lse[b, h])
             dpt = do[b, h] @ v[b, hk, c].T
             dst = pt * (dpt - D[b, h][:, None])
             dk[b, hk] += scale * (dst.T @ q[b, h])

@@ -74,8 +74,9 @@ def test_kvlen_equal_lengths_match_fa_fwd(fa):
 def test_kvlen_chunked_prefill_workload_sampled_rows(fa):
     """The unequal-length bench workload at full size (GQA 32/8 heads, 4096
     queries at the end of 32768 keys, causal): 256 seeded query rows per head
-    of the forward against the oracle, and two backward launches giving
-    bit-identical dK, dV and finite, bounded gradients."""
+    of O, LSE and dQ, and 256 seeded key rows per KV head of dK and dV,
+    against the oracle (which computes LSE and D of every query row itself);
+    two backward launches give bit-identical dK and dV."""
     w = configs.WORKLOADS["bf16_gqa_h32kv8_nq4096_nk32768_d128_causal_fwdbwd"]
     t = inputs.make_workload_inputs(w)
     dev = torch.device("cuda:0")
@@ -84,17 +85,25 @@ def test_kvlen_chunked_prefill_workload_sampled_rows(fa):
     a = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=w.scale)
     b = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=w.scale)
     fa.check_device_status()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     rows = inputs.sample_rows(w.B, w.Hq, w.N, 256, seed=1)
-    f = {n: inputs.to_f64(t[n]) for n in ("q", "k", "v")}
+    krows = inputs.sample_rows(w.B, w.Hkv, w.Nk, 256, seed=2)
+    f = {n: inputs.to_f64(t[n]) for n in ("q", "k", "v", "do")}
     ro, rl = oracle.forward_rows(f["q"], f["k"], f["v"], True, w.scale, rows)
     bi = np.arange(w.B)[:, None, None]
     hi = np.arange(w.Hq)[None, :, None]
+    hk = np.arange(w.Hkv)[None, :, None]
     og = o.float().cpu().numpy()[bi, hi, rows]
     lg = lse.cpu().numpy()[bi, hi, rows]
     err = np.abs(og - ro)
     assert err.max() <= configs.TOL_O_MAX and err.mean() <= configs.TOL_O_MEAN
     assert np.abs(lg - rl).max() <= configs.TOL_LSE_MAX
-    for x in a:
-        xf = x.float()
-        assert bool(torch.isfinite(xf).all()) and float(xf.abs().max()) < 1e3
-    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    rl_all, rD_all = oracle.row_statistics(f["q"], f["k"], f["v"], f["do"], True, w.scale)
+    assert np.abs(lse.cpu().numpy() - rl_all).max() <= configs.TOL_LSE_MAX
+    rdq, rdk, rdv = oracle.backward_rows(f["q"], f["k"], f["v"], f["do"], True, w.scale, rows, krows, rl_all, rD_all)
+    dq, dk, dv = (x.float().cpu().numpy() for x in a)
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+    errs = {"dq": rel_fro(dq[bi, hi, rows], rdq), "dk": rel_fro(dk[bi, hk, krows], rdk),
+            "dv": rel_fro(dv[bi, hk, krows], rdv)}
+    print(w.name, errs)
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs

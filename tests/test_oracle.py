@@ -552,3 +552,67 @@ def test_kv_length_rows_mode_matches_full():
     for h in range(2):
         np.testing.assert_array_equal(ro[0, h], o[0, h, rows[0, h]])
         np.testing.assert_array_equal(rl[0, h], lse[0, h, rows[0, h]])
+
+
+# ---------------------------------------------------------------- row modes with Nq != Nk and block masks
+@pytest.mark.parametrize("Nq,Nk,causal", [(150, 400, True), (300, 130, True), (1, 257, True), (120, 333, False)])
+def test_kv_length_row_statistics_and_backward_rows_match_full(Nq, Nk, causal):
+    """The sampled-row modes with keys longer (or shorter) than queries equal
+    the full `backward`, itself pinned against torch above; rows that see no
+    key (Nq > Nk, causal) have LSE = -inf, D = 0 and dQ = 0."""
+    B, Hq, Hkv, d = 1, 4, 2, 8
+    rng = np.random.default_rng(Nq * 31 + Nk)
+    q = rng.standard_normal((B, Hq, Nq, d))
+    k = rng.standard_normal((B, Hkv, Nk, d))
+    v = rng.standard_normal((B, Hkv, Nk, d))
+    do = rng.standard_normal((B, Hq, Nq, d))
+    o, lse, dq, dk, dv = oa.backward(q, k, v, do, causal, 0.35)
+    lse_s, D_s = oa.row_statistics(q, k, v, do, causal, 0.35, block=64, threads=2)
+    seen = np.isfinite(lse)
+    assert np.array_equal(np.isfinite(lse_s), seen)
+    np.testing.assert_allclose(lse_s[seen], lse[seen], atol=1e-13)
+    np.testing.assert_allclose(D_s, (do * o).sum(-1), atol=1e-13)
+    assert np.all(D_s[~seen] == 0)
+    qr = np.stack([np.stack([np.sort(rng.choice(Nq, min(Nq, 9), replace=False)) for _ in range(Hq)])])
+    kr = np.stack([np.stack([np.sort(rng.choice(Nk, 11, replace=False)) for _ in range(Hkv)])])
+    if Nq > Nk and causal:
+        qr[0, 0, 0] = 0                        # a row that sees no key
+    dq_r, dk_r, dv_r = oa.backward_rows(q, k, v, do, causal, 0.35, qr, kr, lse_s, D_s)
+    for h in range(Hq):
+        np.testing.assert_allclose(dq_r[0, h], dq[0, h, qr[0, h]], atol=1e-12)
+    for g in range(Hkv):
+        np.testing.assert_allclose(dk_r[0, g], dk[0, g, kr[0, g]], atol=1e-12)
+        np.testing.assert_allclose(dv_r[0, g], dv[0, g, kr[0, g]], atol=1e-12)
+    if Nq > Nk and causal:
+        assert np.all(dq_r[0, 0, 0] == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_row_statistics_and_backward_rows_match_full(causal):
+    """The same for a block mask (pinned against torch above), including a
+    query tile that sees no key tile and a local-window mask whose slabs span
+    several tiles."""
+    B, Hq, Hkv, N, d = 1, 4, 2, 520, 8
+    q, k, v, do = rand_qkv(B, Hq, Hkv, N, d, seed=61, with_do=True)
+    T = 5
+    bm = _block_mask(B, Hq, T, 0.6, seed=62)
+    bm[:, 1, 2, :] = False                     # head 1, query tile 2 sees nothing
+    i, j = np.arange(T)[:, None], np.arange(T)[None, :]
+    bm[:, 3] = (j <= i) & (j > i - 2)          # head 3: a window of two tiles
+    o, lse, dq, dk, dv = oa.backward(q, k, v, do, causal, 0.3, block_mask=bm)
+    lse_s, D_s = oa.row_statistics(q, k, v, do, causal, 0.3, block=200, threads=2, block_mask=bm)
+    seen = np.isfinite(lse)
+    assert (~seen).any() and np.array_equal(np.isfinite(lse_s), seen)
+    np.testing.assert_allclose(lse_s[seen], lse[seen], atol=1e-13)
+    np.testing.assert_allclose(D_s, (do * o).sum(-1), atol=1e-13)
+    rng = np.random.default_rng(63)
+    qr = np.stack([np.stack([np.sort(rng.choice(N, 12, replace=False)) for _ in range(Hq)])])
+    qr[0, 1, 0] = 300                          # head 1, inside the empty query tile
+    qr[0, 1] = np.sort(qr[0, 1])
+    kr = np.stack([np.stack([np.sort(rng.choice(N, 14, replace=False)) for _ in range(Hkv)])])
+    dq_r, dk_r, dv_r = oa.backward_rows(q, k, v, do, causal, 0.3, qr, kr, lse_s, D_s, block_mask=bm)
+    for h in range(Hq):
+        np.testing.assert_allclose(dq_r[0, h], dq[0, h, qr[0, h]], atol=1e-12)
+    for g in range(Hkv):
+        np.testing.assert_allclose(dk_r[0, g], dk[0, g, kr[0, g]], atol=1e-12)
+        np.testing.assert_allclose(dv_r[0, g], dv[0, g, kr[0, g]], atol=1e-12)

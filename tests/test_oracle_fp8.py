@@ -135,31 +135,71 @@ def test_forward_fp8_is_dense_oracle_of_dequantised_inputs():
     assert np.abs(o - o3).mean() < 0.05
 
 
+def _emulate_rounded_p(q, k, v, causal, scale, pow2, max_lag, seed):
+    """Attention with P rounded the way any admissible kernel may round it:
+    P' = exp(s - m') relative to a reference m' that trails the row's true
+    max by a random t in [0, max_lag] (log2 units, a different t per row),
+    multiplied by 2^pow2, rounded to e4m3, divided back, and normalised by the
+    unrounded sum; then the bf16 rounding of the result."""
+    rng = np.random.default_rng(seed)
+    N = q.shape[2]
+    s = (q[0, 0] @ k[0, 0].T) * scale
+    if causal:
+        s = np.where(np.arange(k.shape[2])[None, :] <= np.arange(N)[:, None] + (k.shape[2] - N), s, -np.inf)
+    lag = rng.uniform(0, max_lag, (N, 1)) * np.log(2.0)
+    p_stale = np.exp(s - s.max(axis=1, keepdims=True) + lag)
+    assert (p_stale * 2.0 ** pow2).max() < 448
+    p_r = fp8.e4m3_decode(fp8.e4m3_encode((p_stale * 2.0 ** pow2).astype(np.float32))) / 2.0 ** pow2
+    o = (p_r @ v[0, 0]) / p_stale.sum(axis=1, keepdims=True)
+    return torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+
+
 @pytest.mark.parametrize("causal", [False, True])
-def test_p_rounding_bound_covers_rounded_probabilities(causal):
-    """Emulate the kernel's approximation directly: round P' * 2^4 to e4m3,
-    where P' is relative to a running max that trails the true one by a
-    random amount up to 2^4 per row (the kernel's lazy rescale), keep l
-    unrounded, and check the result stays within the bound."""
-    rng = np.random.default_rng(10 + causal)
-    N, d = 300, 128
-    q = rng.normal(0, 1, (1, 1, N, d)) * 2.0
+@pytest.mark.parametrize("pow2,max_lag,q_mult", [(0, 0.0, 1.0), (4, 4.0, 1.0), (8, 0.5, 2.0), (2, 6.0, 4.0)])
+def test_p_rounding_bound_covers_rounded_probabilities(causal, pow2, max_lag, q_mult):
+    """The per-element bound holds, and the mean error stays within the
+    expected-error bound with the bias coefficient near 0, for every
+    admissible choice of scaling and reference lag (emulated directly); an
+    output scaled by 1.03 breaks the mean or the bias gate."""
+    rng = np.random.default_rng(10 + causal + pow2)
+    N, d = 400, 128
+    q = rng.normal(0, 1, (1, 1, N, d)) * q_mult
     k = rng.normal(0, 1, (1, 1, N, d))
     v = rng.normal(0, 1, (1, 1, N, d))
     scale = d ** -0.5
     o, _ = oracle.forward(q, k, v, causal, scale)
-    s = (q[0, 0] @ k[0, 0].T) * scale
-    if causal:
-        s = np.where(np.tril(np.ones((N, N), bool)), s, -np.inf)
-    lag = rng.uniform(0, 4, (N, 1)) * np.log(2.0)               # m - m' in natural-log units
-    p_stale = np.exp(s - s.max(axis=1, keepdims=True) + lag)   # P' <= 2^4
-    l = p_stale.sum(axis=1, keepdims=True)
-    p_r = fp8.e4m3_decode(fp8.e4m3_encode((p_stale * fp8.P_SCALE).astype(np.float32))) / fp8.P_SCALE
-    o_emul = (p_r @ v[0, 0]) / l
+    o_emul = _emulate_rounded_p(q, k, v, causal, scale, pow2, max_lag, seed=pow2)
+    err = o_emul - o[0, 0]
     bound = fp8.p_rounding_bound(q, k, v, causal, scale, o)[0, 0]
-    assert (np.abs(o_emul - o[0, 0]) <= bound).all()
-    assert np.abs(o_emul - o[0, 0]).max() > 1e-4            # the rounding is visible, so the check bites
+    expected = fp8.p_rounding_expected(q, k, v, causal, scale, o)[0, 0]
+    assert (np.abs(err) <= bound).all()
+    assert np.abs(err).max() > 1e-4                   # the rounding is visible, so the check bites
+    assert np.abs(err).mean() <= expected.mean()
+    assert np.abs(err).mean() >= 0.2 * expected.mean()   # and the expectation is not vacuous
+    assert abs(fp8.error_bias(err, o[0, 0])) <= fp8.BIAS_MAX
+    bad = o_emul * 1.03 - o[0, 0]
+    assert np.abs(bad).mean() > expected.mean() or abs(fp8.error_bias(bad, o[0, 0])) > fp8.BIAS_MAX
     # and the bound of a subset of rows is the same as the full one there
-    rows = np.array([[[0, 7, 150, 299]]])
+    rows = np.array([[[0, 7, 150, 399]]])
     sub = fp8.p_rounding_bound(q, k, v, causal, scale, o[:, :, rows[0, 0]], rows=rows)
     assert np.allclose(sub[0, 0], bound[rows[0, 0]], rtol=1e-12, atol=0)
+    sub_e = fp8.p_rounding_expected(q, k, v, causal, scale, o[:, :, rows[0, 0]], rows=rows)
+    assert np.allclose(sub_e[0, 0], expected[rows[0, 0]], rtol=1e-12, atol=0)
+
+
+def test_p_rounding_bound_breaks_on_a_planted_mistake():
+    """Rounding P to 2 fraction bits instead of 3 (one bit lost) exceeds the
+    per-element bound somewhere: the bound is tight enough to see it."""
+    rng = np.random.default_rng(5)
+    N, d = 400, 128
+    q, k, v = (rng.normal(0, 1, (1, 1, N, d)) for _ in range(3))
+    scale = d ** -0.5
+    o, _ = oracle.forward(q, k, v, False, scale)
+    s = (q[0, 0] @ k[0, 0].T) * scale
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    m, e = np.frexp(p)
+    p2 = np.ldexp(np.round(m * 8) / 8, e)               # 3 significant bits: 2 fraction bits
+    o_bad = (p2 @ v[0, 0]) / p.sum(axis=1, keepdims=True)
+    bound = fp8.p_rounding_bound(q, k, v, False, scale, o)[0, 0]
+    expected = fp8.p_rounding_expected(q, k, v, False, scale, o)[0, 0]
+    assert (np.abs(o_bad - o[0, 0]) > bound).any() or np.abs(o_bad - o[0, 0]).mean() > expected.mean()
