@@ -13,8 +13,12 @@
 
 namespace {
 
-// Set by kernels whose bounded waits ran out; read and cleared by fa_device_status.
-__device__ unsigned g_status_word;
+// Status words set by kernels whose bounded waits ran out, one per stream:
+// a call launched on a stream reports to that stream's word, which
+// fa_device_status(stream) reads and clears. Slot 0 is shared by the streams
+// beyond the first kStatusSlots - 1 that a device sees.
+constexpr int kStatusSlots = 256;
+__device__ unsigned g_status_words[kStatusSlots];
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -38,13 +42,29 @@ struct DeviceState {
   std::once_flag once;
   bool arch_ok = false;
   int num_sms = 0;
-  unsigned* status = nullptr;
+  unsigned* status = nullptr;           // device address of g_status_words on this device
+  std::mutex mu;                        // guards the stream -> slot table below
+  const void* owner[kStatusSlots] = {}; // owner[i]: the stream whose calls report to slot i (i >= 1)
+  int used = 1;
 };
 DeviceState g_dev[kMaxDevices];
 
-// Checks the current device once (compute capability 10.3) and resolves the
-// device address of the status word on it.
-fa_status device_state(unsigned** status_out, int* num_sms = nullptr) {
+// The status word of `stream` on this device: the slot the stream was given
+// the first time it was seen, or the shared slot 0 once the table is full.
+unsigned* stream_slot(DeviceState& s, const void* stream) {
+  std::lock_guard<std::mutex> lock(s.mu);
+  for (int i = 1; i < s.used; ++i)
+    if (s.owner[i] == stream) return s.status + i;
+  if (s.used < kStatusSlots) {
+    s.owner[s.used] = stream;
+    return s.status + s.used++;
+  }
+  return s.status;
+}
+
+// Checks the current device once (compute capability 10.3), resolves the
+// device address of the status words on it and returns the word of `stream`.
+fa_status device_state(const void* stream, unsigned** status_out, int* num_sms = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
@@ -56,11 +76,11 @@ fa_status device_state(unsigned** status_out, int* num_sms = nullptr) {
     s.arch_ok = (major == 10 && minor == 3);
     if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) s.num_sms = 0;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) s.status = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_status_words) == cudaSuccess) s.status = static_cast<unsigned*>(p);
   });
   if (!s.arch_ok) return FA_ERR_ARCH;
   if (!s.status || s.num_sms <= 0) return FA_ERR_CUDA;
-  *status_out = s.status;
+  *status_out = stream_slot(s, stream);
   if (num_sms) *num_sms = s.num_sms;
   return FA_OK;
 }
@@ -146,7 +166,7 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   const bool wide = d > 128;                // one query tile per CTA, V in 64-key halves
   if (wide && mask) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
-  st = device_state(&status);
+  st = device_state(stream, &status);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
@@ -201,7 +221,7 @@ BwdWorkspace bwd_workspace(int B, int Hq, int Hkv, int N, int d) {
 // Validates sizes and workspace, resolves the device, fills BwdParams. With
 // lse_d_only the workspace only has to hold the LSE and D parts.
 fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
-                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms, bool lse_d_only = false,
+                    size_t workspace_bytes, fa::BwdParams* p, int* num_sms, void* stream, bool lse_d_only = false,
                     const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0,
                     int Nk = -1) {
   if (Nk < 0) Nk = N;
@@ -215,7 +235,7 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
       workspace_bytes < (mask ? w.total_sparse : (lse_d_only ? w.off_dq : w.total)))
     return FA_ERR_WORKSPACE;
   unsigned* status = nullptr;
-  st = device_state(&status, num_sms);
+  st = device_state(stream, &status, num_sms);
   if (st != FA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p->ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
@@ -271,7 +291,7 @@ fa_status fa_bwd_blocksparse(const void* q, const void* k, const void* v, const 
   if ((N + 127) / 128 > fa::kMaskMaxTiles) return FA_ERR_UNSUPPORTED;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, false,
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, stream, false,
                            block_mask, mask_stride_b, mask_stride_h);
   if (st != FA_OK) return st;
   fa::BwdMaps m;
@@ -293,7 +313,7 @@ fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, voi
   if (!o || !lse || !dO || !aligned16(o) || !aligned16(lse) || !aligned16(dO)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, 1.0f, workspace, workspace_bytes, &p, &num_sms);
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, 1.0f, workspace, workspace_bytes, &p, &num_sms, stream);
   if (st != FA_OK) return st;
   const cudaError_t e = fa::launch_bwd_pre(d, o, dO, lse, p, num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -310,7 +330,7 @@ fa_status bwd_dkdv_common(const void* q, const void* k, const void* v, const voi
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, false,
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, stream, false,
                            nullptr, 0, 0, Nk);
   if (st != FA_OK) return st;
   fa::BwdMaps m;
@@ -339,7 +359,7 @@ fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, in
   if (!dq || !aligned16(dq)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, scale, workspace, workspace_bytes, &p, &num_sms);
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, 0, scale, workspace, workspace_bytes, &p, &num_sms, stream);
   if (st != FA_OK) return st;
   const cudaError_t e = fa::launch_bwd_dq(d, dq, p, num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -380,7 +400,7 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p{};
   int num_sms = 0;
-  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, true);
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, stream, true);
   if (st != FA_OK) return st;
   fa::BwdMaps m;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
@@ -428,7 +448,7 @@ fa_status fa_fp8_quantize_rows(const void* x, void* out, float* scales, int BH, 
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
-  const fa_status st = device_state(&status);
+  const fa_status st = device_state(stream, &status);
   if (st != FA_OK) return st;
   return fa::launch_fp8_quant_rows(x, out, scales, BH, N, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK : FA_ERR_CUDA;
@@ -439,7 +459,7 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
   if (BH < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
-  const fa_status st = device_state(&status);
+  const fa_status st = device_state(stream, &status);
   if (st != FA_OK) return st;
   return fa::launch_fp8_quant_v(v, vt, scales, BH, N, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK : FA_ERR_CUDA;
@@ -459,7 +479,7 @@ fa_status fwd_fp8_common(const void* q, const float* q_scale, const void* k, con
   if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
   if (!fp8_dim(d)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
-  st = device_state(&status);
+  st = device_state(stream, &status);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mvt, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
@@ -508,7 +528,7 @@ fa_status fa_ex2_throughput(double* per_sm_per_cycle, void* stream) {
   if (!per_sm_per_cycle) return FA_ERR_INVALID_ARG;
   unsigned* status = nullptr;
   int num_sms = 0;
-  const fa_status st = device_state(&status, &num_sms);
+  const fa_status st = device_state(stream, &status, &num_sms);
   if (st != FA_OK) return st;
   if (num_sms > fa::kEx2MaxSms) return FA_ERR_UNSUPPORTED;
   return fa::measure_ex2_rate(num_sms, 4096, per_sm_per_cycle, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -517,15 +537,17 @@ fa_status fa_ex2_throughput(double* per_sm_per_cycle, void* stream) {
 
 fa_status fa_device_status(void* stream) {
   unsigned* status = nullptr;
-  fa_status st = device_state(&status);
+  fa_status st = device_state(stream, &status);
   if (st != FA_OK) return st;
+  // read and clear this stream's word in the stream's own order: work on
+  // other streams is neither waited for nor reported here
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
   unsigned host = 0;
-  if (cudaMemcpyFromSymbol(&host, g_status_word, sizeof(host)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyAsync(&host, status, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
   if (host != 0) {
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
     return (host & 1u) ? FA_ERR_TIMEOUT : FA_ERR_DEVICE;
   }
   return FA_OK;

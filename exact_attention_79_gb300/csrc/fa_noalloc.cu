@@ -27,22 +27,27 @@ __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 struct ScratchSlot {
-  std::once_flag once;
-  cudaError_t rc = cudaErrorUnknown;
-  void* ptr = nullptr;
+  std::mutex mu;
+  void* ptr = nullptr;     // set once a lookup on this device has succeeded
 };
 ScratchSlot g_slots[kMaxDevices];
 
 // Device address of the array on the current device. In host code the
 // array's name only stands in for it; the real address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up with that device current. Only a
+// successful lookup is kept: a failed one (for example during stream
+// capture, where the lookup may not run) is retried on the next call.
 fa_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   ScratchSlot& s = g_slots[dev];
-  std::call_once(s.once, [&s] { s.rc = cudaGetSymbolAddress(&s.ptr, g_bwd_scratch); });
-  if (s.rc != cudaSuccess || s.ptr == nullptr) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    s.ptr = p;
+  }
   *out = s.ptr;
   return FA_OK;
 }

@@ -43,14 +43,16 @@
  *     is not sm_103, FA_ERR_CUDA when a launch fails. Inside the kernels every
  *     wait is bounded (2 s, or FA_WAIT_LIMIT_MS milliseconds from the
  *     environment, read once per process); a wait that runs out makes its
- *     block unwind, store nothing and set the device status word, which
- *     fa_device_status reports as FA_ERR_TIMEOUT; the context stays usable.
+ *     block unwind, store nothing and set the status word of the call's
+ *     stream, which fa_device_status reports as FA_ERR_TIMEOUT; the context
+ *     stays usable.
  *     FA_TEST_STALL=1 in the environment (read at every call) makes the
  *     tensor-core issuer of every fa_fwd* call (fa_fwd_fp8* included) and of
  *     fa_bwd's dK/dV pass wait on a barrier nothing arrives on, to exercise
  *     that path; unset in normal use.
  *   Threads: calls may come from several host threads; each call is
- *     independent.
+ *     independent, and device-side failures are reported per stream (see
+ *     fa_device_status).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -257,18 +259,24 @@ fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, in
  * Returns FA_ERR_WORKSPACE, launching nothing, when the problem needs more
  * than 32 MiB of scratch (fa_bwd_workspace_bytes > 33554432). The first call
  * on a device looks up the array's device address; make that first call
- * before any stream capture. Allocates nothing. All calls share the one
+ * before any stream capture. Only a successful lookup is kept: if it fails
+ * (FA_ERR_CUDA), the next call tries again. Allocates nothing. All calls share the one
  * array: calls whose work overlaps on the GPU (other streams, other host
  * threads on the same device) race and corrupt each other's results. */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                          int causal, float scale, void* stream);
 
-/* Synchronises `stream`, then returns and clears the device status word:
- * FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran out; that call's
- * outputs are invalid), FA_ERR_DEVICE (a kernel found the device's
+/* Synchronises `stream`, then returns and clears the status word of that
+ * stream: FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran out; that
+ * call's outputs are invalid), FA_ERR_DEVICE (a kernel found the device's
  * shared-memory window unusable and did nothing) or FA_ERR_CUDA (the stream
- * reported an error). */
+ * reported an error). Each stream handle has its own word on each device,
+ * set only by calls launched on that stream, so a failure on one stream is
+ * neither reported to nor cleared by a caller that asks about another. The
+ * first 255 stream handles a device sees get a word each; later ones share
+ * one word (and so do threads that all pass cudaStreamPerThread, one handle
+ * value). Calls on other streams are neither waited for nor reported. */
 fa_status fa_device_status(void* stream);
 
 /* Diagnostic: throughput of the exponential instruction the softmax uses

@@ -5,7 +5,8 @@ the backward's dK/dV pass) first waits on a barrier nothing arrives on, so its
 bounded wait (FA_WAIT_LIMIT_MS, here 300 ms) runs out; every other role of
 the block sees the abort flag and unwinds, the block stores nothing and the
 call reports FA_ERR_TIMEOUT through fa_device_status. The next call on the
-same context must be correct. Runs in a child process because the wait
+same context must be correct, and a stall on one stream must not be reported
+to a call on another.  Runs in a child process because the wait
 limit is read once per process."""
 import os
 import subprocess
@@ -78,6 +79,23 @@ for name, call in (("wide", lambda: fa.fwd(gw["q"], gw["k"], gw["v"], causal=Tru
     assert lib.fa_device_status(stream) == 0, name
     ref = refs[name]
     assert torch.equal(again[0], ref[0]) and torch.equal(again[1], ref[1]), name
+# status words are per stream: a stall on one stream is reported to that
+# stream only, while a call on another stream, overlapping it, reports FA_OK
+sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+ha, hb = ctypes.c_void_p(sa.cuda_stream), ctypes.c_void_p(sb.cuda_stream)
+torch.cuda.synchronize()
+os.environ["FA_TEST_STALL"] = "1"
+with torch.cuda.stream(sa):
+    fa.fwd(g["q"], g["k"], g["v"], causal=True)
+os.environ["FA_TEST_STALL"] = "0"
+with torch.cuda.stream(sb):
+    o_b, lse_b = fa.fwd(g["q"], g["k"], g["v"], causal=True)
+t0 = time.time()
+assert lib.fa_device_status(hb) == 0
+assert torch.equal(o_b, o_ok) and torch.equal(lse_b, lse_ok)
+assert lib.fa_device_status(ha) == 5
+assert lib.fa_device_status(ha) == 0             # read and cleared
+assert lib.fa_device_status(stream) == 0
 print("timeout-path-ok")
 '''
 
