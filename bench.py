@@ -99,23 +99,51 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, kernel_mhz=None):
+        """Clock record of the timed region. nvidia-smi samples every 50 ms,
+        so a short timed region holds few samples: its median SM clock is
+        reported only from samples inside the window (at least 3), else under
+        smi_sm_mhz_out_of_window. sm_mhz is the clock the timed kernels
+        measured themselves (fa_sm_clock_mhz) when available. Throttle
+        reasons are those seen in any sample of the run."""
         inside = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9]
-        rows = inside if len(inside) >= 3 else [r for _, r in self.rows if len(r) >= 9]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        every = [r for _, r in self.rows if len(r) >= 9]
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
-        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+
+        def median_sm(rows):
+            sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
+            return sm[len(sm) // 2] if sm else None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows), "in_window": len(inside)}
+        reasons = sorted({names[i] for r in every for i in range(4) if r[5 + i].lower().startswith("active")})
+        mx = [v for v in (num(r[2]) for r in every) if v is not None]
+        out = {"sm_max_mhz": max(mx) if mx else None, "reasons": reasons if every else ["unavailable"],
+               "samples": len(every), "in_window": len(inside)}
+        if len(inside) >= 3:
+            out["smi_sm_mhz_in_window"] = median_sm(inside)
+        else:
+            out["smi_sm_mhz_out_of_window"] = median_sm(every)
+        if kernel_mhz:
+            out["sm_mhz"] = kernel_mhz
+            out["sm_mhz_source"] = "timed kernels themselves (fa_sm_clock_mhz: SM cycles / ns over every CTA)"
+        else:
+            out["sm_mhz"] = out.get("smi_sm_mhz_in_window")
+            out["sm_mhz_source"] = "nvidia-smi samples inside the timed region" if out["sm_mhz"] else None
+        return out
+
+
+def clock_rated_peak(dtype, n_sms, mhz):
+    """Dense tensor rate at the given SM clock: 4096 bf16 multiply-adds per
+    SM per clock (8192 FLOP; measured for every MMA form the kernels use),
+    twice that for e4m3, half for tf32. TFLOP/s, or None without a clock."""
+    if not mhz:
+        return None
+    per_clk = {"fp8e4m3": 16384.0, "fp32": 4096.0}.get(dtype, 8192.0)
+    return n_sms * per_clk * mhz * 1e6 / 1e12
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -425,6 +453,7 @@ def native_arm(args, w):
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
     events = [new_events() for _ in range(args.steps)]
+    fa.sm_clock_mhz(stream.cuda_stream)          # reset the kernels' clock sums
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -436,6 +465,7 @@ def native_arm(args, w):
     if world > 1:
         dist.barrier()
     t1 = time.time()
+    kernel_mhz = fa.sm_clock_mhz(stream.cuda_stream)
     time.sleep(0.2)
     sampler.stop()
     fa.check_device_status(stream.cuda_stream)
@@ -538,8 +568,14 @@ def native_arm(args, w):
 
     if rank != 0:
         return
-    clocks = sampler.summary(t0, t1)
+    clocks = sampler.summary(t0, t1, kernel_mhz)
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rated = clock_rated_peak(w.dtype, n_sms, clocks.get("sm_mhz"))
+    if rated:
+        roofline["clock_rated_peak"] = rated
+        roofline["frac_of_clock_rated"] = roofline["achieved"] / rated
+        roofline["clock_rated_note"] = (f"{n_sms} SMs x dense tensor FLOP per SM clock x the SM clock the timed "
+                                        "kernels measured")
     line = {
         "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -551,6 +587,7 @@ def native_arm(args, w):
         "frac_of_peak": value / world / peak,
         "fwd_tflops": w.flops_fwd / (mean[0] / 1e3) / 1e12,
         "fwd_frac_of_peak": w.flops_fwd / (mean[0] / 1e3) / 1e12 / peak,
+        "fwd_frac_of_clock_rated": (w.flops_fwd / (mean[0] / 1e3) / 1e12 / rated) if rated else None,
         "bwd_tflops": None if fwd_only else w.flops_bwd / (sum(mean[1:]) / 1e3) / 1e12,
         "kernel_ms": {n: m for n, m in zip(names, mean) if n != "-"},
         "roofline": roofline,

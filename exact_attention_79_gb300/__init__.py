@@ -47,6 +47,7 @@ SIGNATURES = {
     "fa_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_fp8_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_ex2_throughput": (_I, [ctypes.POINTER(ctypes.c_double), _VP]),
+    "fa_sm_clock_mhz": (_I, [ctypes.POINTER(ctypes.c_double), _VP]),
     "fa_device_status": (_I, [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),
@@ -294,6 +295,16 @@ def ex2_throughput(stream=None):
     s = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
     out = ctypes.c_double(0.0)
     _check("fa_ex2_throughput", load().fa_ex2_throughput(ctypes.byref(out), s))
+    return out.value
+
+
+def sm_clock_mhz(stream=None):
+    """Mean SM clock (MHz) of the forward and dK/dV kernels since the last
+    call, measured by the kernels (fa_sm_clock_mhz); 0.0 if none ran."""
+    import torch
+    s = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    out = ctypes.c_double(0.0)
+    _check("fa_sm_clock_mhz", load().fa_sm_clock_mhz(ctypes.byref(out), s))
     return out.value
 
 

@@ -19,6 +19,9 @@ namespace {
 // beyond the first kStatusSlots - 1 that a device sees.
 constexpr int kStatusSlots = 256;
 __device__ unsigned g_status_words[kStatusSlots];
+// SM cycles and nanoseconds summed over the CTAs of the forward and dK/dV
+// kernels since the last fa_sm_clock_mhz (diagnostic, device-wide).
+__device__ unsigned long long g_clock_acc[2];
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -43,6 +46,7 @@ struct DeviceState {
   bool arch_ok = false;
   int num_sms = 0;
   unsigned* status = nullptr;           // device address of g_status_words on this device
+  unsigned long long* clock_acc = nullptr;  // device address of g_clock_acc on this device
   std::mutex mu;                        // guards the stream -> slot table below
   const void* owner[kStatusSlots] = {}; // owner[i]: the stream whose calls report to slot i (i >= 1)
   int used = 1;
@@ -64,7 +68,8 @@ unsigned* stream_slot(DeviceState& s, const void* stream) {
 
 // Checks the current device once (compute capability 10.3), resolves the
 // device address of the status words on it and returns the word of `stream`.
-fa_status device_state(const void* stream, unsigned** status_out, int* num_sms = nullptr) {
+fa_status device_state(const void* stream, unsigned** status_out, int* num_sms = nullptr,
+                       unsigned long long** clock_acc = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
@@ -77,11 +82,14 @@ fa_status device_state(const void* stream, unsigned** status_out, int* num_sms =
     if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) s.num_sms = 0;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_words) == cudaSuccess) s.status = static_cast<unsigned*>(p);
+    void* c = nullptr;
+    if (cudaGetSymbolAddress(&c, g_clock_acc) == cudaSuccess) s.clock_acc = static_cast<unsigned long long*>(c);
   });
   if (!s.arch_ok) return FA_ERR_ARCH;
-  if (!s.status || s.num_sms <= 0) return FA_ERR_CUDA;
+  if (!s.status || !s.clock_acc || s.num_sms <= 0) return FA_ERR_CUDA;
   *status_out = stream_slot(s, stream);
   if (num_sms) *num_sms = s.num_sms;
+  if (clock_acc) *clock_acc = s.clock_acc;
   return FA_OK;
 }
 
@@ -166,7 +174,8 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   const bool wide = d > 128;                // one query tile per CTA, V in 64-key halves
   if (wide && mask) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
-  st = device_state(stream, &status);
+  unsigned long long* clock_acc = nullptr;
+  st = device_state(stream, &status, nullptr, &clock_acc);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
@@ -176,6 +185,7 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   fa::FwdParams p{};
   p.lse = lse;
   p.status = status;
+  p.clock_acc = clock_acc;
   p.N = N;
   p.Nk = Nk;
   p.causal_off = Nk - N;
@@ -235,13 +245,15 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
       workspace_bytes < (mask ? w.total_sparse : (lse_d_only ? w.off_dq : w.total)))
     return FA_ERR_WORKSPACE;
   unsigned* status = nullptr;
-  st = device_state(stream, &status, num_sms);
+  unsigned long long* clock_acc = nullptr;
+  st = device_state(stream, &status, num_sms, &clock_acc);
   if (st != FA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p->ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
   p->ws_d = reinterpret_cast<float*>(ws + w.off_d);
   p->ws_dq = reinterpret_cast<float*>(ws + w.off_dq);
   p->status = status;
+  p->clock_acc = clock_acc;
   p->N = N;
   p->NQP = ((N + 127) / 128) * 128;
   p->Nk = Nk;
@@ -553,6 +565,22 @@ fa_status fa_device_status(void* stream) {
   return FA_OK;
 }
 
+fa_status fa_sm_clock_mhz(double* mhz, void* stream) {
+  if (!mhz) return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  unsigned long long* acc = nullptr;
+  const fa_status st = device_state(stream, &status, nullptr, &acc);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  unsigned long long host[2] = {0, 0};
+  if (cudaMemcpyAsync(host, acc, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemsetAsync(acc, 0, sizeof(host), s) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  *mhz = host[1] > 0 ? static_cast<double>(host[0]) * 1e3 / static_cast<double>(host[1]) : 0.0;
+  return FA_OK;
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "ok";
@@ -567,6 +595,6 @@ const char* fa_status_string(fa_status s) {
   return "unknown status";
 }
 
-int fa_version(void) { return 300; }
+int fa_version(void) { return 400; }
 
 }  // extern "C"

@@ -183,6 +183,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t bar_stall = bars + 208;                   // nothing arrives (timeout test)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 192);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 196);
+  unsigned long long* const clock_start = reinterpret_cast<unsigned long long*>(gbase + C::kOffBar + 224);   // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -213,6 +214,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const unsigned* const steps = kSparse ? p.ws_list + static_cast<size_t>(cta) * G * nq : nullptr;
 
   if (threadIdx.x == 0) {
+    clock_mark(clock_start);
     *abort_flag = 0;
     mbar_init(bar_kv_full, 1);
     for (int st = 0; st < 2; ++st) {
@@ -611,6 +613,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+  if (threadIdx.x == 0) clock_record(p.clock_acc, clock_start);
 }
 
 // ------------------------------------------------------------------ launch

@@ -31,6 +31,22 @@ __device__ __forceinline__ void abort_grace_period() {
   while (global_timer_ns() < until) __nanosleep(10000);
 }
 
+// SM clock of a launch, measured by the kernel itself: one thread per CTA
+// notes the SM cycle counter and the global nanosecond timer when the CTA
+// starts (clock_mark, into two words of shared memory, so that no register
+// is held across the kernel) and adds both differences into acc[0] (cycles)
+// and acc[1] (ns) when it exits, so acc[0] / acc[1] is the mean SM clock over
+// the CTAs' lifetimes.
+__device__ __forceinline__ void clock_mark(unsigned long long* start) {
+  start[0] = static_cast<unsigned long long>(clock64());
+  start[1] = global_timer_ns();
+}
+__device__ __forceinline__ void clock_record(unsigned long long* acc, const unsigned long long* start) {
+  if (acc == nullptr) return;
+  atomicAdd(acc, static_cast<unsigned long long>(clock64()) - start[0]);
+  atomicAdd(acc + 1, global_timer_ns() - start[1]);
+}
+
 // Byte address, inside a 128-byte-swizzled box, of 16-byte unit `u` (0..7)
 // of row `r`: the unit index is XORed with the row's position in its 8-row
 // (1024-byte) group. This is the layout TMA writes with 128-byte swizzle and

@@ -168,6 +168,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   // barriers; entry = tile | (visible to tile 0) << 14 | (visible to tile 1) << 15
   int* const list_count = reinterpret_cast<int*>(gbars + 480);       // [0] all, [1] group 0's prefix
   const uint32_t bar_stall = bars + 472;                             // nothing arrives (timeout test)
+  unsigned long long* const clock_start = reinterpret_cast<unsigned long long*>(gbars + 456);   // [2]
+  static_assert(80 + 16 * C::kStages <= 456, "barrier area");
   uint16_t* const tile_list = reinterpret_cast<uint16_t*>(gbars + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -195,6 +197,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const bool has_tile[2] = {true, C::kPingPong && qt[1] < nq};
 
   if (threadIdx.x == 0) {
+    clock_mark(clock_start);
     *abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
@@ -613,6 +616,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+  if (threadIdx.x == 0) clock_record(p.clock_acc, clock_start);
 }
 
 template <typename T, int D, bool kSparse>

@@ -29,6 +29,7 @@ struct FwdParams {
   const float* k_scale;
   const float* v_scale;
   int head_dim;                    // FP8 forward: d (64 runs in the d = 128 kernel, columns past d zero)
+  unsigned long long* clock_acc;   // [2] SM cycles and ns of every CTA's lifetime, summed (fwd_kernel); may be null
 };
 constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 131072)
 
@@ -87,6 +88,7 @@ struct BwdParams {
   unsigned* ws_list;
   int test_stall;                  // 1: the issuer first waits on a barrier nothing arrives on (timeout test)
   int head_group;                  // dK/dV: KV heads scheduled together (set by launch_bwd_dkdv)
+  unsigned long long* clock_acc;   // [2] SM cycles and ns of every CTA's lifetime, summed (dK/dV); may be null
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO, dk, dv;

@@ -279,6 +279,18 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * value). Calls on other streams are neither waited for nor reported. */
 fa_status fa_device_status(void* stream);
 
+/* Diagnostic: the mean SM clock, in MHz, of the forward (fa_fwd, fa_fwd_f32,
+ * fa_fwd_kv, fa_fwd_blocksparse at d <= 128) and dK/dV (fa_bwd and its
+ * variants) kernels launched on this device since the previous call, as
+ * measured by the kernels themselves: each block adds the SM cycle count and
+ * the nanoseconds between its start and its exit to two device-wide sums,
+ * and *mhz = cycles / ns * 1000 (0 when no such kernel ran). Synchronises
+ * the device, then resets the sums. Calls from several host threads or on
+ * several streams share the sums. FA_ERR_INVALID_ARG for a null pointer.
+ * No counterpart on the pages: it attributes a measured time to the clock it
+ * ran at. */
+fa_status fa_sm_clock_mhz(double* mhz, void* stream);
+
 /* Diagnostic: throughput of the exponential instruction the softmax uses
  * (ex2.approx), measured on the current device, for the exponential ceiling
  * of the forward (one exponential per 4 d floating-point operations).
