@@ -145,33 +145,20 @@ struct BwdCfg {
   static_assert(kDqHalfBoxes * kBoxBytes <= kDsBytes && kDqHalfBoxes * kBoxBytes <= kTileBytes, "dQ staging");
 };
 
-// kPair (dense only): the kernel runs in clusters of two CTAs that own the
-// adjacent key tiles 2p and 2p+1 of one (batch, KV head) and visit the same
-// query tiles in the same order (tile 2p first visits the ones only it sees,
-// when causal). For every step they share, each CTA reduces only half of dQ_i
-// (CTA rank c: columns [c D/2, (c+1) D/2)): the group that owns the other
-// half stages it in shared memory as before, and the peer's owning group
-// reads it across the cluster (distributed shared memory), adds its own
-// partial and stages the sum for its reducer. One fp32 reduction into the
-// L2 then covers 256 keys instead of 128, halving the reduce traffic that
-// bounds this kernel. The MMAs and the dK, dV results are unchanged.
-template <int D, bool kSparse, bool kPair>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(384, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                 const __grid_constant__ CUtensorMap map_dqacc, const BwdParams p) {
   using C = BwdCfg<D>;
-  static_assert(!(kSparse && kPair), "block-sparse step lists differ between key tiles: no pairing");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kLayoutBytes > static_cast<uint32_t>(C::kSmemAlloc)) {
     // The layout needs the dynamic window to start within 768 bytes of a
-    // 1 KB boundary; refuse (and report) rather than overrun. (Both CTAs of a
-    // pair run the same kernel image, so both refuse and neither waits for
-    // the other.)
+    // 1 KB boundary; refuse (and report) rather than overrun.
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
   }
@@ -197,11 +184,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 192);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 196);
   unsigned long long* const clock_start = reinterpret_cast<unsigned long long*>(gbase + C::kOffBar + 224);   // [2]
-  // pair exchange (kPair), per parity of the shared-step index k: "the peer
-  // staged its partial of my half of dQ_k" and "the peer has read my staged
-  // partial of its half", each arrived by the peer's 128 threads of one group
-  auto bar_x_staged = [&](int k) { return bars + ((k & 1) ? 216u : 200u); };
-  auto bar_x_read = [&](int k) { return bars + ((k & 1) ? 248u : 240u); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -212,41 +194,23 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   // causal) go first. `cta` is the item's logical index, key tile * BHkv +
   // batch * Hkv + kv head (the block-sparse step lists are kept by it).
   const int nkt = p.NKP / kBN;
-  // pairs (kPair): the cluster's two CTAs take key tiles 2 jp and 2 jp + 1
-  const int nunits = kPair ? (nkt + 1) / 2 : nkt;
-  const int rank = kPair ? static_cast<int>(blockIdx.x & 1) : 0;
-  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int grp = unit / (nunits * p.head_group);
+  const int grp = blockIdx.x / (nkt * p.head_group);
   const int gsize = min(p.head_group, p.BHkv - grp * p.head_group);
-  const int local = unit - grp * p.head_group * nunits;
-  const int ju = local / gsize;
-  const int jt = kPair ? 2 * ju + rank : ju;
-  const bool ghost = jt >= nkt;                  // the second tile of a pair when nkt is odd: no keys
+  const int local = blockIdx.x - grp * p.head_group * nkt;
+  const int jt = local / gsize;
   const int bhkv = grp * p.head_group + local % gsize;
   const int cta = jt * p.BHkv + bhkv;
   const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int nq = p.NQP / kBM;
-  // first query tile that sees key tile j: causal, the one holding query
-  // row j*128 - (Nk - N) (bottom-right alignment; j itself when Nk == N)
-  auto first_tile = [&](int j) {
-    const int first_row = j * kBN - p.causal_off;
-    return p.causal ? (first_row <= 0 ? 0 : min(nq, first_row / kBM)) : 0;
-  };
-  const int it0 = ghost ? nq : first_tile(jt);
+  // first query tile that sees key tile jt: causal, the one holding query
+  // row jt*128 - (Nk - N) (bottom-right alignment; jt itself when Nk == N)
+  const int first_row = jt * kBN - p.causal_off;
+  const int it0 = p.causal ? (first_row <= 0 ? 0 : min(nq, first_row / kBM)) : 0;
   const int tiles_per_head = nq - it0;
   // block-sparse: only the (head, query tile) steps the mask lets see this key
   // tile, in the dense order, from the list bwd_blocklist_kernel compacted
   const int nsteps = kSparse ? p.ws_count[cta] : G * tiles_per_head;
-  // pairing: every step of tile 2 jp + 1 is shared; so are the steps of tile
-  // 2 jp at query tiles it >= it0 of tile 2 jp + 1 (first_tile grows with j).
-  // Shared step (head h, tile it) has index k = h tph1 + it - it0_1 in both
-  // CTAs; a CTA's own step index of it is h tph_own + it - it0_own.
-  const bool has_pair = kPair && !ghost && (2 * ju + 1) < nkt;
-  const int it0_0 = kPair ? first_tile(2 * ju) : 0;
-  const int it0_1 = has_pair ? first_tile(2 * ju + 1) : nq;
-  const int tph0 = nq - it0_0, tph1 = nq - it0_1;
-  const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
   const unsigned* const steps = kSparse ? p.ws_list + static_cast<size_t>(cta) * G * nq : nullptr;
 
   if (threadIdx.x == 0) {
@@ -271,12 +235,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     mbar_init(bar_dq_free, 257);           // + the watcher: dO of the next step has landed
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
-    if (kPair) {
-      for (int x = 0; x < 2; ++x) {
-        mbar_init(bar_x_staged(x), 128);
-        mbar_init(bar_x_read(x), 128);
-      }
-    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -284,9 +242,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     tmem_relinquish();
   }
   tc_fence_before();
-  // a pair's barriers are initialised on both sides before either arrives remotely
-  if constexpr (kPair) cluster_sync_all();
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
@@ -295,14 +251,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   };
   auto step_tile = [&](int step) {
     return kSparse ? static_cast<int>(steps[step] & 0xFFFFu) : it0 + step % tiles_per_head;
-  };
-  // kPair: whether step `step` is shared with the peer, its shared index k,
-  // and the peer's stage for it
-  auto step_paired = [&](int step) { return has_pair && step_tile(step) >= it0_1; };
-  auto step_k = [&](int step) { return (step / tiles_per_head) * tph1 + step_tile(step) - it0_1; };
-  auto peer_stage = [&](int step) {
-    const int h = step / tiles_per_head, it = step_tile(step);
-    return (rank == 0 ? h * tph1 + it - it0_1 : h * tph0 + it - it0_0) & 1;
   };
 
   if (warp == 0) {
@@ -423,52 +371,22 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // reductions, both halves in flight together; each region goes back to
     // the producer as soon as its half has been read.
     if (lane == 0) {
-      // phases completed so far by the staged barriers of the half this CTA
-      // does not own, per stage: they are used on unshared steps only
-      int other_uses[2] = {0, 0};
       for (int step = 0; step < nsteps; ++step) {
         const int st = step & 1;
         const int bh = step_head(step), it = step_tile(step);
         bool ok = true;
-        if (kPair && step_paired(step)) {
-          // shared step: reduce the summed half this CTA owns; the other
-          // half's region goes back once the peer has read it
-          const int k = step_k(step);
-          const int go = rank;
-          const uint32_t src = go ? s_do(st) : s_q(st);
-          for (int bx = 0; bx < C::kDqHalfBoxes && ok; ++bx) {
-            ok = mbar_wait(bar_dq_staged(go, st, bx), (step >> 1) & 1, abort_flag, deadline);
-            if (!ok) break;
-            tma_reduce_add_3d(&map_dqacc, src + bx * kBoxBytes, go * (D / 2) + bx * 32, it * kBM, bh);
-            tma_store_commit();
-          }
-          if (ok && go == 1) {
-            ok = mbar_wait_cluster(bar_x_read(k), (k >> 1) & 1, abort_flag, deadline);
-            if (ok) mbar_arrive(bar_q_empty(st));
-          }
-          if (!ok) break;
-          tma_store_wait_read0();
-          mbar_arrive(go ? bar_do_empty(st) : bar_q_empty(st));
-          if (go == 0) {
-            if (!mbar_wait_cluster(bar_x_read(k), (k >> 1) & 1, abort_flag, deadline)) break;
-            mbar_arrive(bar_do_empty(st));
-          }
-          continue;
-        }
         // group 0's boxes first (its region, Q, is needed first again), each
         // box as soon as it has been written
         for (int g = 0; g < 2 && ok; ++g) {
           const uint32_t src = g ? s_do(st) : s_q(st);
-          const int par = (kPair && g != rank) ? (other_uses[st] & 1) : ((step >> 1) & 1);
           for (int bx = 0; bx < C::kDqHalfBoxes && ok; ++bx) {
-            ok = mbar_wait(bar_dq_staged(g, st, bx), par, abort_flag, deadline);
+            ok = mbar_wait(bar_dq_staged(g, st, bx), (step >> 1) & 1, abort_flag, deadline);
             if (!ok) break;
             tma_reduce_add_3d(&map_dqacc, src + bx * kBoxBytes, g * (D / 2) + bx * 32, it * kBM, bh);
             tma_store_commit();
           }
         }
         if (!ok) break;
-        ++other_uses[st];
         tma_store_wait_read<C::kDqHalfBoxes>();
         mbar_arrive(bar_q_empty(st));
         tma_store_wait_read0();
@@ -617,33 +535,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle, each released
       // to the reducer as soon as this group has written it
       const uint32_t dst0 = g ? s_do(st) : s_q(st);
-      const bool paired = kPair && step_paired(step);
-      if (paired && g == rank) {
-        // this CTA owns half g: add the peer's partial, staged in the same
-        // region of the peer's stage for this step, and stage the sum
-        const int k = step_k(step);
-        ok = mbar_wait_cluster(bar_x_staged(k), (k >> 1) & 1, abort_flag, deadline);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const int sp = peer_stage(step);
-        const uint32_t src0 = mapa_shared(g ? s_do(sp) : s_q(sp), peer);
-#pragma unroll
-        for (int bx = 0; bx < C::kDqHalfBoxes; ++bx) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t off = swz128(bx * kBoxBytes, r, u);
-            const float4 pv = ld_shared_cluster_v4(src0 + off);
-            const int c = 32 * bx + 4 * u;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(dst0 + off),
-                         "f"(__uint_as_float(dq[c]) + pv.x), "f"(__uint_as_float(dq[c + 1]) + pv.y),
-                         "f"(__uint_as_float(dq[c + 2]) + pv.z), "f"(__uint_as_float(dq[c + 3]) + pv.w) : "memory");
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(bar_dq_staged(g, st, bx));
-        }
-        mbar_arrive_remote(mapa_shared(bar_x_read(k), peer));   // the peer may reuse its region
-        continue;
-      }
 #pragma unroll
       for (int bx = 0; bx < C::kDqHalfBoxes; ++bx) {
 #pragma unroll
@@ -654,10 +545,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                        "r"(dq[c + 2]), "r"(dq[c + 3]) : "memory");
         }
         fence_proxy_async_smem();
-        if (!paired) mbar_arrive(bar_dq_staged(g, st, bx));
+        mbar_arrive(bar_dq_staged(g, st, bx));
       }
-      // the peer owns this half: it reads the staged partial across the cluster
-      if (paired) mbar_arrive_remote(mapa_shared(bar_x_staged(step_k(step)), peer));
     }
     // ---------------------------------------------------------- dK, dV epilogue
     if (ok) {
@@ -722,46 +611,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
     abort_grace_period();
   }
-  // neither CTA of a pair leaves while the other may still read its shared
-  // memory or arrive on its barriers
-  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
   if (threadIdx.x == 0) clock_record(p.clock_acc, clock_start);
 }
 
 // ------------------------------------------------------------------ launch
-template <int D, bool kSparse, bool kPair>
+template <int D, bool kSparse>
 static cudaError_t launch_dkdv_d(const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static PerDeviceOnce attr;
   const cudaError_t e = attr.run([] {
-    return cudaFuncSetAttribute(bwd_dkdv_kernel<D, kSparse, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(bwd_dkdv_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemAlloc);
   });
   if (e != cudaSuccess) return e;
-  const int nkt = p.NKP / kBN;
-  // pairs: clusters of two CTAs on key tiles 2p, 2p + 1 (the second one
-  // empty when the count is odd)
-  const int grid = (kPair ? 2 * ((nkt + 1) / 2) : nkt) * p.BHkv;
+  const int grid = (p.NKP / kBN) * p.BHkv;
   // KV heads per group: the group's Q and dO (bf16) and fp32 dQ accumulator,
   // G query heads of N x d each, within 64 MB, half of L2
   BwdParams q = p;
   const long long per_kv_head = 8LL * (p.Hq / p.Hkv) * p.N * D;
   q.head_group = static_cast<int>(std::max(1LL, std::min<long long>(p.BHkv, (64LL << 20) / per_kv_head)));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmemAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kPair ? 2 : 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = kPair ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D, kSparse, kPair>, m.q, m.k, m.v, m.dO, m.dk, m.dv, m.dqacc, q);
+  bwd_dkdv_kernel<D, kSparse><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv,
+                                                                             m.dqacc, q);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ block list
@@ -825,13 +698,9 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* ls
 
 cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   const bool sparse = p.mask != nullptr;
-  // dense: key-tile pairs that sum their dQ partials before the reduction;
-  // block-sparse: one CTA per key tile (the step lists of two tiles differ).
   // d < 128 runs in the kernel for the next size up (zero-filled columns)
-  if (d > 64 && d <= 128)
-    return sparse ? launch_dkdv_d<128, true, false>(m, p, stream) : launch_dkdv_d<128, false, true>(m, p, stream);
-  if (d >= 8 && d <= 64)
-    return sparse ? launch_dkdv_d<64, true, false>(m, p, stream) : launch_dkdv_d<64, false, true>(m, p, stream);
+  if (d > 64 && d <= 128) return sparse ? launch_dkdv_d<128, true>(m, p, stream) : launch_dkdv_d<128, false>(m, p, stream);
+  if (d >= 8 && d <= 64) return sparse ? launch_dkdv_d<64, true>(m, p, stream) : launch_dkdv_d<64, false>(m, p, stream);
   return cudaErrorInvalidValue;
 }
 
