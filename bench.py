@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd", choices=["fused", "deterministic"], default="fused",
                     help="backward timed: fa_bwd's three phases (default) or fa_bwd_deterministic")
+    ap.add_argument("--fwd", choices=["single", "pair"], default="single",
+                    help="dense bf16 forward timed: fa_fwd (default) or fa_fwd_pair (CTA pairs, cta_group::2)")
     return ap.parse_args()
 
 
@@ -360,6 +362,9 @@ def native_arm(args, w):
     if fwd_only and (sparse or kvlen or det):
         raise SystemExit("forward-only workloads are dense with equal lengths")
     fwd_name = "fa_fwd" if w.dtype == "bf16" else "fa_fwd_f32"
+    pair_fwd = args.fwd == "pair"
+    if pair_fwd and (w.dtype != "bf16" or not 64 < w.d <= 128 or sparse or kvlen):
+        raise SystemExit("fa_fwd_pair: dense bf16 workloads with 64 < d <= 128 only")
     fp8 = w.dtype == "fp8e4m3"
     if fp8:
         # e4m3 codes and scales, resident before the timed region
@@ -396,7 +401,12 @@ def native_arm(args, w):
             return marks(1)
         if fwd_only:
             mark(0)
-            check(fwd_name, getattr(lib, fwd_name)(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
+            if pair_fwd:
+                check("fa_fwd_pair", lib.fa_fwd_pair(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), w.B, w.Hq, w.Hkv, w.N,
+                                                     w.N, w.d, causal, scale, sp))
+            else:
+                check(fwd_name, getattr(lib, fwd_name)(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale,
+                                                       sp))
             return marks(1)
         if kvlen:
             # queries are the last N of Nk positions (fa_fwd_kv / fa_bwd_kv)
@@ -419,7 +429,11 @@ def native_arm(args, w):
                                                                0, *dims, causal, scale, sp))
             return marks(2)
         mark(0)
-        check("fa_fwd", lib.fa_fwd(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
+        if pair_fwd:
+            check("fa_fwd_pair", lib.fa_fwd_pair(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), w.B, w.Hq, w.Hkv, w.N, w.N,
+                                                 w.d, causal, scale, sp))
+        else:
+            check("fa_fwd", lib.fa_fwd(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
         mark(1)
         if det:
             # one call: preprocess, dK/dV pass, dQ pass (no atomics)
@@ -479,6 +493,8 @@ def native_arm(args, w):
     if fp8:
         fwd_kernel = "fwd_fp8_wide_kernel" if w.d > 128 else "fwd_fp8_kernel"
         fwd_src = "fa_fwd_fp8_wide.cu" if w.d > 128 else "fa_fwd_fp8.cu"
+    elif pair_fwd:
+        fwd_kernel, fwd_src = "fwd_pair_kernel", "fa_fwd_pair.cu"
     else:
         fwd_kernel = "fwd_wide_kernel" if w.d > 128 else "fwd_kernel"
         fwd_src = "fa_fwd_wide.cu" if w.d > 128 else "fa_fwd.cu"
@@ -583,7 +599,8 @@ def native_arm(args, w):
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "bwd_variant": "none" if fwd_only else args.bwd},
+                   "bwd_variant": "none" if fwd_only else args.bwd,
+                   "fwd_variant": args.fwd},
         "frac_of_peak": value / world / peak,
         "fwd_tflops": w.flops_fwd / (mean[0] / 1e3) / 1e12,
         "fwd_frac_of_peak": w.flops_fwd / (mean[0] / 1e3) / 1e12 / peak,

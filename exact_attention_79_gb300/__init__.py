@@ -25,6 +25,7 @@ SIGNATURES = {
     "fa_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "fa_fwd_pair": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_bwd_kv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                        _I, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "fa_fwd_blocksparse": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _LL, _LL, _I, _I, _I, _I, _I, _I, _F, _VP]),

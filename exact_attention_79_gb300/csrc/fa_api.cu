@@ -163,7 +163,7 @@ fa_status bwd_dim(int d) { return d > 128 ? FA_ERR_UNSUPPORTED : FA_OK; }
 fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, int N, int d, int causal, float scale, void* stream,
                      const unsigned char* mask = nullptr, long long mask_sb = 0, long long mask_sh = 0,
-                     int Nk = -1) {
+                     int Nk = -1, bool use_pair = false) {
   if (Nk < 0) Nk = N;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
@@ -173,13 +173,17 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   if (elt == 4 && d != 64) return FA_ERR_UNSUPPORTED;
   const bool wide = d > 128;                // one query tile per CTA, V in 64-key halves
   if (wide && mask) return FA_ERR_UNSUPPORTED;
+  // fa_fwd_pair: CTA pairs (cta_group::2), K loaded in 64-row halves; bf16,
+  // 64 < d <= 128, dense only
+  const bool pair = use_pair;
+  if (pair && (elt != 2 || mask || d <= 64 || d > 128)) return FA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   unsigned long long* clock_acc = nullptr;
   st = device_state(stream, &status, nullptr, &clock_acc);
   if (st != FA_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-  if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, Nk, BHkv) ||
+  if (!make_map(&mq, q, elt, d, N, BHq) || !make_map(&mk, k, elt, d, Nk, BHkv, pair ? 64 : 128) ||
       !make_map(&mv, v, elt, d, Nk, BHkv, wide ? 64 : 128) || !make_map(&mo, o, elt, d, N, BHq))
     return FA_ERR_CUDA;
   fa::FwdParams p{};
@@ -200,8 +204,10 @@ fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void*
   p.mask_sb = mask_sb;
   p.mask_sh = mask_sh;
   p.mask_nt = (N + 127) / 128;
-  const cudaError_t e = wide ? fa::launch_fwd_wide(d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream))
-                             : fa::launch_fwd(elt, d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = wide ? fa::launch_fwd_wide(d, mq, mk, mv, mo, p, s)
+                        : pair ? fa::launch_fwd_pair(mq, mk, mv, mo, p, s)
+                               : fa::launch_fwd(elt, d, mq, mk, mv, mo, p, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -435,6 +441,12 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float*
                     int Nk, int d, int causal, float scale, void* stream) {
   if (Nk < 1) return FA_ERR_INVALID_ARG;
   return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, Nq, d, causal, scale, stream, nullptr, 0, 0, Nk);
+}
+
+fa_status fa_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                      int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  return fwd_common(2, q, k, v, o, lse, B, Hq, Hkv, Nq, d, causal, scale, stream, nullptr, 0, 0, Nk, true);
 }
 
 fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,

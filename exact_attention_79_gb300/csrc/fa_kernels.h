@@ -37,6 +37,12 @@ constexpr int kMaskMaxTiles = 1024;  // block-mask rows up to 1024 tiles (N <= 1
 cudaError_t launch_fwd(int dtype_bytes, int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
 
+// bf16, d in (64, 128], no block mask: clusters of two CTAs (four query tiles)
+// whose MMAs run as cta_group::2 pairs; mk64 is the K map with 64-row boxes
+// (each CTA loads half of every K tile), mv the usual V map.
+cudaError_t launch_fwd_pair(const CUtensorMap& mq, const CUtensorMap& mk64, const CUtensorMap& mv,
+                            const CUtensorMap& mo, FwdParams p, cudaStream_t stream);
+
 // Head dims 136..256 (bf16, dense): one 128-row query tile per CTA; the V
 // map has 64-row boxes (the kernel stages V in 64-key halves).
 cudaError_t launch_fwd_wide(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,

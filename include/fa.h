@@ -92,6 +92,20 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale, void* stream);
 
+/* fa_fwd_kv computed by clusters of two CTAs whose matrix products run as
+ * tcgen05 cta_group::2 pairs (M = 256 over two SMs; each CTA loads half of
+ * every K and V tile). Same arguments, layouts, masking and results as
+ * fa_fwd_kv (bit for bit on this GPU: each row's products and softmax are
+ * the same operations in the same order); bf16 only, 64 < d <= 128, no block
+ * mask (FA_ERR_UNSUPPORTED otherwise). Slower than fa_fwd_kv on GB300 (one
+ * issuing thread must still start an MMA every 64 cycles to keep both SMs
+ * busy, and every hand-off gains a cross-CTA step), so fa_fwd and fa_fwd_kv
+ * do not use it; it is kept as the measured pair form. No counterpart on the
+ * pages beyond the forward itself ("FlashAttention技术解析" 2.1-2.2). */
+fa_status fa_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                      int Nq, int Nk, int d, int causal, float scale, void* stream);
+
+
 /* Forward with a block mask, bf16 ("FlashAttention技术解析", section 6.2: whole
  * blocks are skipped, as the causal mask skips the blocks above the diagonal).
  * Same arguments and outputs as fa_fwd, plus a block mask over 128 x 128 tiles:
