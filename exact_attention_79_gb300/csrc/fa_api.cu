@@ -257,7 +257,9 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p->ws_lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
   p->ws_d = reinterpret_cast<float*>(ws + w.off_d);
-  p->ws_dq = reinterpret_cast<float*>(ws + w.off_dq);
+  // a workspace sized for the LSE and D parts alone has no dQ accumulator:
+  // nothing may write past its end
+  p->ws_dq = lse_d_only ? nullptr : reinterpret_cast<float*>(ws + w.off_dq);
   p->status = status;
   p->clock_acc = clock_acc;
   p->N = N;

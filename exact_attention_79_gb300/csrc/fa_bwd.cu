@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       p.ws_lse2[r] = (i < p.N) ? lse[static_cast<size_t>(bh) * p.N + i] * kLog2e : INFINITY;
     }
   }
+  // the dQ accumulator, when the workspace has one (the deterministic
+  // backward's workspace holds only the LSE and D parts: ws_dq is null)
+  if (p.ws_dq == nullptr) return;
   const long long n4 = static_cast<long long>(p.BH) * p.N * d / 4;
   float4* acc4 = reinterpret_cast<float4*>(p.ws_dq);
   for (long long x = tid; x < n4; x += nthreads) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);

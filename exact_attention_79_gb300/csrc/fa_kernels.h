@@ -75,7 +75,8 @@ cudaError_t measure_ex2_rate(int num_sms, int iters, double* per_sm_per_cycle, c
 struct BwdParams {
   float* ws_lse2;                  // [BH, NQP] LSE * log2(e), +inf in the padding rows
   float* ws_d;                     // [BH, NQP] rowsum(dO * O), 0 in the padding rows
-  float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled, TMA reduce-add target)
+  float* ws_dq;                    // [BH, N, d] fp32 dQ accumulator (unscaled, TMA reduce-add target);
+                                   // null when the workspace holds only the LSE and D parts
   unsigned* status;                // device status word
   int N, NQP;                      // query positions; NQP = N rounded up to a multiple of 128
   int Nk, NKP;                     // key positions and Nk rounded up to a multiple of 128

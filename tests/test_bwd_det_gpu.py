@@ -83,7 +83,10 @@ def test_det_bwd_workspace_needs_only_lse_and_d(fa):
     t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=5, with_grad=True)
     q, k, v, do = (t[n].to(dev) for n in ("q", "k", "v", "do"))
     o, lse = fa.fwd(q, k, v, causal=False)
-    ws = torch.empty(small, dtype=torch.uint8, device=dev)
+    # the workspace is the head of a larger buffer whose tail is a canary: the
+    # call may write only the `small` bytes it was given
+    arena = torch.full((small + (1 << 20),), 0xA5, dtype=torch.uint8, device=dev)
+    ws = arena[:small]
     out = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
     P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
     args = [P(q), P(k), P(v), P(o), P(lse), P(do), P(out[0]), P(out[1]), P(out[2]), P(ws)]
@@ -91,6 +94,7 @@ def test_det_bwd_workspace_needs_only_lse_and_d(fa):
     assert lib.fa_bwd_deterministic(*args, small, B, Hq, Hkv, N, d, 0, 0.125, s) == 0
     assert lib.fa_bwd_deterministic(*args, small - 256, B, Hq, Hkv, N, d, 0, 0.125, s) == 6
     fa.check_device_status()
+    assert bool((arena[small:] == 0xA5).all()), "wrote past the end of the workspace"
     ref = fa.bwd(q, k, v, o, lse, do, causal=False, scale=0.125)
     for x, r in zip(out, ref):
         assert rel_fro(x.float().cpu().numpy(), r.float().cpu().numpy()) < 5e-3
