@@ -435,9 +435,10 @@ def native_arm(args, w):
         else:
             check("fa_fwd", lib.fa_fwd(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), *dims, causal, scale, sp))
         mark(1)
-        if det:
-            # one call: preprocess, dK/dV pass, dQ pass (no atomics)
-            check("fa_bwd_deterministic", lib.fa_bwd_deterministic(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(b.do),
+        if det or w.d > 128:
+            # one call: preprocess, then the dK/dV and dQ passes (no atomics); above
+            # d = 128 fa_bwd itself runs the three passes (dV, dK, dQ)
+            check("fa_bwd_deterministic", (lib.fa_bwd_deterministic if det else lib.fa_bwd)(P(b.q), P(b.k), P(b.v), P(b.o), P(b.lse), P(b.do),
                                                                    P(b.dq), P(b.dk), P(b.dv), P(ws), ws_bytes, *dims,
                                                                    causal, scale, sp))
             return marks(2)
@@ -503,16 +504,19 @@ def native_arm(args, w):
         names = [fwd_kernel, "-", "-", "-"]
     if det:
         names = ["fwd_kernel", "bwd_deterministic (preprocess + det_dkdv_kernel + det_dq_kernel)", "-", "-"]
+    elif w.backward and w.d > 128:
+        names = [fwd_kernel, "bwd_wide (preprocess + wide_kv_kernel dV, dK + wide_dq_kernel)", "-", "-"]
     if sparse:
         names = ["fwd_kernel (block-sparse)", "bwd_blocksparse (preprocess + block list + dkdv + dq convert)", "-", "-"]
     if kvlen:
         names = ["fwd_kernel (Nq != Nk)", "bwd_kv (preprocess + dkdv + dq convert)", "-", "-"]
     peak, peak_src = peak_tflops(w.dtype)
     # dominant kernel of the step and its tensor roofline
-    dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if (det or sparse or kvlen) else 2)
+    one_call_bwd = det or sparse or kvlen or (w.backward and w.d > 128)
+    dom = 0 if mean[0] >= max(mean[1], mean[2]) else (1 if one_call_bwd else 2)
     dom_flops = w.flops_fwd if dom == 0 else w.flops_bwd
     achieved = dom_flops / (mean[dom] / 1e3) / 1e12
-    traffic = None if ((det or sparse or kvlen) and dom != 0) else traffic_from_profile(
+    traffic = None if (one_call_bwd and dom != 0) else traffic_from_profile(
         fwd_src if dom == 0 else "fa_bwd.cu", names[dom], w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": names[dom], "peak_source": peak_src,
@@ -612,7 +616,8 @@ def native_arm(args, w):
         "step_ms_percentiles": percentiles(step_ms),
         "e2e": e2e,
         # fwd, preprocess, [block list], dK/dV, dQ convert
-        "gpu_launches": (1 if (fwd_only or fp8) else 5 if sparse else 4) * args.steps,
+        "gpu_launches": (1 if (fwd_only or fp8) else 5 if (sparse or (w.backward and w.d > 128)) else
+                         3 if det else 4) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t1 - t0,
     }

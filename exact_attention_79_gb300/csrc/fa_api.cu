@@ -156,9 +156,11 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
   return FA_OK;
 }
 
-// The backward kernels hold dK, dV, S^T and dP^T of a 128-key tile in TMEM
-// (4 x d columns of 512): head dims above 128 are not built.
-fa_status bwd_dim(int d) { return d > 128 ? FA_ERR_UNSUPPORTED : FA_OK; }
+// The one-pass backward kernels hold dK, dV, S^T and dP^T of a 128-key tile
+// in TMEM (4 x d columns of 512): up to d = 128. Above that the three-pass
+// backward (fa_bwd_wide.cu) serves fa_bwd, fa_bwd_kv, fa_bwd_deterministic
+// and fa_bwd_noalloc; the single phases and the block-sparse backward stop at 128.
+fa_status bwd_dim(int d, bool wide_ok = false) { return d > 128 && !wide_ok ? FA_ERR_UNSUPPORTED : FA_OK; }
 
 fa_status fwd_common(int elt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, int N, int d, int causal, float scale, void* stream,
@@ -244,7 +246,8 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale);
   if (st != FA_OK) return st;
   if (Nk < 1 || check_sizes(B, Hq, Hkv, Nk, d, scale) != FA_OK) return FA_ERR_INVALID_ARG;
-  st = bwd_dim(d);
+  // above d = 128 only the three-pass backward, which needs the LSE and D parts alone
+  st = bwd_dim(d, lse_d_only && !mask);
   if (st != FA_OK) return st;
   const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, N, d);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
@@ -290,8 +293,9 @@ fa_status bwd_setup(int B, int Hq, int Hkv, int N, int d, int causal, float scal
 extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
-  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK || bwd_dim(d) != FA_OK) return 0;
-  return bwd_workspace(B, Hq, Hkv, N, d).total;
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f) != FA_OK) return 0;
+  const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, N, d);
+  return d > 128 ? w.off_dq : w.total;      // the three-pass backward keeps no dQ accumulator
 }
 
 size_t fa_bwd_blocksparse_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
@@ -365,6 +369,35 @@ fa_status bwd_dkdv_common(const void* q, const void* k, const void* v, const voi
 }
 }  // namespace
 
+namespace {
+// Head dims 136..256: the three passes of fa_bwd_wide.cu after the
+// preprocess (no dQ accumulator in the workspace).
+fa_status bwd_wide(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                   int N, int Nk, int d, int causal, float scale, void* stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p{};
+  int num_sms = 0;
+  fa_status st = bwd_setup(B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, &p, &num_sms, stream, true,
+                           nullptr, 0, 0, Nk);
+  if (st != FA_OK) return st;
+  fa::BwdMaps m, m64;
+  const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+  if (!make_map(&m.q, q, 2, d, N, BHq) || !make_map(&m.k, k, 2, d, Nk, BHkv) || !make_map(&m.v, v, 2, d, Nk, BHkv) ||
+      !make_map(&m.dO, dO, 2, d, N, BHq) || !make_map(&m.dk, dk, 2, d, Nk, BHkv) ||
+      !make_map(&m.dv, dv, 2, d, Nk, BHkv) || !make_map(&m.dq, dq, 2, d, N, BHq) ||
+      !make_map(&m64.q, q, 2, d, N, BHq, 64) || !make_map(&m64.dO, dO, 2, d, N, BHq, 64) ||
+      !make_map(&m64.k, k, 2, d, Nk, BHkv, 64) || !make_map(&m64.v, v, 2, d, Nk, BHkv, 64))
+    return FA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_pre(d, o, dO, lse, p, num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_wide(m, m64, p, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
@@ -388,6 +421,9 @@ fa_status fa_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, in
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                  int N, int d, int causal, float scale, void* stream) {
+  if (d > 128)
+    return bwd_wide(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, N, d, causal, scale,
+                    stream);
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
@@ -401,10 +437,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                     int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  if (d > 128)
+    return bwd_wide(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk, d, causal,
+                    scale, stream);
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
-  if (Nk < 1) return FA_ERR_INVALID_ARG;
   fa_status st = fa_bwd_preprocess(o, lse, dO, workspace, workspace_bytes, B, Hq, Hkv, Nq, d, stream);
   if (st != FA_OK) return st;
   st = bwd_dkdv_common(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
@@ -415,6 +454,9 @@ fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, 
 fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                                int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
+  if (d > 128)       // the three-pass backward is bit reproducible too
+    return bwd_wide(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, N, d, causal, scale,
+                    stream);
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;

@@ -694,7 +694,7 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, const float* ls
   const int grid = num_sms * kStreamCtasPerSm;
   if (d == 128) bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
   else if (d == 64) bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
-  else if (d >= 8 && d <= 128 && d % 8 == 0) bwd_pre_kernel<0><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
+  else if (d >= 8 && d <= 256 && d % 8 == 0) bwd_pre_kernel<0><<<grid, 256, 0, stream>>>(o16, do16, lse, p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

@@ -1,0 +1,671 @@
+// Backward exact attention on sm_103a for head dimensions 136..256 (built for
+// d = 256; a smaller d reads zeros past its columns and stores none of them).
+//
+// Method: as fa_bwd.cu, the probabilities are recomputed from the stored
+// logsumexp ("4.3 FlashAttention-2与FlashAttention-3演进", FlashAttention-3
+// section 3) tile by tile (deepschool.ru FlashAttention-2, "Улучшение backward
+// pass"); FlashAttention-2 extends the supported head dimension to 256 (same
+// page, "Снижение накладных расходов").
+//
+// At d = 256 the dK and dV accumulators of a 128-key tile alone fill the 512
+// TMEM columns, and one step's Q, dO, K and V tiles (64 KB each) exceed shared
+// memory. The gradients are therefore formed in three passes over 64-row
+// sub-tiles (N = 64 products for the scores), each with a fixed order of
+// additions (no atomics: every output is bit reproducible):
+//   wide_kv_kernel<true>   per 128-key tile: S^T = K Q_s^T, P^T -> TMEM (bf16),
+//                          dV += P^T dO_s                      over 64-query steps s
+//   wide_kv_kernel<false>  per 128-key tile: S^T, dP^T = V dO_s^T,
+//                          dS^T = P^T (dP^T - D) -> shared memory, dK += dS^T Q_s
+//   wide_dq_kernel         per 128-row query tile: S = Q K_j^T, dP = dO V_j^T,
+//                          dS -> shared memory, dQ += dS K_j   over 64-key steps j
+// S (or S^T) and dP are formed twice or three times: 8 GEMMs of the 5 the
+// method needs. bwd_pre_kernel (fa_bwd.cu) writes D and the base-2 LSE first.
+//
+// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
+// (one thread), warps 2-5 one thread per TMEM lane (key row in the kv passes,
+// query row in the dQ pass).
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+
+namespace {
+
+constexpr int kWD = 256;                          // head-dimension build
+constexpr int kWSub = 64;                         // rows of a sub-tile step
+constexpr int kWTile = kWD / 64 * kBoxBytes;      // [128, 256] bf16: 64 KB
+constexpr int kWSubTile = kWTile / 2;             // [64, 256] bf16: 32 KB
+constexpr int kWSubBox = kBoxBytes / 2;           // one 64-row box: 8 KB
+constexpr int kWDs = kBoxBytes;                   // [128, 64] bf16 (dS or dS^T): 16 KB
+constexpr int kWThreads = 192;
+constexpr uint32_t kWColAcc = 0, kWColS = 256, kWColDP = 384;   // TMEM: accumulator | S x2 | dP x2
+
+// S (M = 128 rows of `a`, N = 64 rows of `b`, K = 256): both K-major, `a` in
+// boxes of 128 rows (16 KB), `b` in boxes of 64 rows (8 KB)
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a, uint32_t b) {
+  const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
+  const uint64_t ad = smem_desc_sw128(a, 16, 1024), bd = smem_desc_sw128(b, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kWD / 16; ++kk) {
+    const uint32_t kb = kk * 32;
+    mma_bf16_ss(d_tmem, desc_add(ad, (kb / 128) * kBoxBytes + kb % 128),
+                desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id, kk > 0);
+  }
+}
+
+// D[128, 256] += A[128, 64] B[64, 256]: B MN-major in boxes of 64 rows (one box
+// per 64 columns); A K-major in shared memory (one 16 KB box) or in TMEM
+__device__ __forceinline__ void issue_acc_ss(uint32_t d_tmem, uint32_t a, uint32_t b, bool acc) {
+  const uint32_t id = make_idesc(1, 128, kWD, 0, 1);
+  const uint64_t ad = smem_desc_sw128(a, 16, 1024), bd = smem_desc_sw128(b, kWSubBox, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kWSub / 16; ++kk)
+    mma_bf16_ss(d_tmem, desc_add(ad, kk * 32), desc_add(bd, kk * 16 * 128), id, acc || kk > 0);
+}
+__device__ __forceinline__ void issue_acc_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b, bool acc) {
+  const uint32_t id = make_idesc(1, 128, kWD, 0, 1);
+  const uint64_t bd = smem_desc_sw128(b, kWSubBox, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kWSub / 16; ++kk)
+    mma_bf16_ts(d_tmem, a_tmem + kk * 8, desc_add(bd, kk * 16 * 128), id, acc || kk > 0);
+}
+
+// 64 fp32 TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t r[2][32];
+  tmem_ld_32x32b_x32(taddr, r[0]);
+  tmem_ld_32x32b_x32(taddr + 32, r[1]);
+  tmem_wait_ld();
+  reg_fence_x32(r[0]);
+  reg_fence_x32(r[1]);
+#pragma unroll
+  for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(r[c >> 5][c & 31]);
+}
+
+// 64 bf16 values as row `row` of a [128, 64] 128-byte-swizzled box
+__device__ __forceinline__ void store_row64(uint32_t box, int row, const float (&x)[64]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, row, u)),
+                 "r"(pack_bf16x2(x[8 * u], x[8 * u + 1])), "r"(pack_bf16x2(x[8 * u + 2], x[8 * u + 3])),
+                 "r"(pack_bf16x2(x[8 * u + 4], x[8 * u + 5])), "r"(pack_bf16x2(x[8 * u + 6], x[8 * u + 7]))
+                 : "memory");
+}
+
+// The 256 fp32 accumulator columns of this thread's lane, times `mul`, as
+// row `row` of a [128, 256] bf16 tile (four 128-row boxes) at `stg`
+__device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int row, float mul) {
+#pragma unroll
+  for (int c0 = 0; c0 < kWD; c0 += 32) {
+    uint32_t t[32];
+    tmem_ld_32x32b_x32(taddr + c0, t);
+    tmem_wait_ld();
+    reg_fence_x32(t);
+    const uint32_t box = stg + (c0 / 64) * kBoxBytes;
+    const int u0 = (c0 % 64) / 8;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(t[8 * u + 2 * e]) * mul, __uint_as_float(t[8 * u + 2 * e + 1]) * mul);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(swz128(box, row, u0 + u)),
+                   "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+    }
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ dV (kDV) or dK per key tile
+// Shared memory: K | (dK: V) | two 32 KB sub-tile slots | (dK: dS^T x2) | LSE, D x2 | barriers.
+// dV: Q_s goes to slot s & 1 and dO_s to the other one of its own pair (four
+// slots: Q x2, dO x2 fit beside K). dK: Q_s is read by S^T_s and dK_s, dO_s
+// only by dP^T_s, so the two slots alternate: Q_{s+1} takes the slot dO_s
+// leaves early, dO_{s+1} the one Q_s leaves at the end of step s.
+template <bool kDV>
+struct WideKvCfg {
+  static constexpr int kSlots = kDV ? 4 : 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kWTile;                                  // dK only
+  static constexpr int kOffSlot = kDV ? kWTile : 2 * kWTile;
+  static constexpr int kOffDs = kOffSlot + kSlots * kWSubTile;          // dK only
+  static constexpr int kOffVec = kOffDs + (kDV ? 0 : 2 * kWDs);
+  static constexpr int kVecBytes = 512;                                 // LSE[64], D[64] of one step
+  static constexpr int kOffBar = kOffVec + 2 * kVecBytes;
+  static constexpr int kLayout = kOffBar + 256;
+  static constexpr int kSmemAlloc = kLayout + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
+
+template <bool kDV>
+__global__ void __launch_bounds__(192, 1)
+wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do64,
+               const __grid_constant__ CUtensorMap map_out, const BwdParams p) {
+  using C = WideKvCfg<kDV>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  if ((base - raw) + C::kLayout > static_cast<uint32_t>(C::kSmemAlloc)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
+    return;
+  }
+  const uint32_t s_k = base + C::kOffK, s_v = base + C::kOffV;
+  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWSubTile; };
+  auto s_ds = [&](int i) { return base + C::kOffDs + i * kWDs; };
+  auto s_vec = [&](int i) { return base + C::kOffVec + i * C::kVecBytes; };
+  const uint32_t bars = base + C::kOffBar;
+  const uint32_t bar_kv_full = bars;
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };           // slots (up to 4)
+  auto bar_empty = [&](int i) { return bars + 40u + 8u * i; };
+  auto bar_vec_full = [&](int i) { return bars + 72u + 8u * i; };
+  auto bar_vec_empty = [&](int i) { return bars + 88u + 8u * i; };
+  auto bar_s_full = [&](int i) { return bars + 104u + 8u * i; };
+  auto bar_dp_full = [&](int i) { return bars + 120u + 8u * i; };      // dK
+  auto bar_ready = [&](int i) { return bars + 136u + 8u * i; };        // P^T (dV) or dS^T (dK) written
+  const uint32_t bar_o_final = bars + 152, bar_stall = bars + 160;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 168);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 172);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: (key tile, batch * kv head); causal: small key tiles first
+  const int nkt = p.NKP / kBN;
+  const int jt = blockIdx.x / p.BHkv;
+  const int bhkv = blockIdx.x % p.BHkv;
+  const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int nq64 = p.NQP / kWSub;
+  // first 64-query sub-tile that sees key tile jt (bottom-right causal)
+  const int first_row = jt * kBN - p.causal_off;
+  const int s0 = p.causal ? (first_row <= 0 ? 0 : min(nq64, first_row / kWSub)) : 0;
+  const int per_head = nq64 - s0;
+  const int nsteps = (jt < nkt) ? G * per_head : 0;
+  auto step_head = [&](int s) { return b * p.Hq + hk * G + s / per_head; };
+  auto step_sub = [&](int s) { return s0 + s % per_head; };
+  // slot of step s's Q and dO
+  auto q_slot = [&](int s) { return kDV ? (s & 1) : (s & 1); };
+  auto do_slot = [&](int s) { return kDV ? 2 + (s & 1) : ((s + 1) & 1); };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_kv_full, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_vec_full(i), 1);
+      mbar_init(bar_vec_empty(i), 128);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_dp_full(i), 1);
+      mbar_init(bar_ready(i), 128);
+    }
+    mbar_init(bar_o_final, 1);
+    mbar_init(bar_stall, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_q64);
+      tma_prefetch_map(&map_do64);
+      mbar_arrive_expect_tx(bar_kv_full, kDV ? kWTile : 2 * kWTile);
+      for (int bx = 0; bx < kWD / 64; ++bx) {
+        tma_load_3d(s_k + bx * kBoxBytes, &map_k, bar_kv_full, bx * 64, jt * kBN, bhkv);
+        if (!kDV) tma_load_3d(s_v + bx * kBoxBytes, &map_v, bar_kv_full, bx * 64, jt * kBN, bhkv);
+      }
+      // per-slot use counts give the parity of each empty wait
+      int uses[4] = {0, 0, 0, 0};
+      auto load = [&](const CUtensorMap* m, int slot, int row0, int bh) -> bool {
+        if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
+        ++uses[slot];
+        mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
+        for (int bx = 0; bx < kWD / 64; ++bx)
+          tma_load_3d(s_slot(slot) + bx * kWSubBox, m, bar_full(slot), bx * 64, row0, bh);
+        return true;
+      };
+      for (int s = 0; s < nsteps; ++s) {
+        const int bh = step_head(s), row0 = step_sub(s) * kWSub;
+        if (!load(&map_q64, q_slot(s), row0, bh)) break;
+        const int vb = s & 1;
+        if (!mbar_wait(bar_vec_empty(vb), ((s >> 1) & 1) ^ 1, abort_flag, deadline)) break;
+        mbar_arrive_expect_tx(bar_vec_full(vb), 2 * kWSub * 4);
+        const size_t voff = static_cast<size_t>(bh) * p.NQP + row0;
+        bulk_load(s_vec(vb), p.ws_lse2 + voff, kWSub * 4, bar_vec_full(vb));
+        bulk_load(s_vec(vb) + kWSub * 4, p.ws_d + voff, kWSub * 4, bar_vec_full(vb));
+        if (!load(&map_do64, do_slot(s), row0, bh)) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int fulls[4] = {0, 0, 0, 0};     // phases of each slot's full barrier waited for so far
+      auto wait_full = [&](int slot) -> bool {
+        return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
+      };
+      bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
+      ok = ok && (nsteps == 0 || mbar_wait(bar_kv_full, 0, abort_flag, deadline));
+      auto scores = [&](int s) {       // S^T_s into buffer s & 1
+        issue_scores(tbase + kWColS + 64u * (s & 1), s_k, s_slot(q_slot(s)));
+        mma_commit(bar_s_full(s & 1));
+      };
+      auto dp = [&](int s) {           // dP^T_s into buffer s & 1; dO_s's slot is then free
+        issue_scores(tbase + kWColDP + 64u * (s & 1), s_v, s_slot(do_slot(s)));
+        mma_commit(bar_dp_full(s & 1));
+        mma_commit(bar_empty(do_slot(s)));
+      };
+      if (kDV) {
+        // S^T_{s+1} goes in as soon as Q_{s+1} lands (its buffer's P^T_{s-1}
+        // was read by dV_{s-1}, issued before); dV_s once P^T_s is written
+        if (ok && nsteps > 0) {
+          ok = wait_full(q_slot(0));
+          if (ok) { tc_fence_after(); scores(0); mma_commit(bar_empty(q_slot(0))); }
+        }
+        for (int s = 0; s < nsteps && ok; ++s) {
+          if (s + 1 < nsteps) {
+            if (!(ok = wait_full(q_slot(s + 1)))) break;
+            tc_fence_after();
+            scores(s + 1);
+            mma_commit(bar_empty(q_slot(s + 1)));
+          }
+          if (!(ok = mbar_wait(bar_ready(s & 1), (s >> 1) & 1, abort_flag, deadline))) break;
+          if (!(ok = wait_full(do_slot(s)))) break;
+          tc_fence_after();
+          issue_acc_ts(tbase + kWColAcc, tbase + kWColS + 64u * (s & 1), s_slot(do_slot(s)), s > 0);
+          mma_commit(bar_empty(do_slot(s)));
+        }
+      } else {
+        // order: S^T_0, dP^T_0, S^T_1; per step s: [dS^T_s] dK_s (Q_s's slot
+        // free after), [dO_{s+1}] dP^T_{s+1}, [Q_{s+2}] S^T_{s+2}
+        if (ok && nsteps > 0) {
+          ok = wait_full(q_slot(0));
+          if (ok) { tc_fence_after(); scores(0); }
+          ok = ok && wait_full(do_slot(0));
+          if (ok) { tc_fence_after(); dp(0); }
+          if (ok && nsteps > 1) {
+            ok = wait_full(q_slot(1));
+            if (ok) { tc_fence_after(); scores(1); }
+          }
+        }
+        for (int s = 0; s < nsteps && ok; ++s) {
+          if (!(ok = mbar_wait(bar_ready(s & 1), (s >> 1) & 1, abort_flag, deadline))) break;
+          tc_fence_after();
+          issue_acc_ss(tbase + kWColAcc, s_ds(s & 1), s_slot(q_slot(s)), s > 0);
+          mma_commit(bar_empty(q_slot(s)));
+          if (s + 1 < nsteps) {
+            if (!(ok = wait_full(do_slot(s + 1)))) break;
+            tc_fence_after();
+            dp(s + 1);
+          }
+          if (s + 2 < nsteps) {
+            if (!(ok = wait_full(q_slot(s + 2)))) break;
+            tc_fence_after();
+            scores(s + 2);
+          }
+        }
+      }
+      if (ok) mma_commit(bar_o_final);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ one thread per key row
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int key = jt * kBN + r;
+    const bool key_pad = key >= p.Nk;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int sb = s & 1;
+      const int q0 = step_sub(s) * kWSub;
+      ok = mbar_wait(bar_s_full(sb), (s >> 1) & 1, abort_flag, deadline) &&
+           mbar_wait(bar_vec_full(sb), (s >> 1) & 1, abort_flag, deadline);
+      if (!kDV) ok = ok && mbar_wait(bar_dp_full(sb), (s >> 1) & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base));
+      float x[64];
+      tmem_ld64(tbase + lane_off + kWColS + 64u * sb, x);
+      // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
+      const int lim = key - p.causal_off - q0;             // first visible query column
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float e = ex2_approx(fmaf(x[c], sl2, -vec[c]));
+        x[c] = (key_pad || (p.causal && c < lim)) ? 0.f : e;
+      }
+      if (kDV) {
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+        tmem_st_32x32b_x32(tbase + lane_off + kWColS + 64u * sb, pp);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_ready(sb));
+      } else {
+        float dpv[64];
+        tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - vec[kWSub + c]);
+        // dS^T buffer sb was last read by dK_{s-2}, which completed before S^T_s
+        store_row64(s_ds(sb), r, x);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_ready(sb));
+      }
+      mbar_arrive(bar_vec_empty(sb));
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) {
+      ok = mbar_wait(bar_o_final, 0, abort_flag, deadline);
+      if (nsteps == 0) ok = ok && mbar_wait(bar_kv_full, 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    // staging: the K tile (dV) or the V tile (dK), idle once every MMA has completed
+    const uint32_t stg = kDV ? s_k : s_v;
+    if (ok) {
+      tc_fence_after();
+      if (nsteps > 0) {
+        stage_acc_row(tbase + lane_off + kWColAcc, stg, r, kDV ? 1.0f : p.scale);
+      } else {
+#pragma unroll
+        for (int bx = 0; bx < kWD / 64; ++bx)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" :: "r"(swz128(stg + bx * kBoxBytes, r, u)), "r"(0u)
+                         : "memory");
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 128);
+    if (!*abort_flag && warp == 2 && lane == 0 && jt < nkt) {
+      for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_out, stg + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+      tma_store_commit();
+      tma_store_wait_all0();
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    abort_grace_period();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ dQ per query tile
+// Shared memory: Q | dO | two 32 KB slots (K_j, V_j alternating) | dS x2 | barriers.
+// K_j is read by S_j and dQ_j, V_j only by dP_j: K_{j+1} takes the slot V_j
+// leaves early, V_{j+1} the one K_j leaves at the end of step j.
+struct WideDqCfg {
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDo = kWTile;
+  static constexpr int kOffSlot = 2 * kWTile;
+  static constexpr int kOffDs = kOffSlot + 2 * kWSubTile;
+  static constexpr int kOffBar = kOffDs + 2 * kWDs;
+  static constexpr int kLayout = kOffBar + 256;
+  static constexpr int kSmemAlloc = kLayout + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(192, 1)
+wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k64,
+               const __grid_constant__ CUtensorMap map_v64, const __grid_constant__ CUtensorMap map_do,
+               const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
+  using C = WideDqCfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  if ((base - raw) + C::kLayout > static_cast<uint32_t>(C::kSmemAlloc)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
+    return;
+  }
+  const uint32_t s_q = base + C::kOffQ, s_do = base + C::kOffDo;
+  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWSubTile; };
+  auto s_ds = [&](int i) { return base + C::kOffDs + i * kWDs; };
+  const uint32_t bars = base + C::kOffBar;
+  const uint32_t bar_q_full = bars;
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };
+  auto bar_empty = [&](int i) { return bars + 24u + 8u * i; };
+  auto bar_s_full = [&](int i) { return bars + 40u + 8u * i; };
+  auto bar_dp_full = [&](int i) { return bars + 56u + 8u * i; };
+  auto bar_ready = [&](int i) { return bars + 72u + 8u * i; };
+  const uint32_t bar_o_final = bars + 88, bar_stall = bars + 96;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 104);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 108);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: (query tile, batch * head); causal: the longest rows first
+  const int nq = p.NQP / kBM;
+  const int qt = nq - 1 - static_cast<int>(blockIdx.x / p.BH);
+  const int bh = blockIdx.x % p.BH;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int nk64 = (p.Nk + kWSub - 1) / kWSub;
+  int nsteps = nk64;
+  if (p.causal) {
+    const int last = qt * kBM + kBM - 1 + p.causal_off;   // the tile's last row sees keys up to here
+    nsteps = last < 0 ? 0 : min(nk64, last / kWSub + 1);
+  }
+  auto k_slot = [&](int j) { return j & 1; };
+  auto v_slot = [&](int j) { return (j + 1) & 1; };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_dp_full(i), 1);
+      mbar_init(bar_ready(i), 128);
+    }
+    mbar_init(bar_o_final, 1);
+    mbar_init(bar_stall, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nsteps > 0) {
+      tma_prefetch_map(&map_k64);
+      tma_prefetch_map(&map_v64);
+      mbar_arrive_expect_tx(bar_q_full, 2 * kWTile);
+      for (int bx = 0; bx < kWD / 64; ++bx) {
+        tma_load_3d(s_q + bx * kBoxBytes, &map_q, bar_q_full, bx * 64, qt * kBM, bh);
+        tma_load_3d(s_do + bx * kBoxBytes, &map_do, bar_q_full, bx * 64, qt * kBM, bh);
+      }
+      int uses[2] = {0, 0};
+      auto load = [&](const CUtensorMap* m, int slot, int row0) -> bool {
+        if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
+        ++uses[slot];
+        mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
+        for (int bx = 0; bx < kWD / 64; ++bx)
+          tma_load_3d(s_slot(slot) + bx * kWSubBox, m, bar_full(slot), bx * 64, row0, bh_kv);
+        return true;
+      };
+      for (int j = 0; j < nsteps; ++j) {
+        if (!load(&map_k64, k_slot(j), j * kWSub)) break;
+        if (!load(&map_v64, v_slot(j), j * kWSub)) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int fulls[2] = {0, 0};
+      auto wait_full = [&](int slot) -> bool {
+        return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
+      };
+      bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
+      ok = ok && (nsteps == 0 || mbar_wait(bar_q_full, 0, abort_flag, deadline));
+      auto scores = [&](int j) {
+        issue_scores(tbase + kWColS + 64u * (j & 1), s_q, s_slot(k_slot(j)));
+        mma_commit(bar_s_full(j & 1));
+      };
+      auto dp = [&](int j) {
+        issue_scores(tbase + kWColDP + 64u * (j & 1), s_do, s_slot(v_slot(j)));
+        mma_commit(bar_dp_full(j & 1));
+        mma_commit(bar_empty(v_slot(j)));
+      };
+      if (ok && nsteps > 0) {
+        ok = wait_full(k_slot(0));
+        if (ok) { tc_fence_after(); scores(0); }
+        ok = ok && wait_full(v_slot(0));
+        if (ok) { tc_fence_after(); dp(0); }
+        if (ok && nsteps > 1) {
+          ok = wait_full(k_slot(1));
+          if (ok) { tc_fence_after(); scores(1); }
+        }
+      }
+      for (int j = 0; j < nsteps && ok; ++j) {
+        if (!(ok = mbar_wait(bar_ready(j & 1), (j >> 1) & 1, abort_flag, deadline))) break;
+        tc_fence_after();
+        issue_acc_ss(tbase + kWColAcc, s_ds(j & 1), s_slot(k_slot(j)), j > 0);
+        mma_commit(bar_empty(k_slot(j)));
+        if (j + 1 < nsteps) {
+          if (!(ok = wait_full(v_slot(j + 1)))) break;
+          tc_fence_after();
+          dp(j + 1);
+        }
+        if (j + 2 < nsteps) {
+          if (!(ok = wait_full(k_slot(j + 2)))) break;
+          tc_fence_after();
+          scores(j + 2);
+        }
+      }
+      if (ok) mma_commit(bar_o_final);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ one thread per query row
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int q = qt * kBM + r;
+    const float sl2 = p.scale_log2;
+    // this row's LSE log2(e) (+inf past N: P = 0) and D
+    const float lse2 = p.ws_lse2[static_cast<size_t>(bh) * p.NQP + qt * kBM + r];
+    const float dsub = p.ws_d[static_cast<size_t>(bh) * p.NQP + qt * kBM + r];
+    const int key_lim = p.causal ? min(p.Nk, q + p.causal_off + 1) : p.Nk;   // keys < key_lim are visible
+    bool ok = true;
+    for (int j = 0; j < nsteps && ok; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(bar_s_full(sb), (j >> 1) & 1, abort_flag, deadline) &&
+           mbar_wait(bar_dp_full(sb), (j >> 1) & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float x[64], dpv[64];
+      tmem_ld64(tbase + lane_off + kWColS + 64u * sb, x);
+      tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
+      const int lim = key_lim - j * kWSub;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float pe = ex2_approx(fmaf(x[c], sl2, -lse2));
+        x[c] = (c < lim) ? pe * (dpv[c] - dsub) : 0.f;
+      }
+      // dS buffer sb was last read by dQ_{j-2}, which completed before S_j
+      store_row64(s_ds(sb), r, x);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_ready(sb));
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) {
+      ok = mbar_wait(bar_o_final, 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      // staging: the Q tile, idle once every MMA has completed
+      if (nsteps > 0) {
+        stage_acc_row(tbase + lane_off + kWColAcc, s_q, r, p.scale);
+      } else {
+#pragma unroll
+        for (int bx = 0; bx < kWD / 64; ++bx)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" :: "r"(swz128(s_q + bx * kBoxBytes, r, u)), "r"(0u)
+                         : "memory");
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 128);
+    if (!*abort_flag && warp == 2 && lane == 0) {
+      for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_dq, s_q + bx * kBoxBytes, bx * 64, qt * kBM, bh);
+      tma_store_commit();
+      tma_store_wait_all0();
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    abort_grace_period();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ launch
+cudaError_t launch_bwd_wide(const BwdMaps& m, const BwdMaps& m64, const BwdParams& p, cudaStream_t stream) {
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([] {
+    cudaError_t r = cudaFuncSetAttribute(wide_kv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         WideKvCfg<true>::kSmemAlloc);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(wide_kv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               WideKvCfg<false>::kSmemAlloc);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(wide_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WideDqCfg::kSmemAlloc);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  const int kv_grid = (p.NKP / kBN) * p.BHkv;
+  const int q_grid = (p.NQP / kBM) * p.BH;
+  wide_kv_kernel<true><<<kv_grid, kWThreads, WideKvCfg<true>::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dv, p);
+  cudaError_t r = cudaGetLastError();
+  if (r != cudaSuccess) return r;
+  wide_kv_kernel<false><<<kv_grid, kWThreads, WideKvCfg<false>::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dk,
+                                                                                        p);
+  r = cudaGetLastError();
+  if (r != cudaSuccess) return r;
+  wide_dq_kernel<<<q_grid, kWThreads, WideDqCfg::kSmemAlloc, stream>>>(m.q, m64.k, m64.v, m.dO, m.dq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -111,6 +111,12 @@ cudaError_t launch_bwd_dkdv(int d, const BwdMaps& m, const BwdParams& p, cudaStr
 cudaError_t launch_bwd_blocklist(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, void* dq, const BwdParams& p, int num_sms, cudaStream_t stream);
 
+// Head dims 136..256 after launch_bwd_pre (a workspace with the LSE and D
+// parts only): the dV, dK and dQ passes, three launches on `stream`. m holds
+// maps with 128-row boxes (q, k, v, dO, dk, dv, dq), m64 maps with 64-row
+// boxes (q, dO, k, v) for the 64-row sub-tiles.
+cudaError_t launch_bwd_wide(const BwdMaps& m, const BwdMaps& m64, const BwdParams& p, cudaStream_t stream);
+
 // Deterministic backward after launch_bwd_pre: the dK/dV pass and the dQ pass
 // (two launches on `stream`); reads only the LSE and D parts of the workspace.
 cudaError_t launch_bwd_deterministic(int d, const BwdMaps& m, const BwdParams& p, cudaStream_t stream);

@@ -57,7 +57,6 @@ fa_status scratch_for_current_device(void** out) {
 extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                     const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
                                     int d, int causal, float scale, void* stream) {
-  if (d > 128 && d <= 256 && d % 8 == 0) return FA_ERR_UNSUPPORTED;   // no backward kernel above 128
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Hkv, N, d);
   if (need == 0) return FA_ERR_INVALID_ARG;
   if (need > kScratchBytes) return FA_ERR_WORKSPACE;

@@ -50,7 +50,8 @@ def test_workspace_size_formula(lib):
     assert lib.fa_bwd_workspace_bytes(2, 4, 2, 100, 64) == 4096 + 4096 + 8 * 100 * 64 * 4
     assert lib.fa_bwd_workspace_bytes(1, 3, 2, 128, 128) == 0      # Hq not a multiple of Hkv
     assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 100) == 0      # head dim not a multiple of 8
-    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 136) == 0      # head dim above 128
+    # above d = 128 the three-pass backward keeps no dQ accumulator: lse2 + D only
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 136) == 2 * 2 * 128 * 4
 
 
 def test_invalid_arguments_rejected_without_device(lib):
@@ -68,19 +69,26 @@ def test_invalid_arguments_rejected_without_device(lib):
 
 
 def test_head_dim_and_fp8_rules_without_device(lib):
-    """Head dims 8..256 for the forward, 8..128 for every backward, multiples
-    of 16 up to 256 for FP8: the host checks answer before any device work."""
+    """Head dims 8..256 for the forward and for fa_bwd, fa_bwd_kv,
+    fa_bwd_deterministic and fa_bwd_noalloc, 8..128 for the single backward
+    phases and the block-sparse backward, multiples of 16 up to 256 for FP8:
+    the host checks answer before any device work."""
     null = ctypes.c_void_p(0)
     fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
     assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 264, 0, 0.125, null) == 1    # past 256
     assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 128, 252, 0, 0.125, null) == 1    # not a multiple of 8
     args = [fake] * 9
-    # backward above 128: unsupported, before the workspace is looked at
-    assert lib.fa_bwd(*args, null, 0, 1, 1, 1, 128, 256, 1, 0.1, null) == 2
-    assert lib.fa_bwd_deterministic(*args, null, 0, 1, 1, 1, 128, 192, 1, 0.1, null) == 2
-    assert lib.fa_bwd_noalloc(*args, 1, 1, 1, 128, 136, 1, 0.1, null) == 2
-    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 256) == 0
+    # backward above 128: the three-pass path, which checks its workspace first
+    assert lib.fa_bwd(*args, null, 0, 1, 1, 1, 128, 256, 1, 0.1, null) == 6
+    assert lib.fa_bwd_deterministic(*args, null, 0, 1, 1, 1, 128, 192, 1, 0.1, null) == 6
+    assert lib.fa_bwd_kv(*args, null, 0, 1, 1, 1, 128, 300, 200, 1, 0.1, null) == 6
+    assert lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 256) == 2 * 2 * 128 * 4
+    # beyond the no-alloc scratch (32 MiB of LSE and D: 4 M rows) at d = 256
+    assert lib.fa_bwd_noalloc(*args, 1, 64, 64, 65536 + 128, 256, 1, 0.1, null) == 6
+    # the single phases and the block-sparse backward stop at 128
     assert lib.fa_bwd_blocksparse_workspace_bytes(1, 2, 2, 128, 192) == 0
+    assert lib.fa_bwd_preprocess(fake, fake, fake, fake, 1 << 30, 1, 1, 1, 128, 136, null) == 2
+    assert lib.fa_bwd_dkdv(*([fake] * 7), 1 << 30, 1, 1, 1, 128, 256, 1, 0.1, null) == 2
     # FP8: multiples of 16 up to 256; other multiples of 8 are valid arguments
     # but not built (a row of codes must be a multiple of 16 bytes for TMA)
     assert lib.fa_fwd_fp8(*([fake] * 8), 1, 1, 1, 128, 8, 0, 0.1, null) == 2

@@ -119,7 +119,8 @@ def test_bwd_workspace_checks(fa):
     need = fa.bwd_workspace_bytes(B, Hq, Hkv, N, d)
     nqp = 256
     assert need == 2 * B * Hq * nqp * 4 + B * Hq * N * d * 4
-    assert fa.bwd_workspace_bytes(B, Hq, Hkv, N, 100) == 0 and fa.bwd_workspace_bytes(B, Hq, Hkv, N, 136) == 0
+    assert fa.bwd_workspace_bytes(B, Hq, Hkv, N, 100) == 0
+    assert fa.bwd_workspace_bytes(B, Hq, Hkv, N, 136) == 2 * B * Hq * nqp * 4     # LSE and D only above 128
     dev = torch.device("cuda:0")
     x = torch.zeros(B, Hq, N, d, dtype=torch.bfloat16, device=dev)
     lse = torch.zeros(B, Hq, N, dtype=torch.float32, device=dev)
