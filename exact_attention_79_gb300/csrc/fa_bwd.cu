@@ -183,6 +183,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t bar_s_full = bars + 136, bar_dp_full = bars + 144, bar_p_ready = bars + 152;
   const uint32_t bar_ds_ready = bars + 160, bar_dq_full = bars + 168, bar_dq_free = bars + 176;
   const uint32_t bar_o_final = bars + 184;
+  const uint32_t bar_dk_done = bars + 216;                 // dK_i complete: Q_i may be overwritten
   const uint32_t bar_stall = bars + 208;                   // nothing arrives (timeout test)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 192);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 196);
@@ -237,6 +238,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 257);           // + the watcher: dO of the next step has landed
     mbar_init(bar_o_final, 1);
+    mbar_init(bar_dk_done, 1);
     mbar_init(bar_stall, 1);
     fence_mbar_init();
   }
@@ -286,10 +288,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issuer
-    // Step i: [P^T_i ready] dV, [dS^T_i ready] dK, dQ_i, then for step i+1:
-    // [Q_{i+1} landed] S^T, [dQ_i read out of TMEM, dO_{i+1} landed] dP^T.
-    // dQ goes into the dP^T columns; one thread's MMAs run in issue order,
-    // which keeps every TMEM reuse below safe.
+    // Step i: [P^T_i ready] dV, [dS^T_i ready] dQ_i then dK_i, then for step
+    // i+1: [Q_{i+1} landed] S^T, [dQ_i read out of TMEM, dO_{i+1} landed] dP^T.
+    // dQ_i goes first so that its read-out (on the softmax-gradient warps'
+    // critical path) overlaps dK_i; the group that stages over Q_i waits for
+    // dK_i, its last reader. dQ goes into the dP^T columns; one thread's MMAs
+    // run in issue order, which keeps every TMEM reuse below safe.
     if (lane == 0) {
       const uint32_t id_kk = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       const uint32_t id_kmn = make_idesc(1, 128, D, 0, 1);   // dV, dK: A K-major (or TMEM), B MN-major
@@ -343,6 +347,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         if (!mbar_wait(bar_ds_ready, step & 1, abort_flag, deadline)) { ok = false; break; }
         tc_fence_after();
+        // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys), into the dP^T columns
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tbase + C::kColDP, desc_add(ds_mn, kk * 16 * 128), desc_add(k_mn, kk * 16 * 128), id_mnmn, kk > 0);
+        mma_commit(bar_dq_full);
         // dK += dS^T Q  (A = dS^T K-major over queries)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -350,11 +359,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_bf16_ss(tbase + C::kColDK, desc_add(ds_kmaj, off), desc_add(qm, kk * 16 * 128), id_kmn,
                       step > 0 || kk > 0);
         }
-        // dQ_i = dS K  (M = queries: dS^T read MN-major; K = 128 keys), into the dP^T columns
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tbase + C::kColDP, desc_add(ds_mn, kk * 16 * 128), desc_add(k_mn, kk * 16 * 128), id_mnmn, kk > 0);
-        mma_commit(bar_dq_full);
+        mma_commit(bar_dk_done);
         if (step + 1 < nsteps) {
           const int sn = (step + 1) & 1;
           if (!mbar_wait(bar_q_full(sn), ((step + 1) >> 1) & 1, abort_flag, deadline)) { ok = false; break; }
@@ -535,6 +540,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(bar_dq_free);
+      // group 0 stages over Q_i, which dK_i (issued after dQ_i) still reads;
+      // group 1's region, dO_i, was last read by dV_i and dP^T_i, both done
+      if (g == 0) {
+        ok = mbar_wait(bar_dk_done, step & 1, abort_flag, deadline);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
       // fp32 boxes of 32 columns x 128 rows, 128-byte swizzle, each released
       // to the reducer as soon as this group has written it
       const uint32_t dst0 = g ? s_do(st) : s_q(st);

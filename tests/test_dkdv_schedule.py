@@ -5,10 +5,11 @@ the query tiles ("steps") of the heads that read it. Per step the tensor core
 computes S^T = K Q^T into TMEM, the softmax-gradient warps turn it into P^T
 in place, the tensor core runs dV += P^T dO, computes dP^T = V dO^T into a
 second TMEM region, the warps write dS^T to shared memory, the tensor core
-runs dK += dS^T Q and dQ = dS K into the dP^T columns, the warps read dQ
-out and stage its two fp32 halves over the step's own Q and dO regions (two
-stages of each), and a reducer warp adds them into global memory with TMA
-bulk reductions and hands each region back to the producer. A watcher folds
+runs dQ = dS K into the dP^T columns and then dK += dS^T Q, the warps read dQ
+out and stage its two fp32 halves over the step's own Q (once dK, its last
+reader, is done) and dO regions (two stages of each), and a reducer warp adds
+them into global memory with TMA bulk reductions and hands each region back
+to the producer. A watcher folds
 "dO of the next step landed" into the dQ-read-out barrier.
 
 As for the forward kernels, the roles run as coroutines with random
@@ -17,7 +18,7 @@ that every MMA and every warp reads the data of its own step, that no
 region, TMEM column group or the dS^T buffer is overwritten while a reader
 still needs it, and that no parity wait passes on an older phase. Planted
 changes show what the watcher's first wait, the issuer's wait for dQ to be
-read out and the reducer's wait for its reads guard.
+read out, the reducer's wait for its reads and group 0's wait for dK guard.
 """
 import heapq
 import random
@@ -30,7 +31,7 @@ GROUPS, WARPS_PER_GROUP, BOXES = 2, 4, 2
 
 
 def simulate(n, seed, *, watcher_first_wait=True, issuer_waits_dq_free=True, reducer_waits_reads=True,
-             warp_cycles=(200, 1500)):
+             group0_waits_dk=True, warp_cycles=(200, 1500)):
     """Errors seen in one run of n steps (query tiles) for one key tile."""
     rng = random.Random(seed)
     errors = []
@@ -45,6 +46,7 @@ def simulate(n, seed, *, watcher_first_wait=True, issuer_waits_dq_free=True, red
     dq_staged = {(g, st, bx): Barrier(WARPS_PER_GROUP) for g in range(GROUPS) for st in range(2)
                  for bx in range(BOXES)}
     s_full, dp_full, dq_full, o_final = Barrier(1), Barrier(1), Barrier(1), Barrier(1)
+    dk_done = Barrier(1)
     p_ready, ds_ready = Barrier(nthreads), Barrier(nthreads)
     dq_free = Barrier(nthreads + 1)               # + the watcher
 
@@ -168,7 +170,8 @@ def simulate(n, seed, *, watcher_first_wait=True, issuer_waits_dq_free=True, red
             yield from wait(p_ready, step & 1, "issuer p_ready", step)
             pipe.append(("dV", step))
             yield from wait(ds_ready, step & 1, "issuer ds_ready", step)
-            pipe.extend([("dK", step), ("dQ", step), ("commit", dq_full)])
+            # dQ first (its read-out is on the warps' critical path), then dK
+            pipe.extend([("dQ", step), ("commit", dq_full), ("dK", step), ("commit", dk_done)])
             if step + 1 < n:
                 sn = (step + 1) & 1
                 yield from wait(q_full[sn], ((step + 1) >> 1) & 1, "issuer q", (step + 1) >> 1)
@@ -246,16 +249,24 @@ def simulate(n, seed, *, watcher_first_wait=True, issuer_waits_dq_free=True, red
             ds_buf.setdefault(step, set()).add(me)
             ds_ready.arrive()
             yield from wait(dq_full, step & 1, f"warp {me} dq_full", step)
+            # the read-out itself takes time (TMEM loads, scheduling); dQ must
+            # still be there at its end
+            yield ("delay", rng.uniform(0, 3000) if rng.random() < 0.2 else rng.uniform(0, 200))
             if tmem_dp != ("dQ", step):
                 errors.append(f"warp {me} read dQ({step}) from TMEM holding {tmem_dp}")
             read_dq.setdefault(step, set()).add(me)
             dq_free.arrive()
+            if g == 0 and group0_waits_dk:
+                # Q_i is still read by dK_i, issued after dQ_i
+                yield from wait(dk_done, step & 1, f"warp {me} dk_done", step)
             # stage this group's dQ half over the step's own Q (g = 0) or dO (g = 1) region
             reg = q_reg if g == 0 else do_reg
             if reg[st] is None or reg[st][1] != step:
                 errors.append(f"warp {me} staged dQ({step}) over region {st} holding {reg[st]}")
-            if done["dK"] < step or done["dV"] < step:
-                errors.append(f"warp {me} staged dQ({step}) before dK / dV of the step read its region")
+            # the region's last MMA readers: S^T and dK read Q_i, dP^T and dV read dO_i
+            readers = ("S", "dK") if g == 0 else ("dP", "dV")
+            if any(done[k] < step for k in readers):
+                errors.append(f"warp {me} staged dQ({step}) before {readers} of the step read its region")
             for bx in range(BOXES):
                 yield ("delay", rng.uniform(20, 200))
                 staged.setdefault((g, st, bx, step), set()).add(me)
@@ -327,6 +338,12 @@ def test_reducer_must_wait_for_its_reads():
 def test_issuer_must_wait_for_dq_read_out():
     """dP^T of the next step goes into the columns dQ occupies."""
     assert bad_runs(issuer_waits_dq_free=False) > 0
+
+
+def test_group0_must_wait_for_dk_before_staging_over_q():
+    """dK_i runs after dQ_i and reads Q_i: staging dQ_i's first half over Q_i
+    before dK_i has completed would corrupt dK."""
+    assert bad_runs(group0_waits_dk=False) > 0
 
 
 def test_watcher_must_observe_the_first_do_load():
