@@ -1,7 +1,7 @@
 """Failure detection on the GPU without any fault: with FA_TEST_STALL=1 the
 tensor-core issuer (of the forward kernels: d <= 128, wide-head, FP8 at d = 128
-and 256; and of
-the backward's dK/dV pass) first waits on a barrier nothing arrives on, so its
+and 256; of the backward's dK/dV pass; and of the three passes of the
+backward above d = 128) first waits on a barrier nothing arrives on, so its
 bounded wait (FA_WAIT_LIMIT_MS, here 300 ms) runs out; every other role of
 the block sees the abort flag and unwinds, the block stores nothing and the
 call reports FA_ERR_TIMEOUT through fa_device_status. The next call on the
@@ -79,6 +79,22 @@ for name, call in (("wide", lambda: fa.fwd(gw["q"], gw["k"], gw["v"], causal=Tru
     assert lib.fa_device_status(stream) == 0, name
     ref = refs[name]
     assert torch.equal(again[0], ref[0]) and torch.equal(again[1], ref[1]), name
+# the backward above d = 128 (three passes, each issuer stalls) takes the same path
+tb = inputs.make_inputs(1, 2, 2, 300, 256, "bf16", seed=3, with_grad=True)
+gb = {n: x.to(dev) for n, x in tb.items()}
+os.environ["FA_TEST_STALL"] = "0"
+ob, lb = fa.fwd(gb["q"], gb["k"], gb["v"], causal=True)
+ref_b = fa.bwd(gb["q"], gb["k"], gb["v"], ob, lb, gb["do"], causal=True)
+assert lib.fa_device_status(stream) == 0
+os.environ["FA_TEST_STALL"] = "1"
+t0 = time.time()
+fa.bwd(gb["q"], gb["k"], gb["v"], ob, lb, gb["do"], causal=True)
+assert lib.fa_device_status(stream) == 5 and time.time() - t0 >= 0.25
+os.environ["FA_TEST_STALL"] = "0"
+again_b = fa.bwd(gb["q"], gb["k"], gb["v"], ob, lb, gb["do"], causal=True)
+assert lib.fa_device_status(stream) == 0
+assert all(torch.equal(x, y) for x, y in zip(again_b, ref_b))
+
 # status words are per stream: a stall on one stream is reported to that
 # stream only, while a call on another stream, overlapping it, reports FA_OK
 sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
