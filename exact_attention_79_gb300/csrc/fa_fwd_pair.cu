@@ -249,7 +249,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       };
       auto release = [&](int slot) {
         mbar_arrive(bar_kv_empty(slot));
-        mbar_arrive_remote(mapa_shared(bar_kv_empty(slot), peer));
+        // relaxed: the MMAs that read the slot have completed (S_L(j) observed)
+        mbar_arrive_remote_relaxed(mapa_shared(bar_kv_empty(slot), peer));
       };
       for (int j = 0; j < nmax && ok; ++j) {
         const int cv = 2 * j + 1;
@@ -273,7 +274,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       for (int i = 0; i < 2 && ok; ++i)
         if (nkv[i] > 0) ok = mbar_wait(bar_q_full(i), 0, abort_flag, deadline);
       if (ok && nmax > 0) ok = mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
-      if (ok && nmax > 0) mbar_arrive_remote(mapa_shared(bar_peer_start, peer));
+      if (ok && nmax > 0) mbar_arrive_remote_relaxed(mapa_shared(bar_peer_start, peer));   // loads observed landed
       for (int j = 0; j < nmax && ok; ++j) {
         const int cv = 2 * j + 1;
         ok = mbar_wait(bar_kv_full(cv % kPStages), (cv / kPStages) & 1, abort_flag, deadline);
@@ -286,7 +287,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           // S_i(j) done means the even CTA's P-ready(i) completed phase j - 1
           // (S_i(j) is issued after it), so this arrival counts for phase j
           ok = mbar_wait(bar_s_full(i), j & 1, abort_flag, deadline);
-          if (ok) mbar_arrive_remote(mapa_shared(bar_p_ready(i), peer));
+          if (ok) mbar_arrive_remote_relaxed(mapa_shared(bar_p_ready(i), peer));   // loads observed landed
         }
       }
     }
@@ -381,7 +382,10 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_arrive(bar_p_ready(g));
       } else {
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(p_ready_remote);   // for the warp's 32 rows
+        // for the warp's 32 rows; relaxed: tcgen05.wait::st above returned, so
+        // P is in TMEM before the arrival, and the P V that reads it is issued
+        // only after the phase completes (the release form cost 18% of the kernel)
+        if (lane == 0) mbar_arrive_remote_relaxed(p_ready_remote);
       }
     }
     // ---------------------------------------------------------- epilogue
