@@ -24,6 +24,8 @@
 // Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
 // (one thread), warps 2-5 one thread per TMEM lane (key row in the kv passes,
 // query row in the dQ pass).
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_kernels.h"
 
@@ -172,10 +174,14 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (key tile, batch * kv head); causal: small key tiles first
+  // ---- work item: (key tile, batch * kv head); causal: small key tiles first.
+  // KV heads go in groups of p.head_group whose Q and dO fit in part of L2.
   const int nkt = p.NKP / kBN;
-  const int jt = blockIdx.x / p.BHkv;
-  const int bhkv = blockIdx.x % p.BHkv;
+  const int grp = blockIdx.x / (nkt * p.head_group);
+  const int gsize = min(p.head_group, p.BHkv - grp * p.head_group);
+  const int local = blockIdx.x - grp * p.head_group * nkt;
+  const int jt = local / gsize;
+  const int bhkv = grp * p.head_group + local % gsize;
   const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int nq64 = p.NQP / kWSub;
@@ -290,17 +296,16 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
           mma_commit(bar_empty(do_slot(s)));
         }
       } else {
-        // order: S^T_0, dP^T_0, S^T_1; per step s: [dS^T_s] dK_s (Q_s's slot
-        // free after), [dO_{s+1}] dP^T_{s+1}, [Q_{s+2}] S^T_{s+2}
+        // order: S^T_0, dP^T_0; per step s: [dS^T_s] dK_s (Q_s's slot free
+        // after), [Q_{s+1}] S^T_{s+1}, [dO_{s+1}] dP^T_{s+1}. dO_{s+1} can only
+        // load once dK_s has freed its slot; S^T_{s+1} runs meanwhile. (S^T two
+        // steps ahead put a second such load, Q_{s+2} behind dP^T_{s+1}, on the
+        // issuer's path in every step.)
         if (ok && nsteps > 0) {
           ok = wait_full(q_slot(0));
           if (ok) { tc_fence_after(); scores(0); }
           ok = ok && wait_full(do_slot(0));
           if (ok) { tc_fence_after(); dp(0); }
-          if (ok && nsteps > 1) {
-            ok = wait_full(q_slot(1));
-            if (ok) { tc_fence_after(); scores(1); }
-          }
         }
         for (int s = 0; s < nsteps && ok; ++s) {
           if (!(ok = mbar_wait(bar_ready(s & 1), (s >> 1) & 1, abort_flag, deadline))) break;
@@ -308,14 +313,14 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
           issue_acc_ss(tbase + kWColAcc, s_ds(s & 1), s_slot(q_slot(s)), s > 0);
           mma_commit(bar_empty(q_slot(s)));
           if (s + 1 < nsteps) {
+            // buffers (s+1)&1 of S^T, dP^T and dS^T were last used by step s-1,
+            // whose warps' reads and dK (issued above) precede these products
+            if (!(ok = wait_full(q_slot(s + 1)))) break;
+            tc_fence_after();
+            scores(s + 1);
             if (!(ok = wait_full(do_slot(s + 1)))) break;
             tc_fence_after();
             dp(s + 1);
-          }
-          if (s + 2 < nsteps) {
-            if (!(ok = wait_full(q_slot(s + 2)))) break;
-            tc_fence_after();
-            scores(s + 2);
           }
         }
       }
@@ -336,7 +341,6 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
       const int q0 = step_sub(s) * kWSub;
       ok = mbar_wait(bar_s_full(sb), (s >> 1) & 1, abort_flag, deadline) &&
            mbar_wait(bar_vec_full(sb), (s >> 1) & 1, abort_flag, deadline);
-      if (!kDV) ok = ok && mbar_wait(bar_dp_full(sb), (s >> 1) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -359,6 +363,11 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
         tc_fence_before();
         mbar_arrive(bar_ready(sb));
       } else {
+        // dP^T_s only now: it may still wait for dO_s's load while P^T is formed
+        ok = mbar_wait(bar_dp_full(sb), (s >> 1) & 1, abort_flag, deadline);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
         float dpv[64];
         tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
 #pragma unroll
@@ -457,10 +466,14 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (query tile, batch * head); causal: the longest rows first
+  // ---- work item: (query tile, batch * head); causal: the longest rows first.
+  // Query heads go in groups of p.head_group whose K and V fit in part of L2.
   const int nq = p.NQP / kBM;
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x / p.BH);
-  const int bh = blockIdx.x % p.BH;
+  const int grp = blockIdx.x / (nq * p.head_group);
+  const int gsize = min(p.head_group, p.BH - grp * p.head_group);
+  const int local = blockIdx.x - grp * p.head_group * nq;
+  const int qt = nq - 1 - local / gsize;
+  const int bh = grp * p.head_group + local % gsize;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int nk64 = (p.Nk + kWSub - 1) / kWSub;
@@ -539,15 +552,14 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         mma_commit(bar_dp_full(j & 1));
         mma_commit(bar_empty(v_slot(j)));
       };
+      // order: S_0, dP_0; per step j: [dS_j] dQ_j (K_j's slot free after),
+      // [K_{j+1}] S_{j+1}, [V_{j+1}] dP_{j+1}: V_{j+1} loads once dQ_j has
+      // freed its slot, while S_{j+1} runs
       if (ok && nsteps > 0) {
         ok = wait_full(k_slot(0));
         if (ok) { tc_fence_after(); scores(0); }
         ok = ok && wait_full(v_slot(0));
         if (ok) { tc_fence_after(); dp(0); }
-        if (ok && nsteps > 1) {
-          ok = wait_full(k_slot(1));
-          if (ok) { tc_fence_after(); scores(1); }
-        }
       }
       for (int j = 0; j < nsteps && ok; ++j) {
         if (!(ok = mbar_wait(bar_ready(j & 1), (j >> 1) & 1, abort_flag, deadline))) break;
@@ -555,14 +567,14 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         issue_acc_ss(tbase + kWColAcc, s_ds(j & 1), s_slot(k_slot(j)), j > 0);
         mma_commit(bar_empty(k_slot(j)));
         if (j + 1 < nsteps) {
+          // buffers (j+1)&1 of S, dP and dS were last used by step j-1, whose
+          // warps' reads and dQ (issued above) precede these products
+          if (!(ok = wait_full(k_slot(j + 1)))) break;
+          tc_fence_after();
+          scores(j + 1);
           if (!(ok = wait_full(v_slot(j + 1)))) break;
           tc_fence_after();
           dp(j + 1);
-        }
-        if (j + 2 < nsteps) {
-          if (!(ok = wait_full(k_slot(j + 2)))) break;
-          tc_fence_after();
-          scores(j + 2);
         }
       }
       if (ok) mma_commit(bar_o_final);
@@ -582,20 +594,26 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     bool ok = true;
     for (int j = 0; j < nsteps && ok; ++j) {
       const int sb = j & 1;
-      ok = mbar_wait(bar_s_full(sb), (j >> 1) & 1, abort_flag, deadline) &&
-           mbar_wait(bar_dp_full(sb), (j >> 1) & 1, abort_flag, deadline);
+      // P from S first: dP_j may still wait for V_j's load
+      ok = mbar_wait(bar_s_full(sb), (j >> 1) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       float x[64], dpv[64];
       tmem_ld64(tbase + lane_off + kWColS + 64u * sb, x);
-      tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
       const int lim = key_lim - j * kWSub;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float pe = ex2_approx(fmaf(x[c], sl2, -lse2));
-        x[c] = (c < lim) ? pe * (dpv[c] - dsub) : 0.f;
+        x[c] = (c < lim) ? pe : 0.f;
       }
+      ok = mbar_wait(bar_dp_full(sb), (j >> 1) & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - dsub);
       // dS buffer sb was last read by dQ_{j-2}, which completed before S_j
       store_row64(s_ds(sb), r, x);
       fence_proxy_async_smem();
@@ -657,14 +675,22 @@ cudaError_t launch_bwd_wide(const BwdMaps& m, const BwdMaps& m64, const BwdParam
   if (e != cudaSuccess) return e;
   const int kv_grid = (p.NKP / kBN) * p.BHkv;
   const int q_grid = (p.NQP / kBM) * p.BH;
-  wide_kv_kernel<true><<<kv_grid, kWThreads, WideKvCfg<true>::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dv, p);
+  // head groups whose streamed operands (bf16) fit in 64 MB, half of L2: the kv
+  // passes stream the Q and dO of a KV head's G query heads, the dQ pass the K
+  // and V of a query head's KV head (shared by its G siblings, kept adjacent)
+  const long long G = p.Hq / p.Hkv;
+  const long long budget = 64LL << 20;
+  BwdParams pk = p, pq = p;
+  pk.head_group = static_cast<int>(std::max(1LL, std::min<long long>(p.BHkv, budget / (4LL * G * p.N * kWD))));
+  pq.head_group = static_cast<int>(std::max(1LL, std::min<long long>(p.BH, budget * G / (4LL * p.Nk * kWD))));
+  wide_kv_kernel<true><<<kv_grid, kWThreads, WideKvCfg<true>::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dv, pk);
   cudaError_t r = cudaGetLastError();
   if (r != cudaSuccess) return r;
   wide_kv_kernel<false><<<kv_grid, kWThreads, WideKvCfg<false>::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dk,
-                                                                                        p);
+                                                                                        pk);
   r = cudaGetLastError();
   if (r != cudaSuccess) return r;
-  wide_dq_kernel<<<q_grid, kWThreads, WideDqCfg::kSmemAlloc, stream>>>(m.q, m64.k, m64.v, m.dO, m.dq, p);
+  wide_dq_kernel<<<q_grid, kWThreads, WideDqCfg::kSmemAlloc, stream>>>(m.q, m64.k, m64.v, m.dO, m.dq, pq);
   return cudaGetLastError();
 }
 
