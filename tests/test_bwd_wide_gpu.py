@@ -91,6 +91,31 @@ def test_wide_backward_full_size_sampled_rows(fa):
     assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
 
 
+def test_wide_backward_ragged_head_groups(fa):
+    """3 heads at N = 24576, d = 256, causal: the passes walk heads in groups
+    whose streamed operands fit in 64 MB of L2, here groups of 2 and 1 in
+    every pass. 128 seeded query rows (dQ) and 128 key rows (dK, dV) per head
+    against the oracle."""
+    B, H, N, d = 1, 3, 24576, 256
+    scale = d ** -0.5
+    t = inputs.make_inputs(B, H, H, N, d, "bf16", seed=8257, with_grad=True)
+    g = {n: x.to(DEV) for n, x in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=True, scale=scale)
+    dq, dk, dv = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=scale)
+    fa.check_device_status()
+    f = {n: inputs.to_f64(x) for n, x in t.items()}
+    qr = inputs.sample_rows(B, H, N, 128, seed=3)
+    kr = inputs.sample_rows(B, H, N, 128, seed=4)
+    rl, rD = oracle.row_statistics(f["q"], f["k"], f["v"], f["do"], True, scale)
+    rdq, rdk, rdv = oracle.backward_rows(f["q"], f["k"], f["v"], f["do"], True, scale, qr, kr, rl, rD)
+    bi, hi = np.arange(B)[:, None, None], np.arange(H)[None, :, None]
+    dq, dk, dv = (x.float().cpu().numpy() for x in (dq, dk, dv))
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+    errs = {"dq": rel_fro(dq[bi, hi, qr], rdq), "dk": rel_fro(dk[bi, hi, kr], rdk), "dv": rel_fro(dv[bi, hi, kr], rdv)}
+    print(errs)
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+
+
 def test_wide_backward_noalloc_matches_fa_bwd(fa):
     lib = fa.load()
     B, Hq, Hkv, N, d = 1, 4, 2, 600, 256
