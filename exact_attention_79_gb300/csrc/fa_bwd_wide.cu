@@ -426,11 +426,13 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
 // K_j is read by S_j and dQ_j, V_j only by dP_j: K_{j+1} takes the slot V_j
 // leaves early, V_{j+1} the one K_j leaves at the end of step j.
 struct WideDqCfg {
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffDo = kWTile;
-  static constexpr int kOffSlot = 2 * kWTile;
-  static constexpr int kOffDs = kOffSlot + 2 * kWSubTile;
+  static constexpr int kSlots = 4;
+  static constexpr int kOffDo = 0;
+  static constexpr int kOffSlot = kWTile;              // slots 0-1 first hold the Q tile
+  static constexpr int kOffDs = kOffSlot + kSlots * kWSubTile;
   static constexpr int kOffBar = kOffDs + 2 * kWDs;
+  // TMEM: dQ accumulator | S | dP | Q as the A operand of S (two bf16 per column)
+  static constexpr uint32_t kColS = 256, kColDP = 320, kColQ = 384;
   static constexpr int kLayout = kOffBar + 256;
   static constexpr int kSmemAlloc = kLayout + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -449,19 +451,19 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
   }
-  const uint32_t s_q = base + C::kOffQ, s_do = base + C::kOffDo;
+  const uint32_t s_do = base + C::kOffDo;
   auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWSubTile; };
+  const uint32_t s_q = s_slot(0);                      // the Q tile, then the dQ staging
   auto s_ds = [&](int i) { return base + C::kOffDs + i * kWDs; };
   const uint32_t bars = base + C::kOffBar;
-  const uint32_t bar_q_full = bars;
-  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };
-  auto bar_empty = [&](int i) { return bars + 24u + 8u * i; };
-  auto bar_s_full = [&](int i) { return bars + 40u + 8u * i; };
-  auto bar_dp_full = [&](int i) { return bars + 56u + 8u * i; };
-  auto bar_ready = [&](int i) { return bars + 72u + 8u * i; };
-  const uint32_t bar_o_final = bars + 88, bar_stall = bars + 96;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 104);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 108);
+  const uint32_t bar_q_full = bars;                    // Q and dO landed
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };     // slots 0..3
+  auto bar_empty = [&](int i) { return bars + 40u + 8u * i; };
+  const uint32_t bar_s_full = bars + 72, bar_dp_full = bars + 80, bar_ready = bars + 88;
+  const uint32_t bar_o_final = bars + 96, bar_stall = bars + 104;
+  const uint32_t bar_q_tmem = bars + 112;              // every row of Q copied into TMEM
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 120);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 124);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -482,19 +484,22 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int last = qt * kBM + kBM - 1 + p.causal_off;   // the tile's last row sees keys up to here
     nsteps = last < 0 ? 0 : min(nk64, last / kWSub + 1);
   }
-  auto k_slot = [&](int j) { return j & 1; };
-  auto v_slot = [&](int j) { return (j + 1) & 1; };
+  // ring of four slots: K_j and V_j are items 2j and 2j+1, in slot (item + 2) % 4,
+  // so the first two go to slots 2 and 3 while Q still occupies slots 0 and 1
+  auto k_slot = [&](int j) { return (2 * j + 2) & 3; };
+  auto v_slot = [&](int j) { return (2 * j + 3) & 3; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar_q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
-      mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_dp_full(i), 1);
-      mbar_init(bar_ready(i), 128);
     }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_dp_full, 1);
+    mbar_init(bar_ready, 128);
+    mbar_init(bar_q_tmem, 128);
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
     fence_mbar_init();
@@ -519,8 +524,10 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         tma_load_3d(s_q + bx * kBoxBytes, &map_q, bar_q_full, bx * 64, qt * kBM, bh);
         tma_load_3d(s_do + bx * kBoxBytes, &map_do, bar_q_full, bx * 64, qt * kBM, bh);
       }
-      int uses[2] = {0, 0};
+      int uses[C::kSlots] = {0, 0, 0, 0};
       auto load = [&](const CUtensorMap* m, int slot, int row0) -> bool {
+        // slots 0 and 1 take K/V only once every row of Q is in TMEM
+        if (slot < 2 && uses[slot] == 0 && !mbar_wait(bar_q_tmem, 0, abort_flag, deadline)) return false;
         if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
         ++uses[slot];
         mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
@@ -537,24 +544,34 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int fulls[2] = {0, 0};
+      int fulls[C::kSlots] = {0, 0, 0, 0};
       auto wait_full = [&](int slot) -> bool {
         return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
       };
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
-      ok = ok && (nsteps == 0 || mbar_wait(bar_q_full, 0, abort_flag, deadline));
-      auto scores = [&](int j) {
-        issue_scores(tbase + kWColS + 64u * (j & 1), s_q, s_slot(k_slot(j)));
-        mma_commit(bar_s_full(j & 1));
+      ok = ok && (nsteps == 0 || (mbar_wait(bar_q_full, 0, abort_flag, deadline) &&
+                                  mbar_wait(bar_q_tmem, 0, abort_flag, deadline)));
+      auto scores = [&](int j) {     // S_j = Q K_j^T with Q from TMEM
+        const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
+        const uint64_t bd = smem_desc_sw128(s_slot(k_slot(j)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kWD / 16; ++kk) {
+          const uint32_t kb = kk * 32;
+          mma_bf16_ts(tbase + C::kColS, tbase + C::kColQ + kk * 8, desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id,
+                      kk > 0);
+        }
+        mma_commit(bar_s_full);
       };
       auto dp = [&](int j) {
-        issue_scores(tbase + kWColDP + 64u * (j & 1), s_do, s_slot(v_slot(j)));
-        mma_commit(bar_dp_full(j & 1));
+        issue_scores(tbase + C::kColDP, s_do, s_slot(v_slot(j)));
+        mma_commit(bar_dp_full);
         mma_commit(bar_empty(v_slot(j)));
       };
       // order: S_0, dP_0; per step j: [dS_j] dQ_j (K_j's slot free after),
-      // [K_{j+1}] S_{j+1}, [V_{j+1}] dP_{j+1}: V_{j+1} loads once dQ_j has
-      // freed its slot, while S_{j+1} runs
+      // [K_{j+1}] S_{j+1}, [V_{j+1}] dP_{j+1}. S and dP have one TMEM buffer
+      // each: step j+1's are issued only after the warps' read of step j's
+      // (the dS_j they waited for). With four slots K_{j+2} and V_{j+2} load
+      // while step j+1 runs.
       if (ok && nsteps > 0) {
         ok = wait_full(k_slot(0));
         if (ok) { tc_fence_after(); scores(0); }
@@ -562,13 +579,12 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         if (ok) { tc_fence_after(); dp(0); }
       }
       for (int j = 0; j < nsteps && ok; ++j) {
-        if (!(ok = mbar_wait(bar_ready(j & 1), (j >> 1) & 1, abort_flag, deadline))) break;
+        if (!(ok = mbar_wait(bar_ready, j & 1, abort_flag, deadline))) break;
         tc_fence_after();
         issue_acc_ss(tbase + kWColAcc, s_ds(j & 1), s_slot(k_slot(j)), j > 0);
         mma_commit(bar_empty(k_slot(j)));
         if (j + 1 < nsteps) {
-          // buffers (j+1)&1 of S, dP and dS were last used by step j-1, whose
-          // warps' reads and dQ (issued above) precede these products
+          // dS buffer (j+1)&1 was last read by dQ_{j-1}, issued before these products
           if (!(ok = wait_full(k_slot(j + 1)))) break;
           tc_fence_after();
           scores(j + 1);
@@ -592,33 +608,55 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const float dsub = p.ws_d[static_cast<size_t>(bh) * p.NQP + qt * kBM + r];
     const int key_lim = p.causal ? min(p.Nk, q + p.causal_off + 1) : p.Nk;   // keys < key_lim are visible
     bool ok = true;
+    if (nsteps > 0) {
+      // this row of Q into TMEM as the A operand of S: 128 columns of bf16
+      // pairs, the lower dimension in the low half (the tile's 16-byte units
+      // in order), then slots 0 and 1 are free for K and V
+      ok = mbar_wait(bar_q_full, 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+#pragma unroll
+        for (int bx = 0; bx < kWD / 64; ++bx) {
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[4 * u]), "=r"(w[4 * u + 1]), "=r"(w[4 * u + 2]), "=r"(w[4 * u + 3])
+                         : "r"(swz128(s_q + bx * kBoxBytes, r, u)));
+          tmem_st_32x32b_x32(tbase + lane_off + C::kColQ + 32u * bx, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_q_tmem);
+      }
+    }
     for (int j = 0; j < nsteps && ok; ++j) {
       const int sb = j & 1;
       // P from S first: dP_j may still wait for V_j's load
-      ok = mbar_wait(bar_s_full(sb), (j >> 1) & 1, abort_flag, deadline);
+      ok = mbar_wait(bar_s_full, j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       float x[64], dpv[64];
-      tmem_ld64(tbase + lane_off + kWColS + 64u * sb, x);
+      tmem_ld64(tbase + lane_off + C::kColS, x);
       const int lim = key_lim - j * kWSub;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float pe = ex2_approx(fmaf(x[c], sl2, -lse2));
         x[c] = (c < lim) ? pe : 0.f;
       }
-      ok = mbar_wait(bar_dp_full(sb), (j >> 1) & 1, abort_flag, deadline);
+      ok = mbar_wait(bar_dp_full, j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
+      tmem_ld64(tbase + lane_off + C::kColDP, dpv);
 #pragma unroll
       for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - dsub);
       // dS buffer sb was last read by dQ_{j-2}, which completed before S_j
       store_row64(s_ds(sb), r, x);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_ready(sb));
+      mbar_arrive(bar_ready);
     }
     // ---------------------------------------------------------- epilogue
     if (ok) {

@@ -8,16 +8,21 @@ V_s), read only by dP_s. A_s lands in slot s & 1 and B_s in slot (s + 1) & 1,
 so a slot holds A_s, then B_{s+1}, then A_{s+2}. One thread issues S_0, dP_0,
 then per step: [dS_s written] the accumulate, which frees A_s's slot once it
 completes; [A_{s+1} landed] S_{s+1}; [B_{s+1} landed] dP_{s+1}, which frees
-B's slot. S, dP (TMEM) and dS (shared memory) are double-buffered by step
-parity; the dK pass also double-buffers the step's LSE and D. Four warps, one
-per TMEM lane quarter, form P from S, wait for dP, and write dS.
+B's slot. dS (shared memory) is double-buffered by step parity. The dK pass
+also double-buffers S, dP (TMEM) and the step's LSE and D. The dQ pass keeps
+Q in TMEM as the A operand of S instead of in shared memory: Q lands in slots
+0 and 1, every warp copies its rows, and only then do those slots join a ring
+of four (K_j and V_j in slots (2j + 2) % 4 and (2j + 3) % 4); S and dP have
+one TMEM buffer each. Four warps, one per TMEM lane quarter, form P from S,
+wait for dP, and write dS.
 
 As for the other kernels, the roles run as coroutines with random latencies
 over barriers with the hardware's parity rule. The model checks that every
 product and every warp reads the data of its own step, that no slot, TMEM
 buffer, dS buffer or vector buffer is overwritten while a reader still needs
 it, and that no parity wait passes on an older phase. Planted changes show
-what the accumulate's release of A's slot and the warps' wait for dP guard;
+what the accumulate's release of A's slot, the warps' wait for dP and the
+producer's wait for the Q copy guard;
 the vector buffer's release point turns out to be implied by the slot order.
 """
 import heapq
@@ -31,23 +36,29 @@ WARPS = 4
 
 
 def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=True, vec_release_last=True,
-             warp_cycles=(100, 1500)):
-    """Errors seen in one run of n steps of one CTA."""
+             producer_waits_q_copy=True, warp_cycles=(100, 1500)):
+    """Errors seen in one run of n steps of one CTA. The dQ pass (dk_pass
+    False) holds Q in TMEM: four slots, the first two holding the Q tile until
+    every warp has copied its row, and one TMEM buffer each for S and dP."""
     rng = random.Random(seed)
     errors = []
-    full = [Barrier(1), Barrier(1)]
-    empty = [Barrier(1), Barrier(1)]
-    s_full = [Barrier(1), Barrier(1)]
-    dp_full = [Barrier(1), Barrier(1)]
-    ready = [Barrier(WARPS), Barrier(WARPS)]
+    nslots = 2 if dk_pass else 4
+    nbuf = 2 if dk_pass else 1          # TMEM buffers of S and of dP
+    full = [Barrier(1) for _ in range(nslots)]
+    empty = [Barrier(1) for _ in range(nslots)]
+    s_full = [Barrier(1) for _ in range(nbuf)]
+    dp_full = [Barrier(1) for _ in range(nbuf)]
+    ready = [Barrier(WARPS) for _ in range(nbuf)]
+    q_full, q_tmem = Barrier(1), Barrier(WARPS)
+    copied = set()
     vec_full = [Barrier(1), Barrier(1)]
     vec_empty = [Barrier(WARPS), Barrier(WARPS)]
     o_final = Barrier(1)
 
-    slot = [None, None]              # ("A" | "B", step); None while a load is in flight
-    inflight = [False, False]
+    slot = [None] * nslots           # ("A" | "B", step) or ("Q",); None while a load is in flight
+    inflight = [False] * nslots
     vec = [None, None]
-    s_buf, dp_buf = [None, None], [None, None]   # step whose S / dP the buffer holds
+    s_buf, dp_buf = [None] * nbuf, [None] * nbuf   # step whose S / dP the buffer holds
     read_s, read_dp = {}, {}                      # step -> warps that read it
     ds_buf = [None, None]                         # (step, set of warps that wrote it)
     done = {"S": -1, "dP": -1, "acc": -1}
@@ -56,10 +67,13 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
     events = []
 
     def a_slot(s):
-        return s & 1
+        return s & 1 if dk_pass else (2 * s + 2) & 3
 
     def b_slot(s):
-        return (s + 1) & 1
+        return (s + 1) & 1 if dk_pass else (2 * s + 3) & 3
+
+    def buf(s):
+        return s % nbuf
 
     def wait(bar, parity, who, phase=None):
         yield ("wait", lambda: bar.passes(parity))
@@ -83,13 +97,15 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             if kind == "S":
                 if slot[a_slot(s)] != ("A", s):
                     errors.append(f"S({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
-                if s >= 2 and len(read_s.get(s - 2, ())) < WARPS:
-                    errors.append(f"S({s}) overwrote S({s - 2}) before every warp read it")
+                if not dk_pass and len(copied) < WARPS:
+                    errors.append(f"S({s}) read Q from TMEM before every warp copied its rows")
+                if s >= nbuf and len(read_s.get(s - nbuf, ())) < WARPS:
+                    errors.append(f"S({s}) overwrote S({s - nbuf}) before every warp read it")
             elif kind == "dP":
                 if slot[b_slot(s)] != ("B", s):
                     errors.append(f"dP({s}) read slot {b_slot(s)} holding {slot[b_slot(s)]}")
-                if s >= 2 and len(read_dp.get(s - 2, ())) < WARPS:
-                    errors.append(f"dP({s}) overwrote dP({s - 2}) before every warp read it")
+                if s >= nbuf and len(read_dp.get(s - nbuf, ())) < WARPS:
+                    errors.append(f"dP({s}) overwrote dP({s - nbuf}) before every warp read it")
             elif kind == "acc":
                 if ds_buf[x] is None or ds_buf[x][0] != s or len(ds_buf[x][1]) < WARPS:
                     errors.append(f"accumulate({s}) read dS buffer {x} holding {ds_buf[x]}")
@@ -98,13 +114,13 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 errors.append(f"accumulate({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
             done[kind] = s
             if kind == "S":
-                s_buf[x] = s
+                s_buf[buf(s)] = s
             elif kind == "dP":
-                dp_buf[x] = s
+                dp_buf[buf(s)] = s
 
     # ------------------------------------------------------------ producer
     def producer():
-        uses = [0, 0]
+        uses = [0] * nslots
 
         def land(i, what):
             def f():
@@ -118,7 +134,19 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 vec_full[x].complete_tx(1)
             return f
 
+        def land_q():
+            slot[0] = slot[1] = ("Q",)
+            q_full.complete_tx(1)
+
+        if not dk_pass and n > 0:
+            # the Q tile (and dO, resident) into slots 0 and 1
+            q_full.expect_tx(1)
+            q_full.arrive()
+            later(rng.uniform(300, 4000), land_q)
+
         def load(i, what):
+            if not dk_pass and i < 2 and uses[i] == 0 and producer_waits_q_copy:
+                yield from wait(q_tmem, 0, "producer q_tmem", 0)
             yield from wait(empty[i], (uses[i] & 1) ^ 1, "producer empty")
             uses[i] += 1
             if inflight[i]:
@@ -141,7 +169,7 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
 
     # ------------------------------------------------------------ issuer
     def issuer():
-        fulls = [0, 0]
+        fulls = [0] * nslots
 
         def wait_full(i):
             par = fulls[i] & 1
@@ -151,6 +179,9 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
         if n == 0:
             pipe.append(("commit", o_final))
             return
+        if not dk_pass:
+            yield from wait(q_full, 0, "issuer q_full", 0)
+            yield from wait(q_tmem, 0, "issuer q_tmem", 0)
         yield from wait_full(a_slot(0))
         pipe.extend([("S", 0), ("commit", s_full[0])])
         if not release_a_after_acc:
@@ -158,12 +189,12 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
         yield from wait_full(b_slot(0))
         pipe.extend([("dP", 0), ("commit", dp_full[0]), ("commit", empty[b_slot(0)])])
         for s in range(n):
-            yield from wait(ready[s & 1], (s >> 1) & 1, "issuer ready", s >> 1)
+            yield from wait(ready[buf(s)], (s // nbuf) & 1, "issuer ready", s // nbuf)
             pipe.append(("acc", s))
             if release_a_after_acc:
                 pipe.append(("commit", empty[a_slot(s)]))
             if s + 1 < n:
-                x = (s + 1) & 1
+                x = buf(s + 1)
                 yield from wait_full(a_slot(s + 1))
                 pipe.extend([("S", s + 1), ("commit", s_full[x])])
                 if not release_a_after_acc:
@@ -174,37 +205,44 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
 
     # ------------------------------------------------------------ warps
     def warp_role(w):
+        if not dk_pass and n > 0:
+            yield from wait(q_full, 0, f"warp {w} q_full", 0)
+            yield ("delay", rng.uniform(50, 600))          # its rows of Q into TMEM
+            if slot[0] != ("Q",) or slot[1] != ("Q",):
+                errors.append(f"warp {w} copied Q from slots holding {slot[0]}, {slot[1]}")
+            copied.add(w)
+            q_tmem.arrive()
         for s in range(n):
-            x = s & 1
-            yield from wait(s_full[x], (s >> 1) & 1, f"warp {w} s_full", s >> 1)
+            x, v = buf(s), s & 1
+            yield from wait(s_full[x], (s // nbuf) & 1, f"warp {w} s_full", s // nbuf)
             if dk_pass:
-                yield from wait(vec_full[x], (s >> 1) & 1, f"warp {w} vec_full", s >> 1)
-                if vec[x] != s:
-                    errors.append(f"warp {w} read LSE of step {s} from buffer {x} holding {vec[x]}")
+                yield from wait(vec_full[v], (s >> 1) & 1, f"warp {w} vec_full", s >> 1)
+                if vec[v] != s:
+                    errors.append(f"warp {w} read LSE of step {s} from buffer {v} holding {vec[v]}")
             if s_buf[x] != s:
                 errors.append(f"warp {w} read S({s}) from buffer {x} holding {s_buf[x]}")
             read_s.setdefault(s, set()).add(w)
             yield ("delay", rng.uniform(*warp_cycles))          # P from S
             if warps_wait_dp:
-                yield from wait(dp_full[x], (s >> 1) & 1, f"warp {w} dp_full", s >> 1)
+                yield from wait(dp_full[x], (s // nbuf) & 1, f"warp {w} dp_full", s // nbuf)
             if dp_buf[x] != s:
                 errors.append(f"warp {w} read dP({s}) from buffer {x} holding {dp_buf[x]}")
             read_dp.setdefault(s, set()).add(w)
             if dk_pass and not vec_release_last:
-                vec_empty[x].arrive()
+                vec_empty[v].arrive()
                 yield ("delay", rng.uniform(0, 400))
-            if dk_pass and vec[x] != s:
-                errors.append(f"warp {w} read D of step {s} from buffer {x} holding {vec[x]}")
-            # dS buffer x was last read by the accumulate of step s - 2
+            if dk_pass and vec[v] != s:
+                errors.append(f"warp {w} read D of step {s} from buffer {v} holding {vec[v]}")
+            # dS buffer v was last read by the accumulate of step s - 2
             if s >= 2 and done["acc"] < s - 2:
                 errors.append(f"warp {w} wrote dS({s}) before the accumulate of step {s - 2} read the buffer")
             yield ("delay", rng.uniform(*warp_cycles))
-            if ds_buf[x] is None or ds_buf[x][0] != s:
-                ds_buf[x] = (s, set())
-            ds_buf[x][1].add(w)
+            if ds_buf[v] is None or ds_buf[v][0] != s:
+                ds_buf[v] = (s, set())
+            ds_buf[v][1].add(w)
             ready[x].arrive()
             if dk_pass and vec_release_last:
-                vec_empty[x].arrive()
+                vec_empty[v].arrive()
         yield from wait(o_final, 0, f"warp {w} o_final", 0)
 
     roles = [tensor_core(), producer(), issuer()] + [warp_role(w) for w in range(WARPS)]
@@ -269,6 +307,13 @@ def test_a_slot_must_wait_for_the_accumulate(dk_pass):
 def test_warps_must_wait_for_dp(dk_pass):
     """P is formed before dP arrives; the dP read still needs its own wait."""
     assert bad_runs(dk_pass, warps_wait_dp=False) > 0
+
+
+def test_dq_pass_slots_0_1_must_wait_for_the_q_copy():
+    """In the dQ pass Q lands in slots 0 and 1 and each warp copies its rows
+    into TMEM; a K or V load into those slots before every warp has copied
+    would overwrite Q under a warp still reading it."""
+    assert bad_runs(False, producer_waits_q_copy=False) > 0
 
 
 def test_vector_release_is_implied_by_the_slot_order():
