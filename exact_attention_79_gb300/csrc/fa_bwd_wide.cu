@@ -121,16 +121,17 @@ __device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int 
 
 // ------------------------------------------------------------------ dV (kDV) or dK per key tile
 // Shared memory: K | (dK: V) | two 32 KB sub-tile slots | (dK: dS^T x2) | LSE, D x2 | barriers.
-// dV: Q_s goes to slot s & 1 and dO_s to the other one of its own pair (four
-// slots: Q x2, dO x2 fit beside K). dK: Q_s is read by S^T_s and dK_s, dO_s
-// only by dP^T_s, so the two slots alternate: Q_{s+1} takes the slot dO_s
-// leaves early, dO_{s+1} the one Q_s leaves at the end of step s.
+// dV: K | four 32 KB slots | LSE, D x2 | barriers; Q_s goes to slot s & 1
+// and dO_s to slot 2 + (s & 1). dK: V | four slots | dS^T x2 | LSE, D x2 |
+// barriers; K lands in slots 0 and 1, the warps copy it into TMEM as the A
+// operand of S^T, and the slots then join a ring in which Q_s and dO_s are
+// items 2s and 2s+1 in slot (item + 2) % 4.
 template <bool kDV>
 struct WideKvCfg {
-  static constexpr int kSlots = kDV ? 4 : 2;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kWTile;                                  // dK only
-  static constexpr int kOffSlot = kDV ? kWTile : 2 * kWTile;
+  static constexpr int kSlots = 4;
+  static constexpr int kOffSlot = kWTile;
+  static constexpr int kOffK = kDV ? 0 : kOffSlot;                      // dK: slots 0-1, then TMEM
+  static constexpr int kOffV = 0;                                       // dK only
   static constexpr int kOffDs = kOffSlot + kSlots * kWSubTile;          // dK only
   static constexpr int kOffVec = kOffDs + (kDV ? 0 : 2 * kWDs);
   static constexpr int kVecBytes = 512;                                 // LSE[64], D[64] of one step
@@ -170,6 +171,15 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
   const uint32_t bar_o_final = bars + 152, bar_stall = bars + 160;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 168);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 172);
+  const uint32_t bar_k_tmem = bars + 176;                               // dK: every row of K copied into TMEM
+  // dK: TMEM = dK accumulator | S^T | dP^T | K (A operand of S^T); one buffer
+  // each for S^T and dP^T, whose next products follow the warps' dS^T. dV:
+  // two S^T buffers. tb(s) is step s's buffer, tp(s) the parity of its phase.
+  constexpr uint32_t kColKT = 384;
+  auto tb = [&](int s) { return kDV ? (s & 1) : 0; };
+  auto tp = [&](int s) { return static_cast<uint32_t>(kDV ? (s >> 1) & 1 : s & 1); };
+  auto col_s = [&](int s) { return kWColS + 64u * tb(s); };
+  const uint32_t col_dp = kDV ? kWColDP : kWColS + 64u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -193,8 +203,8 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
   auto step_head = [&](int s) { return b * p.Hq + hk * G + s / per_head; };
   auto step_sub = [&](int s) { return s0 + s % per_head; };
   // slot of step s's Q and dO
-  auto q_slot = [&](int s) { return kDV ? (s & 1) : (s & 1); };
-  auto do_slot = [&](int s) { return kDV ? 2 + (s & 1) : ((s + 1) & 1); };
+  auto q_slot = [&](int s) { return kDV ? (s & 1) : (2 * s + 2) & 3; };
+  auto do_slot = [&](int s) { return kDV ? 2 + (s & 1) : (2 * s + 3) & 3; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -212,6 +222,7 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
     }
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
+    mbar_init(bar_k_tmem, 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -237,6 +248,8 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
       // per-slot use counts give the parity of each empty wait
       int uses[4] = {0, 0, 0, 0};
       auto load = [&](const CUtensorMap* m, int slot, int row0, int bh) -> bool {
+        // dK: slots 0 and 1 take Q/dO only once every row of K is in TMEM
+        if (!kDV && slot < 2 && uses[slot] == 0 && !mbar_wait(bar_k_tmem, 0, abort_flag, deadline)) return false;
         if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
         ++uses[slot];
         mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
@@ -265,14 +278,26 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
         return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
       };
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
-      ok = ok && (nsteps == 0 || mbar_wait(bar_kv_full, 0, abort_flag, deadline));
-      auto scores = [&](int s) {       // S^T_s into buffer s & 1
-        issue_scores(tbase + kWColS + 64u * (s & 1), s_k, s_slot(q_slot(s)));
-        mma_commit(bar_s_full(s & 1));
+      ok = ok && (nsteps == 0 || (mbar_wait(bar_kv_full, 0, abort_flag, deadline) &&
+                                  (kDV || mbar_wait(bar_k_tmem, 0, abort_flag, deadline))));
+      auto scores = [&](int s) {       // S^T_s into buffer tb(s)
+        if (kDV) {
+          issue_scores(tbase + col_s(s), s_k, s_slot(q_slot(s)));
+        } else {                       // A = K from TMEM
+          const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
+          const uint64_t bd = smem_desc_sw128(s_slot(q_slot(s)), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kWD / 16; ++kk) {
+            const uint32_t kb = kk * 32;
+            mma_bf16_ts(tbase + col_s(s), tbase + kColKT + kk * 8, desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id,
+                        kk > 0);
+          }
+        }
+        mma_commit(bar_s_full(tb(s)));
       };
-      auto dp = [&](int s) {           // dP^T_s into buffer s & 1; dO_s's slot is then free
-        issue_scores(tbase + kWColDP + 64u * (s & 1), s_v, s_slot(do_slot(s)));
-        mma_commit(bar_dp_full(s & 1));
+      auto dp = [&](int s) {           // dP^T_s; dO_s's slot is then free
+        issue_scores(tbase + col_dp, s_v, s_slot(do_slot(s)));
+        mma_commit(bar_dp_full(tb(s)));
         mma_commit(bar_empty(do_slot(s)));
       };
       if (kDV) {
@@ -289,10 +314,10 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
             scores(s + 1);
             mma_commit(bar_empty(q_slot(s + 1)));
           }
-          if (!(ok = mbar_wait(bar_ready(s & 1), (s >> 1) & 1, abort_flag, deadline))) break;
+          if (!(ok = mbar_wait(bar_ready(tb(s)), tp(s), abort_flag, deadline))) break;
           if (!(ok = wait_full(do_slot(s)))) break;
           tc_fence_after();
-          issue_acc_ts(tbase + kWColAcc, tbase + kWColS + 64u * (s & 1), s_slot(do_slot(s)), s > 0);
+          issue_acc_ts(tbase + kWColAcc, tbase + col_s(s), s_slot(do_slot(s)), s > 0);
           mma_commit(bar_empty(do_slot(s)));
         }
       } else {
@@ -308,13 +333,14 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
           if (ok) { tc_fence_after(); dp(0); }
         }
         for (int s = 0; s < nsteps && ok; ++s) {
-          if (!(ok = mbar_wait(bar_ready(s & 1), (s >> 1) & 1, abort_flag, deadline))) break;
+          if (!(ok = mbar_wait(bar_ready(tb(s)), tp(s), abort_flag, deadline))) break;
           tc_fence_after();
           issue_acc_ss(tbase + kWColAcc, s_ds(s & 1), s_slot(q_slot(s)), s > 0);
           mma_commit(bar_empty(q_slot(s)));
           if (s + 1 < nsteps) {
-            // buffers (s+1)&1 of S^T, dP^T and dS^T were last used by step s-1,
-            // whose warps' reads and dK (issued above) precede these products
+            // the S^T and dP^T buffers were last read by the warps for step s
+            // (their dS^T_s came first); dS^T buffer (s+1)&1 by dK_{s-1}, issued
+            // before these products
             if (!(ok = wait_full(q_slot(s + 1)))) break;
             tc_fence_after();
             scores(s + 1);
@@ -336,17 +362,38 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
     const bool key_pad = key >= p.Nk;
     const float sl2 = p.scale_log2;
     bool ok = true;
+    if (!kDV && nsteps > 0) {
+      // dK: this key row of K into TMEM as the A operand of S^T (128 columns of
+      // bf16 pairs, the tile's 16-byte units in order); then slots 0 and 1 are free
+      ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+#pragma unroll
+        for (int bx = 0; bx < kWD / 64; ++bx) {
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[4 * u]), "=r"(w[4 * u + 1]), "=r"(w[4 * u + 2]), "=r"(w[4 * u + 3])
+                         : "r"(swz128(s_k + bx * kBoxBytes, r, u)));
+          tmem_st_32x32b_x32(tbase + lane_off + kColKT + 32u * bx, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_k_tmem);
+      }
+    }
     for (int s = 0; s < nsteps && ok; ++s) {
       const int sb = s & 1;
       const int q0 = step_sub(s) * kWSub;
-      ok = mbar_wait(bar_s_full(sb), (s >> 1) & 1, abort_flag, deadline) &&
+      ok = mbar_wait(bar_s_full(tb(s)), tp(s), abort_flag, deadline) &&
            mbar_wait(bar_vec_full(sb), (s >> 1) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base));
       float x[64];
-      tmem_ld64(tbase + lane_off + kWColS + 64u * sb, x);
+      tmem_ld64(tbase + lane_off + col_s(s), x);
       // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
       const int lim = key - p.causal_off - q0;             // first visible query column
 #pragma unroll
@@ -358,25 +405,25 @@ wide_kv_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
         uint32_t pp[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-        tmem_st_32x32b_x32(tbase + lane_off + kWColS + 64u * sb, pp);
+        tmem_st_32x32b_x32(tbase + lane_off + col_s(s), pp);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_ready(sb));
+        mbar_arrive(bar_ready(tb(s)));
       } else {
         // dP^T_s only now: it may still wait for dO_s's load while P^T is formed
-        ok = mbar_wait(bar_dp_full(sb), (s >> 1) & 1, abort_flag, deadline);
+        ok = mbar_wait(bar_dp_full(tb(s)), tp(s), abort_flag, deadline);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         float dpv[64];
-        tmem_ld64(tbase + lane_off + kWColDP + 64u * sb, dpv);
+        tmem_ld64(tbase + lane_off + col_dp, dpv);
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - vec[kWSub + c]);
         // dS^T buffer sb was last read by dK_{s-2}, which completed before S^T_s
         store_row64(s_ds(sb), r, x);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar_ready(sb));
+        mbar_arrive(bar_ready(tb(s)));
       }
       mbar_arrive(bar_vec_empty(sb));
     }

@@ -1,18 +1,17 @@
 """A model of the three-pass backward's dK and dQ passes, run on the CPU.
 
 The kernels (csrc/fa_bwd_wide.cu, wide_kv_kernel<false> and wide_dq_kernel)
-walk 64-row sub-tile steps s over two shared-memory slots. Each step has an
+walk 64-row sub-tile steps s over four shared-memory slots. Each step has an
 operand A (Q_s in the dK pass, K_s in the dQ pass), read by the scores S_s and
 by the accumulate (dK += dS^T Q_s, dQ += dS K_s), and an operand B (dO_s or
-V_s), read only by dP_s. A_s lands in slot s & 1 and B_s in slot (s + 1) & 1,
-so a slot holds A_s, then B_{s+1}, then A_{s+2}. One thread issues S_0, dP_0,
+V_s), read only by dP_s. One thread issues S_0, dP_0,
 then per step: [dS_s written] the accumulate, which frees A_s's slot once it
 completes; [A_{s+1} landed] S_{s+1}; [B_{s+1} landed] dP_{s+1}, which frees
-B's slot. dS (shared memory) is double-buffered by step parity. The dK pass
-also double-buffers S, dP (TMEM) and the step's LSE and D. The dQ pass keeps
-Q in TMEM as the A operand of S instead of in shared memory: Q lands in slots
+B's slot. dS (shared memory) and, in the dK pass, the step's LSE and D are
+double-buffered by step parity. Each pass keeps one operand in TMEM as the A
+operand of the scores (K in the dK pass, Q in the dQ pass): it lands in slots
 0 and 1, every warp copies its rows, and only then do those slots join a ring
-of four (K_j and V_j in slots (2j + 2) % 4 and (2j + 3) % 4); S and dP have
+of four (A_s and B_s in slots (2s + 2) % 4 and (2s + 3) % 4); S and dP have
 one TMEM buffer each. Four warps, one per TMEM lane quarter, form P from S,
 wait for dP, and write dS.
 
@@ -22,8 +21,8 @@ product and every warp reads the data of its own step, that no slot, TMEM
 buffer, dS buffer or vector buffer is overwritten while a reader still needs
 it, and that no parity wait passes on an older phase. Planted changes show
 what the accumulate's release of A's slot, the warps' wait for dP and the
-producer's wait for the Q copy guard;
-the vector buffer's release point turns out to be implied by the slot order.
+producer's wait for the TMEM copy guard; the vector buffer's release point
+turns out to be implied by the slot order.
 """
 import heapq
 import random
@@ -42,8 +41,7 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
     every warp has copied its row, and one TMEM buffer each for S and dP."""
     rng = random.Random(seed)
     errors = []
-    nslots = 2 if dk_pass else 4
-    nbuf = 2 if dk_pass else 1          # TMEM buffers of S and of dP
+    nslots, nbuf = 4, 1                 # slots; TMEM buffers of S and of dP
     full = [Barrier(1) for _ in range(nslots)]
     empty = [Barrier(1) for _ in range(nslots)]
     s_full = [Barrier(1) for _ in range(nbuf)]
@@ -67,10 +65,10 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
     events = []
 
     def a_slot(s):
-        return s & 1 if dk_pass else (2 * s + 2) & 3
+        return (2 * s + 2) & 3
 
     def b_slot(s):
-        return (s + 1) & 1 if dk_pass else (2 * s + 3) & 3
+        return (2 * s + 3) & 3
 
     def buf(s):
         return s % nbuf
@@ -97,8 +95,8 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             if kind == "S":
                 if slot[a_slot(s)] != ("A", s):
                     errors.append(f"S({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
-                if not dk_pass and len(copied) < WARPS:
-                    errors.append(f"S({s}) read Q from TMEM before every warp copied its rows")
+                if len(copied) < WARPS:
+                    errors.append(f"S({s}) read its TMEM operand before every warp copied its rows")
                 if s >= nbuf and len(read_s.get(s - nbuf, ())) < WARPS:
                     errors.append(f"S({s}) overwrote S({s - nbuf}) before every warp read it")
             elif kind == "dP":
@@ -138,14 +136,15 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             slot[0] = slot[1] = ("Q",)
             q_full.complete_tx(1)
 
-        if not dk_pass and n > 0:
-            # the Q tile (and dO, resident) into slots 0 and 1
+        if n > 0:
+            # the TMEM-bound operand (K in the dK pass, Q in the dQ pass) into
+            # slots 0 and 1, with the resident one (V or dO)
             q_full.expect_tx(1)
             q_full.arrive()
             later(rng.uniform(300, 4000), land_q)
 
         def load(i, what):
-            if not dk_pass and i < 2 and uses[i] == 0 and producer_waits_q_copy:
+            if i < 2 and uses[i] == 0 and producer_waits_q_copy:
                 yield from wait(q_tmem, 0, "producer q_tmem", 0)
             yield from wait(empty[i], (uses[i] & 1) ^ 1, "producer empty")
             uses[i] += 1
@@ -179,9 +178,8 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
         if n == 0:
             pipe.append(("commit", o_final))
             return
-        if not dk_pass:
-            yield from wait(q_full, 0, "issuer q_full", 0)
-            yield from wait(q_tmem, 0, "issuer q_tmem", 0)
+        yield from wait(q_full, 0, "issuer q_full", 0)
+        yield from wait(q_tmem, 0, "issuer q_tmem", 0)
         yield from wait_full(a_slot(0))
         pipe.extend([("S", 0), ("commit", s_full[0])])
         if not release_a_after_acc:
@@ -205,9 +203,9 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
 
     # ------------------------------------------------------------ warps
     def warp_role(w):
-        if not dk_pass and n > 0:
+        if n > 0:
             yield from wait(q_full, 0, f"warp {w} q_full", 0)
-            yield ("delay", rng.uniform(50, 600))          # its rows of Q into TMEM
+            yield ("delay", rng.uniform(50, 600))          # its rows of K or Q into TMEM
             if slot[0] != ("Q",) or slot[1] != ("Q",):
                 errors.append(f"warp {w} copied Q from slots holding {slot[0]}, {slot[1]}")
             copied.add(w)
@@ -309,11 +307,12 @@ def test_warps_must_wait_for_dp(dk_pass):
     assert bad_runs(dk_pass, warps_wait_dp=False) > 0
 
 
-def test_dq_pass_slots_0_1_must_wait_for_the_q_copy():
-    """In the dQ pass Q lands in slots 0 and 1 and each warp copies its rows
-    into TMEM; a K or V load into those slots before every warp has copied
-    would overwrite Q under a warp still reading it."""
-    assert bad_runs(False, producer_waits_q_copy=False) > 0
+@pytest.mark.parametrize("dk_pass", [True, False])
+def test_slots_0_1_must_wait_for_the_tmem_copy(dk_pass):
+    """K (dK pass) or Q (dQ pass) lands in slots 0 and 1 and each warp copies
+    its rows into TMEM; a load into those slots before every warp has copied
+    would overwrite the operand under a warp still reading it."""
+    assert bad_runs(dk_pass, producer_waits_q_copy=False) > 0
 
 
 def test_vector_release_is_implied_by_the_slot_order():
