@@ -505,7 +505,7 @@ def native_arm(args, w):
     if det:
         names = ["fwd_kernel", "bwd_deterministic (preprocess + det_dkdv_kernel + det_dq_kernel)", "-", "-"]
     elif w.backward and w.d > 128:
-        names = [fwd_kernel, "bwd_wide (preprocess + wide_kv_kernel dV, dK + wide_dq_kernel)", "-", "-"]
+        names = [fwd_kernel, "bwd_wide (preprocess + wide_dv_kernel, wide_dk_kernel, wide_dq_kernel)", "-", "-"]
     if sparse:
         names = ["fwd_kernel (block-sparse)", "bwd_blocksparse (preprocess + block list + dkdv + dq convert)", "-", "-"]
     if kvlen:

@@ -1,6 +1,6 @@
 """A model of the three-pass backward's dK and dQ passes, run on the CPU.
 
-The kernels (csrc/fa_bwd_wide.cu, wide_kv_kernel<false> and wide_dq_kernel)
+The kernels (csrc/fa_bwd_wide.cu, wide_dk_kernel and wide_dq_kernel)
 walk 64-row sub-tile steps s over four shared-memory slots. Each step has an
 operand A (Q_s in the dK pass, K_s in the dQ pass), read by the scores S_s and
 by the accumulate (dK += dS^T Q_s, dQ += dS K_s), and an operand B (dO_s or
