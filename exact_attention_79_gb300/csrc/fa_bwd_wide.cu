@@ -113,7 +113,6 @@ __device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int 
 }  // namespace
 
 // ------------------------------------------------------------------ dK per key tile
-// Shared memory: K | (dK: V) | two 32 KB sub-tile slots | (dK: dS^T x2) | LSE, D x2 | barriers.
 // Shared memory: V | four 32 KB slots | dS^T x2 | LSE, D x2 | barriers. K
 // lands in slots 0 and 1, the warps copy it into TMEM as the A operand of
 // S^T, and the slots then join a ring in which Q_s and dO_s are items 2s and
@@ -686,9 +685,10 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ dQ per query tile
-// Shared memory: Q | dO | two 32 KB slots (K_j, V_j alternating) | dS x2 | barriers.
-// K_j is read by S_j and dQ_j, V_j only by dP_j: K_{j+1} takes the slot V_j
-// leaves early, V_{j+1} the one K_j leaves at the end of step j.
+// Shared memory: dO | four 32 KB slots | dS x2 | barriers. Q lands in slots
+// 0 and 1, the warps copy it into TMEM as the A operand of S, and the slots
+// then join a ring in which K_j and V_j are items 2j and 2j+1 in slot
+// (item + 2) % 4. K_j is read by S_j and dQ_j, V_j only by dP_j.
 struct WideDqCfg {
   static constexpr int kSlots = 4;
   static constexpr int kOffDo = 0;
