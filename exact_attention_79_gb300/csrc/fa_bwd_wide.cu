@@ -9,18 +9,20 @@
 //
 // At d = 256 the dK and dV accumulators of a 128-key tile alone fill the 512
 // TMEM columns, and one step's Q, dO, K and V tiles (64 KB each) exceed shared
-// memory. The gradients are therefore formed in three passes, each with a
-// fixed order of additions (no atomics: every output is bit reproducible):
-//   wide_dv_kernel  per 128-key tile: S^T = K Q_t^T (N = 128 queries),
-//                   P^T -> TMEM (bf16), dV += P^T dO_t          over 128-query steps t
-//   wide_dk_kernel  per 128-key tile: S^T, dP^T = V dO_s^T over 64-query
-//                   sub-tiles, dS^T = P^T (dP^T - D) -> shared memory, dK += dS^T Q_s
-//   wide_dq_kernel  per 128-row query tile: S = Q K_j^T, dP = dO V_j^T over
-//                   64-key sub-tiles, dS -> shared memory, dQ += dS K_j
-// S (or S^T) and dP are formed twice or three times: 8 GEMMs of the 5 the
-// method needs. bwd_pre_kernel (fa_bwd.cu) writes D and the base-2 LSE first.
-// The dK and dQ passes keep K or Q in TMEM as the A operand of the scores and
-// stream the other operands through a ring of four 32 KB slots.
+// memory. The gradients are therefore formed in three passes over 128-row
+// steps, each with a fixed order of additions (no atomics: every output is
+// bit reproducible):
+//   wide_dv_kernel  per 128-key tile: S^T = K Q_t^T, P^T -> TMEM (bf16),
+//                   dV += P^T dO_t                              over query tiles t
+//   wide_dk_kernel  per 128-key tile: S^T, then dP^T = V dO_t^T in the same
+//                   TMEM columns, dS^T = P^T (dP^T - D) -> shared memory,
+//                   dK += dS^T Q_t                              over query tiles t
+//   wide_dq_kernel  per 128-row query tile: S = Q K_j^T, then dP = dO V_j^T,
+//                   dS -> shared memory, dQ += dS K_j           over key tiles j
+// Every score product is M = 128, N = 128, K = 256. S (or S^T) and dP are
+// formed twice or three times: 8 GEMMs of the 5 the method needs.
+// bwd_pre_kernel (fa_bwd.cu) writes D and the base-2 LSE first. The dK and dQ
+// passes keep K or Q in TMEM as the A operand of the scores.
 //
 // Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
 // (one thread), warps 2-5 one thread per TMEM lane (key row in the dV and dK
@@ -35,36 +37,10 @@ namespace fa {
 namespace {
 
 constexpr int kWD = 256;                          // head-dimension build
-constexpr int kWSub = 64;                         // rows of a sub-tile step
 constexpr int kWTile = kWD / 64 * kBoxBytes;      // [128, 256] bf16: 64 KB
-constexpr int kWSubTile = kWTile / 2;             // [64, 256] bf16: 32 KB
-constexpr int kWSubBox = kBoxBytes / 2;           // one 64-row box: 8 KB
-constexpr int kWDs = kBoxBytes;                   // [128, 64] bf16 (dS or dS^T): 16 KB
 constexpr int kWThreads = 192;
-constexpr uint32_t kWColAcc = 0, kWColS = 256;   // TMEM: accumulator (256 columns) | scores
+constexpr uint32_t kWColAcc = 0;                  // TMEM: the dK, dV or dQ accumulator in columns 0-255
 
-// S (M = 128 rows of `a`, N = 64 rows of `b`, K = 256): both K-major, `a` in
-// boxes of 128 rows (16 KB), `b` in boxes of 64 rows (8 KB)
-__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a, uint32_t b) {
-  const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
-  const uint64_t ad = smem_desc_sw128(a, 16, 1024), bd = smem_desc_sw128(b, 16, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kWD / 16; ++kk) {
-    const uint32_t kb = kk * 32;
-    mma_bf16_ss(d_tmem, desc_add(ad, (kb / 128) * kBoxBytes + kb % 128),
-                desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id, kk > 0);
-  }
-}
-
-// D[128, 256] += A[128, 64] B[64, 256]: B MN-major in boxes of 64 rows (one box
-// per 64 columns); A K-major in shared memory (one 16 KB box) or in TMEM
-__device__ __forceinline__ void issue_acc_ss(uint32_t d_tmem, uint32_t a, uint32_t b, bool acc) {
-  const uint32_t id = make_idesc(1, 128, kWD, 0, 1);
-  const uint64_t ad = smem_desc_sw128(a, 16, 1024), bd = smem_desc_sw128(b, kWSubBox, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kWSub / 16; ++kk)
-    mma_bf16_ss(d_tmem, desc_add(ad, kk * 32), desc_add(bd, kk * 16 * 128), id, acc || kk > 0);
-}
 // 64 fp32 TMEM columns of this thread's lane
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
   uint32_t r[2][32];
@@ -112,29 +88,34 @@ __device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int 
 
 }  // namespace
 
-// ------------------------------------------------------------------ dK per key tile
-// Shared memory: V | four 32 KB slots | dS^T x2 | LSE, D x2 | barriers. K
-// lands in slots 0 and 1, the warps copy it into TMEM as the A operand of
-// S^T, and the slots then join a ring in which Q_s and dO_s are items 2s and
-// 2s+1 in slot (item + 2) % 4.
+// ------------------------------------------------------------------ dK per key tile, 128-query steps
+// Shared memory: V | two 64 KB slots | dS^T | LSE, D x2 | barriers. K lands in
+// slot 0 and the warps copy it into TMEM as the A operand of S^T; Q_t then
+// goes to slot (t + 1) & 1 and dO_t to slot t & 1, so Q_{t+1} takes the slot
+// dO_t leaves after dP^T_t and dO_{t+1} the one Q_t leaves after dK_t.
+// TMEM: dK accumulator | S^T, then dP^T, of the step (128 columns) | K.
+// Per step S^T_t (N = 128 queries) goes into the score columns; once every
+// warp has read it, dP^T_t goes into the same columns; once every warp has
+// written dS^T_t, dK += dS^T_t Q_t.
 struct WideDkCfg {
-  static constexpr int kSlots = 4;
   static constexpr int kOffV = 0;
-  static constexpr int kOffSlot = kWTile;
-  static constexpr int kOffK = kOffSlot;                                // slots 0-1, then TMEM
-  static constexpr int kOffDs = kOffSlot + kSlots * kWSubTile;
-  static constexpr int kOffVec = kOffDs + 2 * kWDs;
-  static constexpr int kVecBytes = 512;                                 // LSE[64], D[64] of one step
+  static constexpr int kOffSlot = kWTile;              // two 64 KB slots; slot 0 first holds K
+  static constexpr int kOffDs = kOffSlot + 2 * kWTile;  // dS^T [128 keys, 128 queries] bf16: two boxes
+  static constexpr int kOffVec = kOffDs + 2 * kBoxBytes;
+  static constexpr int kVecBytes = 1024;               // LSE log2(e) and D of 128 queries
   static constexpr int kOffBar = kOffVec + 2 * kVecBytes;
-  static constexpr int kLayout = kOffBar + 256;
-  static constexpr int kSmemAlloc = kLayout + 1024;
-  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+  static constexpr uint32_t kColSP = 256, kColK = 384;
+  static constexpr int kLayout = kOffBar + 144;
+  // the per-block maximum: the layout needs the dynamic window to start within
+  // 880 bytes of a 1 KB boundary (checked at run time)
+  static constexpr int kSmemAlloc = 232448;
+  static_assert(kLayout <= kSmemAlloc, "shared memory budget");
 };
 
 __global__ void __launch_bounds__(192, 1)
-wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constant__ CUtensorMap map_k,
-               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do64,
-               const __grid_constant__ CUtensorMap map_out, const BwdParams p) {
+wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+               const __grid_constant__ CUtensorMap map_dk, const BwdParams p) {
   using C = WideDkCfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -144,31 +125,22 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
   }
-  const uint32_t s_k = base + C::kOffK, s_v = base + C::kOffV;
-  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWSubTile; };
-  auto s_ds = [&](int i) { return base + C::kOffDs + i * kWDs; };
+  const uint32_t s_v = base + C::kOffV;
+  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWTile; };
+  const uint32_t s_k = s_slot(0);                      // the K tile until it is in TMEM
+  const uint32_t s_ds = base + C::kOffDs;
   auto s_vec = [&](int i) { return base + C::kOffVec + i * C::kVecBytes; };
   const uint32_t bars = base + C::kOffBar;
-  const uint32_t bar_kv_full = bars;
-  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };           // slots (up to 4)
-  auto bar_empty = [&](int i) { return bars + 40u + 8u * i; };
-  auto bar_vec_full = [&](int i) { return bars + 72u + 8u * i; };
-  auto bar_vec_empty = [&](int i) { return bars + 88u + 8u * i; };
-  auto bar_s_full = [&](int i) { return bars + 104u + 8u * i; };
-  auto bar_dp_full = [&](int i) { return bars + 120u + 8u * i; };
-  auto bar_ready = [&](int i) { return bars + 136u + 8u * i; };        // dS^T written
-  const uint32_t bar_o_final = bars + 152, bar_stall = bars + 160;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 168);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 172);
-  const uint32_t bar_k_tmem = bars + 176;                               // every row of K copied into TMEM
-  // TMEM: dK accumulator | S^T | dP^T | K (A operand of S^T). One buffer each
-  // for S^T and dP^T, whose next products follow the warps' dS^T: step s uses
-  // barrier 0 at phase parity s & 1.
-  constexpr uint32_t kColKT = 384;
-  auto tb = [&](int) { return 0; };
-  auto tp = [&](int s) { return static_cast<uint32_t>(s & 1); };
-  auto col_s = [&](int) { return kWColS; };
-  const uint32_t col_dp = kWColS + 64u;
+  const uint32_t bar_kv_full = bars;                   // K and V landed
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };
+  auto bar_empty = [&](int i) { return bars + 24u + 8u * i; };
+  auto bar_vec_full = [&](int i) { return bars + 40u + 8u * i; };
+  auto bar_vec_empty = [&](int i) { return bars + 56u + 8u * i; };
+  const uint32_t bar_s_full = bars + 72, bar_s_read = bars + 80, bar_dp_full = bars + 88;
+  const uint32_t bar_ready = bars + 96, bar_o_final = bars + 104, bar_stall = bars + 112;
+  const uint32_t bar_k_tmem = bars + 120;              // every row of K copied into TMEM
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 128);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 132);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -183,35 +155,33 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
   const int bhkv = grp * p.head_group + local % gsize;
   const int b = bhkv / p.Hkv, hk = bhkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int nq64 = p.NQP / kWSub;
-  // first 64-query sub-tile that sees key tile jt (bottom-right causal)
+  const int nq = p.NQP / kBM;
+  // first query tile that sees key tile jt (bottom-right causal)
   const int first_row = jt * kBN - p.causal_off;
-  const int s0 = p.causal ? (first_row <= 0 ? 0 : min(nq64, first_row / kWSub)) : 0;
-  const int per_head = nq64 - s0;
-  const int nsteps = (jt < nkt) ? G * per_head : 0;
-  auto step_head = [&](int s) { return b * p.Hq + hk * G + s / per_head; };
-  auto step_sub = [&](int s) { return s0 + s % per_head; };
-  // slot of step s's Q and dO
-  auto q_slot = [&](int s) { return (2 * s + 2) & 3; };
-  auto do_slot = [&](int s) { return (2 * s + 3) & 3; };
+  const int it0 = p.causal ? (first_row <= 0 ? 0 : min(nq, first_row / kBM)) : 0;
+  const int per_head = nq - it0;
+  const int nsteps = G * per_head;
+  auto step_head = [&](int t) { return b * p.Hq + hk * G + t / per_head; };
+  auto step_tile = [&](int t) { return it0 + t % per_head; };
+  auto q_slot = [&](int t) { return (t + 1) & 1; };
+  auto do_slot = [&](int t) { return t & 1; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar_kv_full, 1);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_vec_full(i), 1);
       mbar_init(bar_vec_empty(i), 128);
-      mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_dp_full(i), 1);
-      mbar_init(bar_ready(i), 128);
     }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_read, 128);
+    mbar_init(bar_dp_full, 1);
+    mbar_init(bar_ready, 128);
+    mbar_init(bar_k_tmem, 128);
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
-    mbar_init(bar_k_tmem, 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -227,92 +197,102 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_map(&map_q64);
-      tma_prefetch_map(&map_do64);
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(bar_kv_full, 2 * kWTile);
       for (int bx = 0; bx < kWD / 64; ++bx) {
         tma_load_3d(s_k + bx * kBoxBytes, &map_k, bar_kv_full, bx * 64, jt * kBN, bhkv);
         tma_load_3d(s_v + bx * kBoxBytes, &map_v, bar_kv_full, bx * 64, jt * kBN, bhkv);
       }
-      // per-slot use counts give the parity of each empty wait
-      int uses[4] = {0, 0, 0, 0};
+      int uses[2] = {0, 0};
       auto load = [&](const CUtensorMap* m, int slot, int row0, int bh) -> bool {
-        // slots 0 and 1 take Q/dO only once every row of K is in TMEM
-        if (slot < 2 && uses[slot] == 0 && !mbar_wait(bar_k_tmem, 0, abort_flag, deadline)) return false;
+        // slot 0 takes Q/dO only once every row of K is in TMEM
+        if (slot == 0 && uses[0] == 0 && !mbar_wait(bar_k_tmem, 0, abort_flag, deadline)) return false;
         if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
         ++uses[slot];
-        mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
+        mbar_arrive_expect_tx(bar_full(slot), kWTile);
         for (int bx = 0; bx < kWD / 64; ++bx)
-          tma_load_3d(s_slot(slot) + bx * kWSubBox, m, bar_full(slot), bx * 64, row0, bh);
+          tma_load_3d(s_slot(slot) + bx * kBoxBytes, m, bar_full(slot), bx * 64, row0, bh);
         return true;
       };
-      for (int s = 0; s < nsteps; ++s) {
-        const int bh = step_head(s), row0 = step_sub(s) * kWSub;
-        if (!load(&map_q64, q_slot(s), row0, bh)) break;
-        const int vb = s & 1;
-        if (!mbar_wait(bar_vec_empty(vb), ((s >> 1) & 1) ^ 1, abort_flag, deadline)) break;
-        mbar_arrive_expect_tx(bar_vec_full(vb), 2 * kWSub * 4);
+      for (int t = 0; t < nsteps; ++t) {
+        const int bh = step_head(t), row0 = step_tile(t) * kBM;
+        if (!load(&map_q, q_slot(t), row0, bh)) break;
+        const int vb = t & 1;
+        if (!mbar_wait(bar_vec_empty(vb), ((t >> 1) & 1) ^ 1, abort_flag, deadline)) break;
+        mbar_arrive_expect_tx(bar_vec_full(vb), 2 * kBM * 4);
         const size_t voff = static_cast<size_t>(bh) * p.NQP + row0;
-        bulk_load(s_vec(vb), p.ws_lse2 + voff, kWSub * 4, bar_vec_full(vb));
-        bulk_load(s_vec(vb) + kWSub * 4, p.ws_d + voff, kWSub * 4, bar_vec_full(vb));
-        if (!load(&map_do64, do_slot(s), row0, bh)) break;
+        bulk_load(s_vec(vb), p.ws_lse2 + voff, kBM * 4, bar_vec_full(vb));
+        bulk_load(s_vec(vb) + kBM * 4, p.ws_d + voff, kBM * 4, bar_vec_full(vb));
+        if (!load(&map_do, do_slot(t), row0, bh)) break;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // S^T_0; per step t: [S^T_t read] dP^T_t into the same columns (dO_t's slot
+    // free after), [dS^T_t written] dK_t (Q_t's slot free after), [Q_{t+1}] S^T_{t+1}.
     if (lane == 0) {
-      int fulls[4] = {0, 0, 0, 0};     // phases of each slot's full barrier waited for so far
+      int fulls[2] = {0, 0};
       auto wait_full = [&](int slot) -> bool {
         return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
       };
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || (mbar_wait(bar_kv_full, 0, abort_flag, deadline) &&
                                   mbar_wait(bar_k_tmem, 0, abort_flag, deadline)));
-      auto scores = [&](int s) {       // S^T_s = K Q_s^T, A = K from TMEM
-        const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
-        const uint64_t bd = smem_desc_sw128(s_slot(q_slot(s)), 16, 1024);
+      const uint32_t id_s = make_idesc(1, 128, 128, 0, 0);     // S^T, dP^T: K-major operands
+      const uint32_t id_k = make_idesc(1, 128, kWD, 0, 1);     // dK: A = dS^T K-major, B = Q MN-major
+      auto scores = [&](int t) {     // S^T_t = K Q_t^T, A = K from TMEM
+        const uint64_t qd = smem_desc_sw128(s_slot(q_slot(t)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kWD / 16; ++kk) {
-          const uint32_t kb = kk * 32;
-          mma_bf16_ts(tbase + col_s(s), tbase + kColKT + kk * 8, desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id,
-                      kk > 0);
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ts(tbase + C::kColSP, tbase + C::kColK + kk * 8, desc_add(qd, off), id_s, kk > 0);
         }
-        mma_commit(bar_s_full(tb(s)));
+        mma_commit(bar_s_full);
       };
-      auto dp = [&](int s) {           // dP^T_s; dO_s's slot is then free
-        issue_scores(tbase + col_dp, s_v, s_slot(do_slot(s)));
-        mma_commit(bar_dp_full(tb(s)));
-        mma_commit(bar_empty(do_slot(s)));
-      };
-      {
-        // order: S^T_0, dP^T_0; per step s: [dS^T_s] dK_s (Q_s's slot free
-        // after), [Q_{s+1}] S^T_{s+1}, [dO_{s+1}] dP^T_{s+1}. dO_{s+1} can only
-        // load once dK_s has freed its slot; S^T_{s+1} runs meanwhile. (S^T two
-        // steps ahead put a second such load, Q_{s+2} behind dP^T_{s+1}, on the
-        // issuer's path in every step.)
-        if (ok && nsteps > 0) {
-          ok = wait_full(q_slot(0));
-          if (ok) { tc_fence_after(); scores(0); }
-          ok = ok && wait_full(do_slot(0));
-          if (ok) { tc_fence_after(); dp(0); }
+      auto dp = [&](int t) {         // dP^T_t = V dO_t^T
+        const uint64_t vd = smem_desc_sw128(s_v, 16, 1024), dod = smem_desc_sw128(s_slot(do_slot(t)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kWD / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + C::kColSP, desc_add(vd, off), desc_add(dod, off), id_s, kk > 0);
         }
-        for (int s = 0; s < nsteps && ok; ++s) {
-          if (!(ok = mbar_wait(bar_ready(tb(s)), tp(s), abort_flag, deadline))) break;
+        mma_commit(bar_dp_full);
+        mma_commit(bar_empty(do_slot(t)));
+      };
+      auto dk = [&](int t) {         // dK += dS^T Q_t over the step's 128 queries
+        const uint64_t dsd = smem_desc_sw128(s_ds, 16, 1024);
+        const uint64_t qmn = smem_desc_sw128(s_slot(q_slot(t)), kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + kWColAcc, desc_add(dsd, off), desc_add(qmn, kk * 16 * 128), id_k, t > 0 || kk > 0);
+        }
+        mma_commit(bar_empty(q_slot(t)));
+      };
+      if (ok && nsteps > 0) {
+        ok = wait_full(q_slot(0));
+        if (ok) {
           tc_fence_after();
-          issue_acc_ss(tbase + kWColAcc, s_ds(s & 1), s_slot(q_slot(s)), s > 0);
-          mma_commit(bar_empty(q_slot(s)));
-          if (s + 1 < nsteps) {
-            // the S^T and dP^T buffers were last read by the warps for step s
-            // (their dS^T_s came first); dS^T buffer (s+1)&1 by dK_{s-1}, issued
-            // before these products
-            if (!(ok = wait_full(q_slot(s + 1)))) break;
-            tc_fence_after();
-            scores(s + 1);
-            if (!(ok = wait_full(do_slot(s + 1)))) break;
-            tc_fence_after();
-            dp(s + 1);
-          }
+          scores(0);
+        }
+      }
+      for (int t = 0; t < nsteps && ok; ++t) {
+        if (!(ok = mbar_wait(bar_s_read, t & 1, abort_flag, deadline))) break;
+        if (!(ok = wait_full(do_slot(t)))) break;
+        tc_fence_after();
+        dp(t);
+        // the single dS^T buffer: dS^T_t is written after dP^T_t completes, so
+        // after dK_{t-1} (issued before dP^T_t) has read dS^T_{t-1}
+        if (!(ok = mbar_wait(bar_ready, t & 1, abort_flag, deadline))) break;
+        tc_fence_after();
+        dk(t);
+        if (t + 1 < nsteps) {
+          // the score columns: every warp read dP^T_t before its dS^T_t
+          if (!(ok = wait_full(q_slot(t + 1)))) break;
+          tc_fence_after();
+          scores(t + 1);
         }
       }
       if (ok) mma_commit(bar_o_final);
@@ -326,10 +306,11 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
     const int key = jt * kBN + r;
     const bool key_pad = key >= p.Nk;
     const float sl2 = p.scale_log2;
+    const uint32_t t_sp = tbase + lane_off + C::kColSP;
     bool ok = true;
     if (nsteps > 0) {
       // this key row of K into TMEM as the A operand of S^T (128 columns of
-      // bf16 pairs, the tile's 16-byte units in order); then slots 0 and 1 are free
+      // bf16 pairs, the tile's 16-byte units in order); slot 0 is then free
       ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
@@ -341,48 +322,57 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w[4 * u]), "=r"(w[4 * u + 1]), "=r"(w[4 * u + 2]), "=r"(w[4 * u + 3])
                          : "r"(swz128(s_k + bx * kBoxBytes, r, u)));
-          tmem_st_32x32b_x32(tbase + lane_off + kColKT + 32u * bx, w);
+          tmem_st_32x32b_x32(tbase + lane_off + C::kColK + 32u * bx, w);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_k_tmem);
       }
     }
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int sb = s & 1;
-      const int q0 = step_sub(s) * kWSub;
-      ok = mbar_wait(bar_s_full(tb(s)), tp(s), abort_flag, deadline) &&
-           mbar_wait(bar_vec_full(sb), (s >> 1) & 1, abort_flag, deadline);
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int vb = t & 1;
+      ok = mbar_wait(bar_s_full, t & 1, abort_flag, deadline) &&
+           mbar_wait(bar_vec_full(vb), (t >> 1) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base));
-      float x[64];
-      tmem_ld64(tbase + lane_off + col_s(s), x);
-      // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
-      const int lim = key - p.causal_off - q0;             // first visible query column
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float e = ex2_approx(fmaf(x[c], sl2, -vec[c]));
-        x[c] = (key_pad || (p.causal && c < lim)) ? 0.f : e;
-      }
+      const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(vb) - base));
+      float pr[128];
       {
-        // dP^T_s only now: it may still wait for dO_s's load while P^T is formed
-        ok = mbar_wait(bar_dp_full(tb(s)), tp(s), abort_flag, deadline);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        float dpv[64];
-        tmem_ld64(tbase + lane_off + col_dp, dpv);
+        uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - vec[kWSub + c]);
-        // dS^T buffer sb was last read by dK_{s-2}, which completed before S^T_s
-        store_row64(s_ds(sb), r, x);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar_ready(tb(s)));
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(t_sp + 32 * q4, sr[q4]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+        // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
+        const int lim = key - p.causal_off - step_tile(t) * kBM;   // first visible query column
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -vec[c]));
+          pr[c] = (key_pad || (p.causal && c < lim)) ? 0.f : e;
+        }
       }
-      mbar_arrive(bar_vec_empty(sb));
+      // S^T_t is in registers: its columns may take dP^T_t
+      tc_fence_before();
+      mbar_arrive(bar_s_read);
+      ok = mbar_wait(bar_dp_full, t & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64];
+        tmem_ld64(t_sp + 64u * hh, x);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = pr[64 * hh + c] * (x[c] - vec[kBM + 64 * hh + c]);
+        // dS^T row r, queries [64 hh, 64 hh + 64): box hh
+        store_row64(s_ds + hh * kBoxBytes, r, x);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_ready);
+      mbar_arrive(bar_vec_empty(vb));
     }
     // ---------------------------------------------------------- epilogue
     if (ok) {
@@ -408,7 +398,7 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q64, const __grid_constan
     }
     named_bar_sync(1, 128);
     if (!*abort_flag && warp == 2 && lane == 0 && jt < nkt) {
-      for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_out, stg + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
+      for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_dk, stg + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
       tma_store_commit();
       tma_store_wait_all0();
     }
@@ -684,27 +674,30 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-// ------------------------------------------------------------------ dQ per query tile
-// Shared memory: dO | four 32 KB slots | dS x2 | barriers. Q lands in slots
-// 0 and 1, the warps copy it into TMEM as the A operand of S, and the slots
-// then join a ring in which K_j and V_j are items 2j and 2j+1 in slot
-// (item + 2) % 4. K_j is read by S_j and dQ_j, V_j only by dP_j.
+// ------------------------------------------------------------------ dQ per query tile, 128-key steps
+// Shared memory: dO | two 64 KB slots | dS | barriers. Q lands in slot 0 and
+// the warps copy it into TMEM as the A operand of S; K_j then goes to slot
+// (j + 1) & 1 and V_j to slot j & 1, so K_{j+1} takes the slot V_j leaves
+// after dP_j and V_{j+1} the one K_j leaves after dQ_j.
+// TMEM: dQ accumulator | S, then dP, of the step (128 columns) | Q.
+// Per step S_j (N = 128 keys) goes into the score columns; once every warp
+// has read it, dP_j goes into the same columns; once every warp has written
+// dS_j, dQ_j += dS_j K_j. With 128 keys per step every score product is
+// N = 128 (an N = 64 product takes about as long).
 struct WideDqCfg {
-  static constexpr int kSlots = 4;
   static constexpr int kOffDo = 0;
-  static constexpr int kOffSlot = kWTile;              // slots 0-1 first hold the Q tile
-  static constexpr int kOffDs = kOffSlot + kSlots * kWSubTile;
-  static constexpr int kOffBar = kOffDs + 2 * kWDs;
-  // TMEM: dQ accumulator | S | dP | Q as the A operand of S (two bf16 per column)
-  static constexpr uint32_t kColS = 256, kColDP = 320, kColQ = 384;
+  static constexpr int kOffSlot = kWTile;              // two 64 KB slots; slot 0 first holds Q
+  static constexpr int kOffDs = kOffSlot + 2 * kWTile;  // dS [128 queries, 128 keys] bf16: two boxes
+  static constexpr int kOffBar = kOffDs + 2 * kBoxBytes;
+  static constexpr uint32_t kColSP = 256, kColQ = 384;
   static constexpr int kLayout = kOffBar + 256;
   static constexpr int kSmemAlloc = kLayout + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
 __global__ void __launch_bounds__(192, 1)
-wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k64,
-               const __grid_constant__ CUtensorMap map_v64, const __grid_constant__ CUtensorMap map_do,
+wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
   using C = WideDqCfg;
   extern __shared__ uint8_t smem_raw[];
@@ -716,18 +709,18 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     return;
   }
   const uint32_t s_do = base + C::kOffDo;
-  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWSubTile; };
+  auto s_slot = [&](int i) { return base + C::kOffSlot + i * kWTile; };
   const uint32_t s_q = s_slot(0);                      // the Q tile, then the dQ staging
-  auto s_ds = [&](int i) { return base + C::kOffDs + i * kWDs; };
+  const uint32_t s_ds = base + C::kOffDs;
   const uint32_t bars = base + C::kOffBar;
   const uint32_t bar_q_full = bars;                    // Q and dO landed
-  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };     // slots 0..3
-  auto bar_empty = [&](int i) { return bars + 40u + 8u * i; };
-  const uint32_t bar_s_full = bars + 72, bar_dp_full = bars + 80, bar_ready = bars + 88;
-  const uint32_t bar_o_final = bars + 96, bar_stall = bars + 104;
-  const uint32_t bar_q_tmem = bars + 112;              // every row of Q copied into TMEM
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 120);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 124);
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };
+  auto bar_empty = [&](int i) { return bars + 24u + 8u * i; };
+  const uint32_t bar_s_full = bars + 40, bar_s_read = bars + 48, bar_dp_full = bars + 56;
+  const uint32_t bar_ready = bars + 64, bar_o_final = bars + 72, bar_stall = bars + 80;
+  const uint32_t bar_q_tmem = bars + 88;               // every row of Q copied into TMEM
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 96);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 100);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -742,25 +735,24 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int bh = grp * p.head_group + local % gsize;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int nk64 = (p.Nk + kWSub - 1) / kWSub;
-  int nsteps = nk64;
+  const int nkt = p.NKP / kBN;
+  int nsteps = nkt;
   if (p.causal) {
     const int last = qt * kBM + kBM - 1 + p.causal_off;   // the tile's last row sees keys up to here
-    nsteps = last < 0 ? 0 : min(nk64, last / kWSub + 1);
+    nsteps = last < 0 ? 0 : min(nkt, last / kBN + 1);
   }
-  // ring of four slots: K_j and V_j are items 2j and 2j+1, in slot (item + 2) % 4,
-  // so the first two go to slots 2 and 3 while Q still occupies slots 0 and 1
-  auto k_slot = [&](int j) { return (2 * j + 2) & 3; };
-  auto v_slot = [&](int j) { return (2 * j + 3) & 3; };
+  auto k_slot = [&](int j) { return (j + 1) & 1; };
+  auto v_slot = [&](int j) { return j & 1; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar_q_full, 1);
-    for (int i = 0; i < C::kSlots; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
     }
     mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_read, 128);
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_ready, 128);
     mbar_init(bar_q_tmem, 128);
@@ -781,80 +773,95 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nsteps > 0) {
-      tma_prefetch_map(&map_k64);
-      tma_prefetch_map(&map_v64);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(bar_q_full, 2 * kWTile);
       for (int bx = 0; bx < kWD / 64; ++bx) {
         tma_load_3d(s_q + bx * kBoxBytes, &map_q, bar_q_full, bx * 64, qt * kBM, bh);
         tma_load_3d(s_do + bx * kBoxBytes, &map_do, bar_q_full, bx * 64, qt * kBM, bh);
       }
-      int uses[C::kSlots] = {0, 0, 0, 0};
+      int uses[2] = {0, 0};
       auto load = [&](const CUtensorMap* m, int slot, int row0) -> bool {
-        // slots 0 and 1 take K/V only once every row of Q is in TMEM
-        if (slot < 2 && uses[slot] == 0 && !mbar_wait(bar_q_tmem, 0, abort_flag, deadline)) return false;
+        // slot 0 takes K/V only once every row of Q is in TMEM
+        if (slot == 0 && uses[0] == 0 && !mbar_wait(bar_q_tmem, 0, abort_flag, deadline)) return false;
         if (!mbar_wait(bar_empty(slot), (uses[slot] & 1) ^ 1, abort_flag, deadline)) return false;
         ++uses[slot];
-        mbar_arrive_expect_tx(bar_full(slot), kWSubTile);
+        mbar_arrive_expect_tx(bar_full(slot), kWTile);
         for (int bx = 0; bx < kWD / 64; ++bx)
-          tma_load_3d(s_slot(slot) + bx * kWSubBox, m, bar_full(slot), bx * 64, row0, bh_kv);
+          tma_load_3d(s_slot(slot) + bx * kBoxBytes, m, bar_full(slot), bx * 64, row0, bh_kv);
         return true;
       };
       for (int j = 0; j < nsteps; ++j) {
-        if (!load(&map_k64, k_slot(j), j * kWSub)) break;
-        if (!load(&map_v64, v_slot(j), j * kWSub)) break;
+        if (!load(&map_k, k_slot(j), j * kBN)) break;
+        if (!load(&map_v, v_slot(j), j * kBN)) break;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // S_0; per step j: [S_j read] dP_j into the same columns (V_j's slot free
+    // after), [dS_j written] dQ_j (K_j's slot free after), [K_{j+1}] S_{j+1}.
     if (lane == 0) {
-      int fulls[C::kSlots] = {0, 0, 0, 0};
+      int fulls[2] = {0, 0};
       auto wait_full = [&](int slot) -> bool {
         return mbar_wait(bar_full(slot), (fulls[slot]++) & 1, abort_flag, deadline);
       };
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || (mbar_wait(bar_q_full, 0, abort_flag, deadline) &&
                                   mbar_wait(bar_q_tmem, 0, abort_flag, deadline)));
-      auto scores = [&](int j) {     // S_j = Q K_j^T with Q from TMEM
-        const uint32_t id = make_idesc(1, 128, kWSub, 0, 0);
-        const uint64_t bd = smem_desc_sw128(s_slot(k_slot(j)), 16, 1024);
+      const uint32_t id_s = make_idesc(1, 128, 128, 0, 0);     // S, dP: K-major operands
+      const uint32_t id_q = make_idesc(1, 128, kWD, 0, 1);     // dQ: A = dS K-major, B = K MN-major
+      auto scores = [&](int j) {     // S_j = Q K_j^T, A = Q from TMEM
+        const uint64_t kd = smem_desc_sw128(s_slot(k_slot(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kWD / 16; ++kk) {
-          const uint32_t kb = kk * 32;
-          mma_bf16_ts(tbase + C::kColS, tbase + C::kColQ + kk * 8, desc_add(bd, (kb / 128) * kWSubBox + kb % 128), id,
-                      kk > 0);
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ts(tbase + C::kColSP, tbase + C::kColQ + kk * 8, desc_add(kd, off), id_s, kk > 0);
         }
         mma_commit(bar_s_full);
       };
-      auto dp = [&](int j) {
-        issue_scores(tbase + C::kColDP, s_do, s_slot(v_slot(j)));
+      auto dp = [&](int j) {         // dP_j = dO V_j^T
+        const uint64_t dod = smem_desc_sw128(s_do, 16, 1024), vd = smem_desc_sw128(s_slot(v_slot(j)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kWD / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + C::kColSP, desc_add(dod, off), desc_add(vd, off), id_s, kk > 0);
+        }
         mma_commit(bar_dp_full);
         mma_commit(bar_empty(v_slot(j)));
       };
-      // order: S_0, dP_0; per step j: [dS_j] dQ_j (K_j's slot free after),
-      // [K_{j+1}] S_{j+1}, [V_{j+1}] dP_{j+1}. S and dP have one TMEM buffer
-      // each: step j+1's are issued only after the warps' read of step j's
-      // (the dS_j they waited for). With four slots K_{j+2} and V_{j+2} load
-      // while step j+1 runs.
+      auto dq = [&](int j) {         // dQ += dS K_j over the step's 128 keys
+        const uint64_t dsd = smem_desc_sw128(s_ds, 16, 1024);
+        const uint64_t kmn = smem_desc_sw128(s_slot(k_slot(j)), kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+          mma_bf16_ss(tbase + kWColAcc, desc_add(dsd, off), desc_add(kmn, kk * 16 * 128), id_q, j > 0 || kk > 0);
+        }
+        mma_commit(bar_empty(k_slot(j)));
+      };
       if (ok && nsteps > 0) {
         ok = wait_full(k_slot(0));
-        if (ok) { tc_fence_after(); scores(0); }
-        ok = ok && wait_full(v_slot(0));
-        if (ok) { tc_fence_after(); dp(0); }
+        if (ok) {
+          tc_fence_after();
+          scores(0);
+        }
       }
       for (int j = 0; j < nsteps && ok; ++j) {
+        if (!(ok = mbar_wait(bar_s_read, j & 1, abort_flag, deadline))) break;
+        if (!(ok = wait_full(v_slot(j)))) break;
+        tc_fence_after();
+        dp(j);
+        // the single dS buffer: dS_j is written after dP_j completes, so after
+        // dQ_{j-1} (issued before dP_j) has read dS_{j-1}
         if (!(ok = mbar_wait(bar_ready, j & 1, abort_flag, deadline))) break;
         tc_fence_after();
-        issue_acc_ss(tbase + kWColAcc, s_ds(j & 1), s_slot(k_slot(j)), j > 0);
-        mma_commit(bar_empty(k_slot(j)));
+        dq(j);
         if (j + 1 < nsteps) {
-          // dS buffer (j+1)&1 was last read by dQ_{j-1}, issued before these products
+          // the score columns: every warp read dP_j before its dS_j
           if (!(ok = wait_full(k_slot(j + 1)))) break;
           tc_fence_after();
           scores(j + 1);
-          if (!(ok = wait_full(v_slot(j + 1)))) break;
-          tc_fence_after();
-          dp(j + 1);
         }
       }
       if (ok) mma_commit(bar_o_final);
@@ -871,11 +878,12 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const float lse2 = p.ws_lse2[static_cast<size_t>(bh) * p.NQP + qt * kBM + r];
     const float dsub = p.ws_d[static_cast<size_t>(bh) * p.NQP + qt * kBM + r];
     const int key_lim = p.causal ? min(p.Nk, q + p.causal_off + 1) : p.Nk;   // keys < key_lim are visible
+    const uint32_t t_sp = tbase + lane_off + C::kColSP;
     bool ok = true;
     if (nsteps > 0) {
       // this row of Q into TMEM as the A operand of S: 128 columns of bf16
       // pairs, the lower dimension in the low half (the tile's 16-byte units
-      // in order), then slots 0 and 1 are free for K and V
+      // in order); slot 0 is then free for K and V
       ok = mbar_wait(bar_q_full, 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
@@ -895,29 +903,41 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     for (int j = 0; j < nsteps && ok; ++j) {
-      const int sb = j & 1;
-      // P from S first: dP_j may still wait for V_j's load
       ok = mbar_wait(bar_s_full, j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float x[64], dpv[64];
-      tmem_ld64(tbase + lane_off + C::kColS, x);
-      const int lim = key_lim - j * kWSub;
+      float pr[128];
+      {
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float pe = ex2_approx(fmaf(x[c], sl2, -lse2));
-        x[c] = (c < lim) ? pe : 0.f;
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(t_sp + 32 * q4, sr[q4]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+        const int lim = key_lim - j * kBN;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float pe = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
+          pr[c] = (c < lim) ? pe : 0.f;
+        }
       }
+      // S_j is in registers: its columns may take dP_j
+      tc_fence_before();
+      mbar_arrive(bar_s_read);
       ok = mbar_wait(bar_dp_full, j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      tmem_ld64(tbase + lane_off + C::kColDP, dpv);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) x[c] = x[c] * (dpv[c] - dsub);
-      // dS buffer sb was last read by dQ_{j-2}, which completed before S_j
-      store_row64(s_ds(sb), r, x);
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64];
+        tmem_ld64(t_sp + 64u * hh, x);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = pr[64 * hh + c] * (x[c] - dsub);
+        // dS row r, keys [64 hh, 64 hh + 64): box hh
+        store_row64(s_ds + hh * kBoxBytes, r, x);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ready);
@@ -987,10 +1007,10 @@ cudaError_t launch_bwd_wide(const BwdMaps& m, const BwdMaps& m64, const BwdParam
   wide_dv_kernel<<<kv_grid, kWThreads, WideDvCfg::kSmemAlloc, stream>>>(m.q, m.k, m.dO, m.dv, pk);
   cudaError_t r = cudaGetLastError();
   if (r != cudaSuccess) return r;
-  wide_dk_kernel<<<kv_grid, kWThreads, WideDkCfg::kSmemAlloc, stream>>>(m64.q, m.k, m.v, m64.dO, m.dk, pk);
+  wide_dk_kernel<<<kv_grid, kWThreads, WideDkCfg::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dk, pk);
   r = cudaGetLastError();
   if (r != cudaSuccess) return r;
-  wide_dq_kernel<<<q_grid, kWThreads, WideDqCfg::kSmemAlloc, stream>>>(m.q, m64.k, m64.v, m.dO, m.dq, pq);
+  wide_dq_kernel<<<q_grid, kWThreads, WideDqCfg::kSmemAlloc, stream>>>(m.q, m.k, m.v, m.dO, m.dq, pq);
   return cudaGetLastError();
 }
 

@@ -1,18 +1,18 @@
 """A model of the three-pass backward's dK and dQ passes, run on the CPU.
 
-The kernels (csrc/fa_bwd_wide.cu, wide_dk_kernel and wide_dq_kernel)
-walk 64-row sub-tile steps s over four shared-memory slots. Each step has an
-operand A (Q_s in the dK pass, K_s in the dQ pass), read by the scores S_s and
-by the accumulate (dK += dS^T Q_s, dQ += dS K_s), and an operand B (dO_s or
-V_s), read only by dP_s. One thread issues S_0, dP_0,
-then per step: [dS_s written] the accumulate, which frees A_s's slot once it
-completes; [A_{s+1} landed] S_{s+1}; [B_{s+1} landed] dP_{s+1}, which frees
-B's slot. dS (shared memory) and, in the dK pass, the step's LSE and D are
-double-buffered by step parity. Each pass keeps one operand in TMEM as the A
-operand of the scores (K in the dK pass, Q in the dQ pass): it lands in slots
-0 and 1, every warp copies its rows, and only then do those slots join a ring
-of four (A_s and B_s in slots (2s + 2) % 4 and (2s + 3) % 4); S and dP have
-one TMEM buffer each. Four warps, one per TMEM lane quarter, form P from S,
+The kernels (csrc/fa_bwd_wide.cu, wide_dk_kernel and wide_dq_kernel) walk
+128-row steps s over two 64 KB shared-memory slots. Each step has an operand
+A (Q_s in the dK pass, K_s in the dQ pass), read by the scores S_s and by the
+accumulate (dK += dS^T Q_s, dQ += dS K_s), and an operand B (dO_s or V_s),
+read only by dP_s. A_s lands in slot (s + 1) & 1 and B_s in slot s & 1, so B
+takes the slot A left and the other way round. Each pass keeps one operand in
+TMEM as the A operand of the scores (K in the dK pass, Q in the dQ pass): it
+lands in slot 0, every warp copies its rows, and only then does slot 0 take
+other loads. S and dP share one 128-column TMEM region: one thread issues
+S_0, then per step [every warp has read S_s] dP_s, which frees B's slot,
+[dS_s written] the accumulate, which frees A's slot, and [A_{s+1} landed]
+S_{s+1}. dS has one shared-memory buffer; the dK pass double-buffers the
+step's LSE and D. Four warps, one per TMEM lane quarter, read S, form P,
 wait for dP, and write dS.
 
 As for the other kernels, the roles run as coroutines with random latencies
@@ -20,9 +20,10 @@ over barriers with the hardware's parity rule. The model checks that every
 product and every warp reads the data of its own step, that no slot, TMEM
 buffer, dS buffer or vector buffer is overwritten while a reader still needs
 it, and that no parity wait passes on an older phase. Planted changes show
-what the accumulate's release of A's slot, the warps' wait for dP and the
-producer's wait for the TMEM copy guard; the vector buffer's release point
-turns out to be implied by the slot order.
+what the accumulate's release of A's slot, the warps' wait for dP, the
+issuer's wait for every warp's read of S and the producer's wait for the
+TMEM copy guard; the vector buffer's release point turns out to be implied
+by the slot order.
 """
 import heapq
 import random
@@ -35,43 +36,36 @@ WARPS = 4
 
 
 def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=True, vec_release_last=True,
-             producer_waits_q_copy=True, warp_cycles=(100, 1500)):
-    """Errors seen in one run of n steps of one CTA. The dQ pass (dk_pass
-    False) holds Q in TMEM: four slots, the first two holding the Q tile until
-    every warp has copied its row, and one TMEM buffer each for S and dP."""
+             producer_waits_copy=True, issuer_waits_s_read=True, warp_cycles=(100, 1500)):
+    """Errors seen in one run of n steps of one CTA."""
     rng = random.Random(seed)
     errors = []
-    nslots, nbuf = 4, 1                 # slots; TMEM buffers of S and of dP
-    full = [Barrier(1) for _ in range(nslots)]
-    empty = [Barrier(1) for _ in range(nslots)]
-    s_full = [Barrier(1) for _ in range(nbuf)]
-    dp_full = [Barrier(1) for _ in range(nbuf)]
-    ready = [Barrier(WARPS) for _ in range(nbuf)]
-    q_full, q_tmem = Barrier(1), Barrier(WARPS)
-    copied = set()
+    full = [Barrier(1), Barrier(1)]
+    empty = [Barrier(1), Barrier(1)]
+    s_full, s_read, dp_full = Barrier(1), Barrier(WARPS), Barrier(1)
+    ready = Barrier(WARPS)
     vec_full = [Barrier(1), Barrier(1)]
     vec_empty = [Barrier(WARPS), Barrier(WARPS)]
+    t_full, t_copied = Barrier(1), Barrier(WARPS)
     o_final = Barrier(1)
 
-    slot = [None] * nslots           # ("A" | "B", step) or ("Q",); None while a load is in flight
-    inflight = [False] * nslots
+    slot = [None, None]              # ("A" | "B", step) or ("T",); None while a load is in flight
+    inflight = [False, False]
     vec = [None, None]
-    s_buf, dp_buf = [None] * nbuf, [None] * nbuf   # step whose S / dP the buffer holds
-    read_s, read_dp = {}, {}                      # step -> warps that read it
-    ds_buf = [None, None]                         # (step, set of warps that wrote it)
+    sp = [None]                      # the score columns: ("S" | "dP", step)
+    read_s, read_dp = {}, {}         # step -> warps that read it
+    copied = set()
+    ds_buf = [None]                  # (step, set of warps that wrote it)
     done = {"S": -1, "dP": -1, "acc": -1}
     pipe = []
     clock = [0.0]
     events = []
 
     def a_slot(s):
-        return (2 * s + 2) & 3
+        return (s + 1) & 1
 
     def b_slot(s):
-        return (2 * s + 3) & 3
-
-    def buf(s):
-        return s % nbuf
+        return s & 1
 
     def wait(bar, parity, who, phase=None):
         yield ("wait", lambda: bar.passes(parity))
@@ -91,34 +85,31 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 op[1].arrive()
                 continue
             kind, s = op
-            x = s & 1
             if kind == "S":
                 if slot[a_slot(s)] != ("A", s):
                     errors.append(f"S({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
                 if len(copied) < WARPS:
                     errors.append(f"S({s}) read its TMEM operand before every warp copied its rows")
-                if s >= nbuf and len(read_s.get(s - nbuf, ())) < WARPS:
-                    errors.append(f"S({s}) overwrote S({s - nbuf}) before every warp read it")
+                if s > 0 and len(read_dp.get(s - 1, ())) < WARPS:
+                    errors.append(f"S({s}) overwrote dP({s - 1}) before every warp read it")
             elif kind == "dP":
                 if slot[b_slot(s)] != ("B", s):
                     errors.append(f"dP({s}) read slot {b_slot(s)} holding {slot[b_slot(s)]}")
-                if s >= nbuf and len(read_dp.get(s - nbuf, ())) < WARPS:
-                    errors.append(f"dP({s}) overwrote dP({s - nbuf}) before every warp read it")
+                if len(read_s.get(s, ())) < WARPS:
+                    errors.append(f"dP({s}) overwrote S({s}) before every warp read it")
             elif kind == "acc":
-                if ds_buf[x] is None or ds_buf[x][0] != s or len(ds_buf[x][1]) < WARPS:
-                    errors.append(f"accumulate({s}) read dS buffer {x} holding {ds_buf[x]}")
+                if ds_buf[0] is None or ds_buf[0][0] != s or len(ds_buf[0][1]) < WARPS:
+                    errors.append(f"accumulate({s}) read dS holding {ds_buf[0]}")
             yield ("delay", rng.uniform(100, 600))
             if kind == "acc" and slot[a_slot(s)] != ("A", s):
                 errors.append(f"accumulate({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
             done[kind] = s
-            if kind == "S":
-                s_buf[buf(s)] = s
-            elif kind == "dP":
-                dp_buf[buf(s)] = s
+            if kind in ("S", "dP"):
+                sp[0] = (kind, s)
 
     # ------------------------------------------------------------ producer
     def producer():
-        uses = [0] * nslots
+        uses = [0, 0]
 
         def land(i, what):
             def f():
@@ -132,20 +123,20 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 vec_full[x].complete_tx(1)
             return f
 
-        def land_q():
-            slot[0] = slot[1] = ("Q",)
-            q_full.complete_tx(1)
+        def land_t():
+            slot[0] = ("T",)
+            t_full.complete_tx(1)
 
         if n > 0:
             # the TMEM-bound operand (K in the dK pass, Q in the dQ pass) into
-            # slots 0 and 1, with the resident one (V or dO)
-            q_full.expect_tx(1)
-            q_full.arrive()
-            later(rng.uniform(300, 4000), land_q)
+            # slot 0, with the resident one (V or dO)
+            t_full.expect_tx(1)
+            t_full.arrive()
+            later(rng.uniform(300, 4000), land_t)
 
         def load(i, what):
-            if i < 2 and uses[i] == 0 and producer_waits_q_copy:
-                yield from wait(q_tmem, 0, "producer q_tmem", 0)
+            if i == 0 and uses[0] == 0 and producer_waits_copy:
+                yield from wait(t_copied, 0, "producer copied", 0)
             yield from wait(empty[i], (uses[i] & 1) ^ 1, "producer empty")
             uses[i] += 1
             if inflight[i]:
@@ -168,7 +159,7 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
 
     # ------------------------------------------------------------ issuer
     def issuer():
-        fulls = [0] * nslots
+        fulls = [0, 0]
 
         def wait_full(i):
             par = fulls[i] & 1
@@ -178,67 +169,67 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
         if n == 0:
             pipe.append(("commit", o_final))
             return
-        yield from wait(q_full, 0, "issuer q_full", 0)
-        yield from wait(q_tmem, 0, "issuer q_tmem", 0)
+        yield from wait(t_full, 0, "issuer t_full", 0)
+        yield from wait(t_copied, 0, "issuer copied", 0)
         yield from wait_full(a_slot(0))
-        pipe.extend([("S", 0), ("commit", s_full[0])])
+        pipe.extend([("S", 0), ("commit", s_full)])
         if not release_a_after_acc:
             pipe.append(("commit", empty[a_slot(0)]))
-        yield from wait_full(b_slot(0))
-        pipe.extend([("dP", 0), ("commit", dp_full[0]), ("commit", empty[b_slot(0)])])
         for s in range(n):
-            yield from wait(ready[buf(s)], (s // nbuf) & 1, "issuer ready", s // nbuf)
+            if issuer_waits_s_read:
+                yield from wait(s_read, s & 1, "issuer s_read", s)
+            yield from wait_full(b_slot(s))
+            pipe.extend([("dP", s), ("commit", dp_full), ("commit", empty[b_slot(s)])])
+            yield from wait(ready, s & 1, "issuer ready", s)
             pipe.append(("acc", s))
             if release_a_after_acc:
                 pipe.append(("commit", empty[a_slot(s)]))
             if s + 1 < n:
-                x = buf(s + 1)
                 yield from wait_full(a_slot(s + 1))
-                pipe.extend([("S", s + 1), ("commit", s_full[x])])
+                pipe.extend([("S", s + 1), ("commit", s_full)])
                 if not release_a_after_acc:
                     pipe.append(("commit", empty[a_slot(s + 1)]))
-                yield from wait_full(b_slot(s + 1))
-                pipe.extend([("dP", s + 1), ("commit", dp_full[x]), ("commit", empty[b_slot(s + 1)])])
         pipe.append(("commit", o_final))
 
     # ------------------------------------------------------------ warps
     def warp_role(w):
         if n > 0:
-            yield from wait(q_full, 0, f"warp {w} q_full", 0)
+            yield from wait(t_full, 0, f"warp {w} t_full", 0)
             yield ("delay", rng.uniform(50, 600))          # its rows of K or Q into TMEM
-            if slot[0] != ("Q",) or slot[1] != ("Q",):
-                errors.append(f"warp {w} copied Q from slots holding {slot[0]}, {slot[1]}")
+            if slot[0] != ("T",):
+                errors.append(f"warp {w} copied its TMEM operand from slot 0 holding {slot[0]}")
             copied.add(w)
-            q_tmem.arrive()
+            t_copied.arrive()
         for s in range(n):
-            x, v = buf(s), s & 1
-            yield from wait(s_full[x], (s // nbuf) & 1, f"warp {w} s_full", s // nbuf)
+            v = s & 1
+            yield from wait(s_full, s & 1, f"warp {w} s_full", s)
             if dk_pass:
                 yield from wait(vec_full[v], (s >> 1) & 1, f"warp {w} vec_full", s >> 1)
                 if vec[v] != s:
                     errors.append(f"warp {w} read LSE of step {s} from buffer {v} holding {vec[v]}")
-            if s_buf[x] != s:
-                errors.append(f"warp {w} read S({s}) from buffer {x} holding {s_buf[x]}")
+            if sp[0] != ("S", s):
+                errors.append(f"warp {w} read S({s}) from score columns holding {sp[0]}")
+            yield ("delay", rng.uniform(*warp_cycles))          # S read, P formed
             read_s.setdefault(s, set()).add(w)
-            yield ("delay", rng.uniform(*warp_cycles))          # P from S
+            s_read.arrive()
             if warps_wait_dp:
-                yield from wait(dp_full[x], (s // nbuf) & 1, f"warp {w} dp_full", s // nbuf)
-            if dp_buf[x] != s:
-                errors.append(f"warp {w} read dP({s}) from buffer {x} holding {dp_buf[x]}")
+                yield from wait(dp_full, s & 1, f"warp {w} dp_full", s)
+            if sp[0] != ("dP", s):
+                errors.append(f"warp {w} read dP({s}) from score columns holding {sp[0]}")
             read_dp.setdefault(s, set()).add(w)
             if dk_pass and not vec_release_last:
                 vec_empty[v].arrive()
                 yield ("delay", rng.uniform(0, 400))
             if dk_pass and vec[v] != s:
                 errors.append(f"warp {w} read D of step {s} from buffer {v} holding {vec[v]}")
-            # dS buffer v was last read by the accumulate of step s - 2
-            if s >= 2 and done["acc"] < s - 2:
-                errors.append(f"warp {w} wrote dS({s}) before the accumulate of step {s - 2} read the buffer")
+            # the single dS buffer was last read by the accumulate of step s - 1
+            if s >= 1 and done["acc"] < s - 1:
+                errors.append(f"warp {w} wrote dS({s}) before the accumulate of step {s - 1} read the buffer")
             yield ("delay", rng.uniform(*warp_cycles))
-            if ds_buf[v] is None or ds_buf[v][0] != s:
-                ds_buf[v] = (s, set())
-            ds_buf[v][1].add(w)
-            ready[x].arrive()
+            if ds_buf[0] is None or ds_buf[0][0] != s:
+                ds_buf[0] = (s, set())
+            ds_buf[0][1].add(w)
+            ready.arrive()
             if dk_pass and vec_release_last:
                 vec_empty[v].arrive()
         yield from wait(o_final, 0, f"warp {w} o_final", 0)
@@ -312,7 +303,14 @@ def test_slots_0_1_must_wait_for_the_tmem_copy(dk_pass):
     """K (dK pass) or Q (dQ pass) lands in slots 0 and 1 and each warp copies
     its rows into TMEM; a load into those slots before every warp has copied
     would overwrite the operand under a warp still reading it."""
-    assert bad_runs(dk_pass, producer_waits_q_copy=False) > 0
+    assert bad_runs(dk_pass, producer_waits_copy=False) > 0
+
+
+@pytest.mark.parametrize("dk_pass", [True, False])
+def test_dp_must_wait_until_every_warp_read_s(dk_pass):
+    """S and dP share the score columns: dP_s may go in only once every warp
+    has read S_s."""
+    assert bad_runs(dk_pass, issuer_waits_s_read=False) > 0
 
 
 def test_vector_release_is_implied_by_the_slot_order():
