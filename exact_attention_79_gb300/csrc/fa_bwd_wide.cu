@@ -538,10 +538,10 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S^T_0; per step t: [Q_{t+1} landed] S^T_{t+1} into the other buffer
-    // (its P^T_{t-1} was read by dV_{t-1}, issued before), then [P^T_t
-    // written, dO_t landed] dV_t. Each S^T frees Q's buffer once it completes,
-    // each dV frees dO's.
+    // S^T_0; per step t: [P^T_t written, dO_t landed] dV_t, then [Q_{t+1}
+    // landed] S^T_{t+1} into the other buffer. Each S^T frees Q's buffer once
+    // it completes, each dV frees dO's. (S^T_{t+1} first put Q_{t+1}'s load in
+    // front of dV_t.)
     if (lane == 0) {
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || mbar_wait(bar_k_full, 0, abort_flag, deadline));
@@ -567,11 +567,6 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         }
       }
       for (int t = 0; t < nsteps && ok; ++t) {
-        if (t + 1 < nsteps) {
-          if (!(ok = mbar_wait(bar_q_full, (t + 1) & 1, abort_flag, deadline))) break;
-          tc_fence_after();
-          scores(t + 1);
-        }
         if (!(ok = mbar_wait(bar_ready(t & 1), (t >> 1) & 1, abort_flag, deadline))) break;
         if (!(ok = mbar_wait(bar_do_full, t & 1, abort_flag, deadline))) break;
         tc_fence_after();
@@ -581,6 +576,13 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         for (int kk = 0; kk < kBM / 16; ++kk)
           mma_bf16_ts(tbase + kWColAcc, a + kk * 8, desc_add(dod, kk * 16 * 128), id_v, t > 0 || kk > 0);
         mma_commit(bar_do_empty);
+        if (t + 1 < nsteps) {
+          // S^T_{t+1} into the other buffer, whose P^T_{t-1} dV_{t-1} (issued
+          // before) has read
+          if (!(ok = mbar_wait(bar_q_full, (t + 1) & 1, abort_flag, deadline))) break;
+          tc_fence_after();
+          scores(t + 1);
+        }
       }
       if (ok) mma_commit(bar_o_final);
     }
