@@ -96,7 +96,7 @@ WORKLOADS = {
     "fp8_h16_n8192_d128_causal_fwd": Workload("fp8_h16_n8192_d128_causal_fwd", "fp8e4m3", 1, 16, 16, 8192, 128, True, False),
     # head dimension 256 (forward; the wide-head kernel), same N and heads as the d = 128 fwd+bwd case
     "bf16_h16_n8192_d256_causal_fwd": Workload("bf16_h16_n8192_d256_causal_fwd", "bf16", 1, 16, 16, 8192, 256, True, False),
-    # head dimension 256, forward + backward (the backward in three passes over 64-row sub-tiles)
+    # head dimension 256, forward + backward (the backward in three passes over 128-row steps)
     "bf16_h16_n8192_d256_causal_fwdbwd": Workload("bf16_h16_n8192_d256_causal_fwdbwd", "bf16", 1, 16, 16, 8192, 256, True, True),
     # FP8 at head dimension 256 (the one-tile-per-CTA e4m3 kernel)
     "fp8_h16_n8192_d256_causal_fwd": Workload("fp8_h16_n8192_d256_causal_fwd", "fp8e4m3", 1, 16, 16, 8192, 256, True, False),

@@ -1,5 +1,5 @@
 """The backward at head dimensions 136..256 (csrc/fa_bwd_wide.cu: dV, dK and
-dQ in three passes over 64-row sub-tiles, no atomics) through fa_bwd,
+dQ in three passes over 128-row steps, no atomics) through fa_bwd,
 fa_bwd_kv, fa_bwd_deterministic and fa_bwd_noalloc, against the
 double-precision oracle on the same rounded inputs: gradients within the
 relative Frobenius bound, bit-identical from run to run and across the entry
@@ -34,7 +34,7 @@ def check_grads(got, ref):
 CASES = [
     # B, Hq, Hkv, Nq, Nk, d, causal
     (1, 2, 2, 128, 128, 256, True),
-    (1, 2, 2, 64, 64, 256, False),       # one 64-row sub-tile, half a key tile
+    (1, 2, 2, 64, 64, 256, False),       # half a 128-row step, half a key tile
     (2, 4, 2, 333, 333, 256, True),      # ragged rows and keys, GQA
     (1, 2, 1, 700, 700, 192, False),     # d = 192 in the 256 build
     (1, 3, 3, 300, 300, 136, True),
