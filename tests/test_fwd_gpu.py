@@ -86,6 +86,39 @@ def test_fwd_workload_sampled_rows(fa, name):
     assert np.isfinite(o).all() and np.isfinite(lse).all()
 
 
+def test_fwd_longest_sequence_sampled_rows(fa):
+    """N = 131072, the longest sequence a block mask can describe (1024 query
+    tiles): the dense causal forward with two query heads on one KV head, and
+    the block-sparse forward with a local window of 8 key tiles. 128 seeded
+    query rows per head, the first and the last row among them, against the
+    oracle."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 131072, 128
+    scale = d ** -0.5
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=131072)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    inner = inputs.sample_rows(B, Hq, N - 2, 126, seed=4) + 1          # rows 1 .. N-2
+    ends = np.broadcast_to(np.array([0, N - 1]), (B, Hq, 2))
+    rows = np.sort(np.concatenate([inner, ends], axis=2), axis=2)
+    bi = np.arange(B)[:, None, None]
+    hi = np.arange(Hq)[None, :, None]
+
+    o, lse = run_fwd(fa, t, True, scale)
+    ro, rl = oracle.forward_rows(f["q"], f["k"], f["v"], True, scale, rows)
+    print("dense", check_fwd(o[bi, hi, rows], lse[bi, hi, rows], ro, rl, "dense N=131072"))
+
+    T = N // 128
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    m = ((j <= i) & (j > i - 8))[None, None]
+    dev = torch.device("cuda:0")
+    q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
+    os_, ls_ = fa.fwd(q, k, v, causal=True, scale=scale, block_mask=torch.from_numpy(m.astype(np.uint8)).to(dev))
+    fa.check_device_status()
+    os_, ls_ = os_.float().cpu().numpy(), ls_.cpu().numpy()
+    ro, rl = oracle.forward_rows(f["q"], f["k"], f["v"], True, scale, rows, block_mask=m)
+    print("local window", check_fwd(os_[bi, hi, rows], ls_[bi, hi, rows], ro, rl, "block-sparse N=131072"))
+
+
 def test_fwd_n8192_full(fa):
     w = configs.WORKLOADS["bf16_h16_n8192_d128_causal_fwdbwd"]
     t = inputs.make_workload_inputs(w, with_grad=False)
