@@ -61,6 +61,34 @@ def test_bwd_edge_sizes(fa, B, Hq, Hkv, N, d, causal):
     assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
 
 
+@pytest.mark.parametrize("d,deterministic", [(128, False), (128, True), (64, False), (256, False)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_sharp_logits(fa, d, deterministic, causal):
+    """Q scaled by 4, as in the second run of the d = 64 forward workload: the
+    logits spread to ~+-20 and most rows put nearly all their weight on a few
+    keys. The recomputed probabilities 2^(s scale log2 e - LSE log2 e) then
+    sit at both ends of their range, and the running max grows across tiles.
+    One-pass (d = 64, 128), deterministic two-pass and three-pass (d = 256)
+    backwards against the oracle."""
+    B, Hq, Hkv, N = 1, 2, 1, 700
+    scale = d ** -0.5
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=4000 + d, with_grad=True, q_mult=4.0)
+    dev = torch.device("cuda:0")
+    g = {k: v.to(dev) for k, v in t.items()}
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=causal, scale=scale,
+                        deterministic=deterministic)
+    fa.check_device_status()
+    o, lse, dq, dk, dv = (x.float().cpu().numpy() for x in (o, lse, dq, dk, dv))
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    ro, rl, rdq, rdk, rdv = oracle.backward(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    assert np.abs(o - ro).max() <= configs.TOL_O_MAX
+    assert np.abs(lse - rl).max() <= configs.TOL_LSE_MAX
+    errs = {n: rel_fro(x, r) for n, x, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv))}
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+
+
 def test_bwd_n8192_full(fa):
     """Forward + backward, B=1, H=16, N=8192, d=128, causal: every element."""
     w = configs.WORKLOADS["bf16_h16_n8192_d128_causal_fwdbwd"]
