@@ -126,6 +126,31 @@ def test_bwd_n65536_sampled_rows(fa):
     assert all(np.isfinite(x).all() for x in (dq, dk, dv))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_ragged_head_groups(fa, causal):
+    """The dK/dV kernel walks KV heads in groups whose Q, dO and fp32 dQ
+    accumulator fit in 64 MB of L2: at N = 12288 with two query heads per KV
+    head that is two KV heads per group, so three KV heads make groups of 2
+    and 1. 256 seeded query rows and key rows per head against the oracle."""
+    B, Hq, Hkv, N, d = 1, 6, 3, 12288, 128
+    scale = d ** -0.5
+    assert (64 << 20) // (8 * (Hq // Hkv) * N * 128) == 2
+    t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=12288 + causal, with_grad=True)
+    o, lse, dq, dk, dv = run_fwd_bwd(fa, t, causal, scale)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    qr = inputs.sample_rows(B, Hq, N, 256, seed=1)
+    kr = inputs.sample_rows(B, Hkv, N, 256, seed=2)
+    rl_all, rD_all = oracle.row_statistics(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    rdq, rdk, rdv = oracle.backward_rows(f["q"], f["k"], f["v"], f["do"], causal, scale, qr, kr, rl_all, rD_all)
+    bq = np.arange(B)[:, None, None]
+    hq = np.arange(Hq)[None, :, None]
+    hk = np.arange(Hkv)[None, :, None]
+    assert np.abs(lse - rl_all).max() <= configs.TOL_LSE_MAX
+    errs = {"dq": rel_fro(dq[bq, hq, qr], rdq), "dk": rel_fro(dk[bq, hk, kr], rdk), "dv": rel_fro(dv[bq, hk, kr], rdv)}
+    assert max(errs.values()) <= configs.TOL_GRAD_REL_FRO, errs
+    assert all(np.isfinite(x).all() for x in (dq, dk, dv))
+
+
 def test_bwd_dk_dv_deterministic(fa):
     B, Hq, Hkv, N, d = 1, 8, 2, 700, 128
     t = inputs.make_inputs(B, Hq, Hkv, N, d, "bf16", seed=9, with_grad=True)
