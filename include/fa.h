@@ -53,6 +53,12 @@
  *   Threads: calls may come from several host threads; each call is
  *     independent, and device-side failures are reported per stream (see
  *     fa_device_status).
+ *   CUDA graphs: every call can be captured on a stream and replayed (launch
+ *     parameters, tensor maps included, are passed by value; nothing is
+ *     allocated). Make one ordinary call on the device first: it does the
+ *     one-time set-up (architecture check, device addresses of the status
+ *     words), which is not meant to run inside a capture. A replay reads and
+ *     writes the captured buffers as they are at replay time.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
