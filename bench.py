@@ -40,6 +40,7 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-sets", type=int, default=3, help="device buffer sets the end-to-end pipeline rotates over")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd", choices=["fused", "deterministic"], default="fused",
@@ -525,41 +526,46 @@ def native_arm(args, w):
     # ---- end to end: pinned host inputs -> device, the path, results -> host,
     # every step. Steps are pipelined the way a user would drive the library:
     # the copy in of step i+1 and the copy out of step i-1 run on their own
-    # streams while step i computes, over two sets of device buffers.
+    # streams while step i computes, over NSETS sets of device buffers (with
+    # two, step i's compute must wait for step i-2's results to leave, which
+    # ties the compute stream to the copy-out stream; three leave it a step
+    # of slack).
     e2e = None
     if args.e2e_steps > 0:
         names_in = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
         names_out = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
         host_in = [getattr(main, n).cpu().pin_memory() for n in names_in]
+        nsets = args.e2e_sets
         host_out = [[torch.empty(getattr(main, n).shape, dtype=getattr(main, n).dtype).pin_memory()
-                     for n in names_out] for _ in range(2)]
+                     for n in names_out] for _ in range(nsets)]
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = sum(x.numel() * x.element_size() for x in host_out[0])
-        sets = [main, Bufs()]
-        for n in names_in + names_out:
-            setattr(sets[1], n, torch.empty_like(getattr(main, n)))
-        if fp8:
-            for n in ("q8", "qs", "k8", "ks", "vt8", "vs"):
-                setattr(sets[1], n, torch.empty_like(getattr(main, n)))
+        sets = [main] + [Bufs() for _ in range(nsets - 1)]
+        for extra in sets[1:]:
+            for n in names_in + names_out:
+                setattr(extra, n, torch.empty_like(getattr(main, n)))
+            if fp8:
+                for n in ("q8", "qs", "k8", "ks", "vt8", "vs"):
+                    setattr(extra, n, torch.empty_like(getattr(main, n)))
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         s_comp = stream
-        done_in = [torch.cuda.Event() for _ in range(2)]
-        done_comp = [torch.cuda.Event() for _ in range(2)]
-        done_out = [torch.cuda.Event() for _ in range(2)]
-        started = [False, False]
+        done_in = [torch.cuda.Event() for _ in range(nsets)]
+        done_comp = [torch.cuda.Event() for _ in range(nsets)]
+        done_out = [torch.cuda.Event() for _ in range(nsets)]
+        started = [False] * nsets
 
         def e2e_step(i):
-            x = i % 2
+            x = i % nsets
             b = sets[x]
             with torch.cuda.stream(s_in):
                 if started[x]:
-                    s_in.wait_event(done_comp[x])       # step i-2 has finished reading set x
+                    s_in.wait_event(done_comp[x])       # step i-nsets has finished reading set x
                 for n, src in zip(names_in, host_in):
                     getattr(b, n).copy_(src, non_blocking=True)
                 done_in[x].record(s_in)
             s_comp.wait_event(done_in[x])
             if started[x]:
-                s_comp.wait_event(done_out[x])          # step i-2's results have left set x
+                s_comp.wait_event(done_out[x])          # step i-nsets's results have left set x
             run(b, s_comp.cuda_stream, lambda _i: None, quantize=True)
             done_comp[x].record(s_comp)
             with torch.cuda.stream(s_out):
@@ -569,14 +575,14 @@ def native_arm(args, w):
                 done_out[x].record(s_out)
             started[x] = True
 
-        for i in range(4):
+        for i in range(2 * nsets):
             e2e_step(i)
         torch.cuda.synchronize(dev)
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s_in)
         for i in range(args.e2e_steps):
             e2e_step(i)
-        for x in range(2):
+        for x in range(nsets):
             s_out.wait_event(done_out[x])
         z.record(s_out)
         torch.cuda.synchronize(dev)
@@ -584,7 +590,7 @@ def native_arm(args, w):
         fa.check_device_status(stream.cuda_stream)
         e2e = {"value": world * flops_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "pipelining": "copy in, compute, copy out on three streams over two device buffer sets"}
+               "pipelining": f"copy in, compute, copy out on three streams over {nsets} device buffer sets"}
 
     if rank != 0:
         return
