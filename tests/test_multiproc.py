@@ -77,3 +77,42 @@ def test_exp_roofline_and_percentiles_arithmetic():
     p = bench.percentiles([5.0, 1.0, 3.0, 2.0, 4.0, 6.0, 7.0, 8.0, 9.0, 10.0, 11.0])
     assert p == {"p10": 2.0, "p50": 6.0, "p90": 10.0}
     assert bench.percentiles([]) is None
+
+
+def test_reference_arm_line_on_cpu():
+    """Rank 0 of the reference arm runs the oracle on the host and prints one
+    JSON line with the contract's keys; its e2e moves no bytes."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["config"]["workload"] == "bf16_h16_n8192_d128_causal_fwdbwd"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"]
+
+
+def test_clock_summary_rules():
+    """Fewer than three nvidia-smi samples inside the timed window are never
+    reported as the timed clock; the kernels' own clock wins when given; any
+    throttle reason seen during the run is listed."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    row = lambda mhz, slow="Not Active", cap="Not Active": ["ts", str(mhz), "2070", "900", "0x0", slow, "Not Active",
+                                                           "Not Active", cap]
+    cs.rows = [(0.5, row(2070)), (1.5, row(1900, cap="Active")), (2.5, row(1950)), (9.0, row(2070))]
+    out = cs.summary(1.0, 2.0)                      # one sample inside
+    assert out["in_window"] == 1 and "smi_sm_mhz_in_window" not in out and out["sm_mhz"] is None
+    assert out["reasons"] == ["sw_power_cap"] and out["sm_max_mhz"] == 2070.0
+    out = cs.summary(1.0, 2.0, kernel_mhz=1923.0)
+    assert out["sm_mhz"] == 1923.0 and "timed kernels" in out["sm_mhz_source"]
+    cs.rows += [(1.6, row(1910)), (1.7, row(1920, slow="Active"))]
+    out = cs.summary(1.0, 2.0)                      # three inside
+    assert out["smi_sm_mhz_in_window"] == 1910.0 and out["sm_mhz"] == 1910.0
+    assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
