@@ -174,8 +174,8 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt, float* scales, int BH, int 
  * [B, Hq, N, d], lse fp32 [B, Hq, N]. The products run on e4m3 tensor cores
  * with fp32 accumulation. Contract on the probabilities: each P_ij is taken
  * relative to a reference no larger than the row's true running maximum
- * (this build lets it trail by up to a factor 2^4), scaled by a power of two
- * >= 1 (this build: 2^4) and rounded to the nearest e4m3 value below 448
+ * (this library lets it trail by up to a factor 2^4), scaled by a power of two
+ * >= 1 (this library: 2^4) and rounded to the nearest e4m3 value below 448
  * before the P V product; the row sum and the LSE use the unrounded values.
  * With P_ij = exp(s_ij - max_j s_ij) and l_i = sum_j P_ij, the result then
  * differs from the exact attention of the dequantised inputs by at most
