@@ -13,12 +13,20 @@
 //    groups against the tensor core ("Flash Attention V3技术解析" 1.2);
 //  * causal blocks above the diagonal skipped ("Flash Attention V3技术解析" 2.1).
 //
-// GB300 mapping. One CTA = two 128-row query tiles of one (batch, head):
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a slot ring
-//   warp 1      tensor-core issuer (one thread) + TMEM owner
-//   warps 2-5   softmax group 0 (query tile 0), one thread per query row
-//   warps 6-9   softmax group 1 (query tile 1)
-//   warp 10     (bf16) ring watcher: waits for V_j and K_{j+1} to land and
+// GB300 mapping. One CTA = two 128-row query tiles of one (batch, head).
+// bf16 (384 threads, three warpgroups):
+//   warps 0-3   softmax group 0 (query tile 0), one thread per query row
+//   warps 4-7   softmax group 1 (query tile 1)
+//   warp 8      TMA producer: Q tiles once, then K_j, V_j into a slot ring
+//   warp 9      tensor-core issuer (one thread)
+//   warp 10     ring watcher (below); warp 11 has no role
+// The softmax warpgroups take registers from the last one (setmaxnreg): 184
+// per thread against 120, where one register budget for all would be 168,
+// at which the softmax spills. They come first: the schedulers favour lower
+// warp indices, and with the watcher ahead of them the long-sequence forward
+// ran 4-8% slower. fp32 (320 threads): warp 0 producer, warp 1 issuer, warps
+// 2-5 the single tile's softmax.
+//   ring watcher (bf16): waits for V_j and K_{j+1} to land and
 //               adds one arrival to each group's P-ready barrier, so the
 //               issuer learns "P_j written and its operands resident" from a
 //               single barrier; it also hands ring slots back to the producer
@@ -48,7 +56,13 @@ struct FwdCfg {
   // loaded into the slot the producer got back two tiles ago, and a shallow
   // ring leaves its TMA latency exposed to the tensor core at every tile.
   static constexpr int kStages = kTf32 ? 3 : ((kTileBytes == 16384) ? 12 : 5);
-  static constexpr int kThreads = kTf32 ? 320 : 352;      // bf16 adds the ring watcher warp
+  static constexpr int kThreads = kTf32 ? 320 : 384;      // bf16: softmax warpgroups 0-1, then producer, issuer, watcher, idle
+  static constexpr int kSm0 = kTf32 ? 2 : 0;              // first softmax warp
+  static constexpr int kProd = kTf32 ? 0 : 8, kIss = kTf32 ? 1 : 9;
+  // bf16 register split (setmaxnreg): 256 softmax threads x 184 + 128 x 120 = 62464
+  // of the 384 x 168 = 64512 the CTA is launched with
+  static constexpr uint32_t kRegsSoftmax = 184, kRegsOther = 120;
+  static_assert(kTf32 || 256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }
   static __device__ __forceinline__ uint32_t col_o(int i) { return 256u + D * i; }
@@ -136,7 +150,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 }
 
 template <typename T, int D, bool kSparse>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(FwdCfg<T, D>::kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const FwdParams p) {
@@ -258,8 +272,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   // key tile of step j
   auto kv_tile = [&](int j) -> int { return kSparse ? (tile_list[j] & 0x3FFF) : j; };
 
-  if (warp == 0) {
+  if (warp == C::kProd) {
     // ------------------------------------------------------------ producer
+    if constexpr (C::kPingPong) setmaxnreg_dec<C::kRegsOther>();
     if (lane == 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
@@ -282,8 +297,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == C::kIss) {
     // ------------------------------------------------------------ tensor-core issuer
+    if constexpr (C::kPingPong) setmaxnreg_dec<C::kRegsOther>();
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(C::kFmt, 128, 128, 0, 0);
       const uint32_t idesc_pv = make_idesc(C::kFmt, 128, D, 0, C::kTf32 ? 0 : 1);
@@ -352,9 +368,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       }
     }
     __syncwarp();
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ ring watcher (bf16)
-    if (C::kPingPong && lane == 0) {
+  } else if (C::kPingPong && warp >= 10) {
+    // ------------------------------------------------------------ ring watcher (bf16; warp 11 idle)
+    setmaxnreg_dec<C::kRegsOther>();
+    if (warp == 10 && lane == 0) {
       // L: the group whose S MMAs are issued last in each step (group 1 unless absent)
       const int L = (nkv[1] == nmax) ? 1 : 0;
       // parity waits only tell phase k from phase k-1: observe every phase of
@@ -390,7 +407,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax groups
-    const int g = (warp - 2) >> 2;                 // 0 or 1
+    if constexpr (C::kPingPong) setmaxnreg_inc<C::kRegsSoftmax>();
+    const int g = (warp - C::kSm0) >> 2;           // 0 or 1
     const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;           // query row within the tile
     const int n_kv = nkv[g];
@@ -599,7 +617,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // so a timeout in one warp cannot leave the others stuck on the barrier;
     // a warp that gave up has raised the abort flag, and then nothing is stored
     named_bar_sync(1 + g, 128);
-    if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {
+    if (has_tile[g] && !*abort_flag && warp == C::kSm0 + 4 * g && lane == 0) {
       for (int bx = 0; bx < C::kNBox; ++bx)
         tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * C::kChunk, qt[g] * kBM, bh);
       tma_store_commit();
