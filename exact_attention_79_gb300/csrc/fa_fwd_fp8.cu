@@ -44,7 +44,13 @@ constexpr int kD = 128;                  // head dimension of the kernel (a smal
 constexpr int kTile = 128 * 128;         // 128 rows x 128 e4m3 codes: one TMA box
 constexpr int kQRegion = 2 * kTile;      // a query tile's region: its codes and P buffer 0, later its bf16 O
 constexpr int kStages = 8;               // K / V^T ring slots
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;   // softmax warps 0-7, producer 8, issuer 9, watcher 10, idle 11
+// Registers move from the last warpgroup to the two softmax warpgroups
+// (setmaxnreg): 256 x 184 + 128 x 120 of the 384 x 168 launched. Softmax
+// warps first: the schedulers favour lower warp indices (+2% from the order,
+// +1% more from the registers, bit-identical).
+constexpr uint32_t kRegsSoftmax = 184, kRegsOther = 120;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
 constexpr int kBarBytes = 512;
 constexpr int kSmem = 2 * kQRegion + 2 * kTile + kStages * kTile + kBarBytes + 1024;   // + P buffers 1
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -168,7 +174,7 @@ __global__ void fp8_v_scale_kernel(unsigned* __restrict__ amax_bits, int count) 
 }
 
 // ------------------------------------------------------------------ attention
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_vt, const __grid_constant__ CUtensorMap map_o,
                const FwdParams p) {
@@ -253,8 +259,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
-  if (warp == 0) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
@@ -276,8 +283,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ tensor-core issuer
+    setmaxnreg_dec<kRegsOther>();
     // Per key tile j: S_i(j+1) for each query tile as soon as its softmax has
     // read S_i(j) out of TMEM (and K_{j+1} has landed), then P_i(j) V_j as
     // soon as P_i(j) is in shared memory (and V_j has landed). Ring slots go
@@ -339,13 +347,14 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 10) {
+  } else if (warp >= 10) {
     // ------------------------------------------------------------ ring watcher
+    setmaxnreg_dec<kRegsOther>();
     // Folds "V_j landed" into P-ready(i, j) and "K_{j+1} landed" into
     // S-consumed(i, j). Parity waits only tell phase k from phase k-1, so it
     // observes every load in ring order (K_0 included) and arrives for a
     // phase only once the previous phase of that barrier has completed.
-    if (lane == 0) {
+    if (warp == 10 && lane == 0) {
       bool ok = nmax == 0 || mbar_wait(bar_kv_full(0), 0, abort_flag, deadline);
       for (int j = 0; j < nmax && ok; ++j) {
         const int cv = 2 * j + 1;
@@ -368,7 +377,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax groups
-    const int g = (warp - 2) >> 2;
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int g = warp >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int n_kv = nkv[g];
@@ -526,7 +536,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         p.lse[static_cast<size_t>(bh) * p.N + q_row] = l > 0.f ? (m + log2f(l) - 4.0f) * kLn2 : -INFINITY;
     }
     named_bar_sync(1 + g, 128);
-    if (has_tile[g] && !*abort_flag && warp == 2 + 4 * g && lane == 0) {
+    if (has_tile[g] && !*abort_flag && warp == 4 * g && lane == 0) {
       // 64-column boxes; one that would start at or past d (d <= 64) is skipped
       for (int bx = 0; bx < 2; ++bx)
         if (bx * 64 < p.head_dim) tma_store_3d(&map_o, s_q[g] + bx * kBoxBytes, bx * 64, qt[g] * kBM, bh);
