@@ -12,17 +12,17 @@
 // head dimensions up to 256: "Flash Attention-2", section
 // "Снижение накладных расходов".
 //
-// 352 threads:
-//   warp 0      TMA producer: Q once, then K_j and V^T_j tiles into a ring of
-//               slots (one tile each), in the order the tensor core consumes them
-//   warp 1      tensor-core issuer (one thread) + TMEM owner
-//   warps 2-9   softmax: two warps per TMEM lane quarter, one per 64-key half
+// 384 threads:
+//   warps 0-7   softmax: two warps per TMEM lane quarter, one per 64-key half
 //               of each 128-key tile, so each thread of a row pair works on 64
 //               logits; the two halves agree on the row max through a shared-
 //               memory exchange guarded by an mbarrier (bounded wait) and keep
 //               separate partial row sums, added once at the end
+//   warp 8      TMA producer: Q once, then K_j and V^T_j tiles into a ring of
+//               slots (one tile each), in the order the tensor core consumes them
+//   warp 9      tensor-core issuer (one thread)
 //   warp 10     ring watcher: folds "V_j landed" into the P-ready barrier of
-//               step j, observing every load in ring order
+//               step j, observing every load in ring order; warp 11 idle
 // An e4m3 row of D codes is D/128 boxes of 128 bytes: Q, a K tile ([128 keys x
 // D]) and a V^T tile ([D rows x 128 keys], boxes at y = 0 and 128 adjacent, so
 // one K-major descriptor with N = D spans them) take D x 128 bytes each. TMEM:
@@ -53,7 +53,12 @@ struct W8Cfg {
   static constexpr int kBoxes = D / 128;                     // 128-byte boxes along d
   static constexpr int kTile = kBoxes * kBoxBytes;           // Q, a K tile or a V^T tile
   static constexpr int kSlots = 6 * 32768 / kTile;           // 6 (D = 256) or 12 (D = 128)
-  static constexpr int kThreads = 352;
+  // softmax warps 0-7 (two per row), then producer 8, issuer 9, watcher 10,
+  // idle 11; the softmax warpgroups take registers from the last one
+  // (setmaxnreg) and come first, as the schedulers favour lower warp indices
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsSoftmax = 184, kRegsOther = 120;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
   static constexpr int kBarBytes = 384;
   static constexpr int kXchgBytes = 2 * 2 * 128 * 4;         // [step parity][half][row] fp32
   static constexpr int kLayout = kTile + kSlots * kTile + kBarBytes + kXchgBytes;
@@ -79,7 +84,7 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
 fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_vt, const __grid_constant__ CUtensorMap map_o,
                     const FwdParams p) {
@@ -169,8 +174,9 @@ fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
-  if (warp == 0) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<C::kRegsOther>();
     if (lane == 0 && n > 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
@@ -198,8 +204,9 @@ fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ tensor-core issuer
+    setmaxnreg_dec<C::kRegsOther>();
     if (lane == 0 && n > 0) {
       const uint32_t idesc_qk = make_idesc(0, 128, 128, 0, 0);     // e4m3, both K-major
       const uint32_t idesc_pv = make_idesc(0, 128, D, 0, 0);       // A = P (TMEM), B = V^T K-major, N = D
@@ -246,13 +253,14 @@ fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       if (ok) mma_commit(bar_o_final);
     }
     __syncwarp();
-  } else if (warp == 10) {
+  } else if (warp >= 10) {
     // ------------------------------------------------------------ ring watcher
+    setmaxnreg_dec<C::kRegsOther>();
     // Parity waits only tell phase k from phase k-1: every load is observed in
     // ring order, K loads only after the step's arrival (their latency never
     // holds P V back); a phase is arrived for only once its previous phase on
     // the same barrier has completed.
-    if (lane == 0 && n > 0) {
+    if (warp == 10 && lane == 0 && n > 0) {
       auto landed = [&](int it) {
         return mbar_wait(bar_full(it % C::kSlots), (it / C::kSlots) & 1, abort_flag, deadline);
       };
@@ -268,7 +276,8 @@ fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int half = (warp - 2) >> 2;              // keys [64 half, 64 half + 64) of each tile
+    setmaxnreg_inc<C::kRegsSoftmax>();
+    const int half = warp >> 2;                    // keys [64 half, 64 half + 64) of each tile
     const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -423,7 +432,7 @@ fwd_fp8_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         p.lse[static_cast<size_t>(bh) * p.N + q_row] = l_row > 0.f ? (m + log2f(l_row) - 4.0f) * kLn2 : -INFINITY;
     }
     named_bar_sync(1, 256);
-    if (!*abort_flag && warp == 2 && lane == 0) {
+    if (!*abort_flag && warp == 0 && lane == 0) {
       // 64-column boxes; one that would start at or past d is skipped
       for (int bx = 0; bx < D / 64; ++bx)
         if (bx * 64 < p.head_dim) tma_store_3d(&map_o, s_ring + bx * kBoxBytes, bx * 64, qt * kBM, bh);
