@@ -24,9 +24,10 @@
 // bwd_pre_kernel (fa_bwd.cu) writes D and the base-2 LSE first. The dK and dQ
 // passes keep K or Q in TMEM as the A operand of the scores.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
-// (one thread), warps 2-5 one thread per TMEM lane (key row in the dV and dK
-// passes, query row in the dQ pass).
+// Roles (320 threads): warps 0-7 two per TMEM lane quarter, each thread one
+// lane (key row in the dV and dK passes, query row in the dQ pass) and one
+// half of the step's 128 score columns (warps 0-3 the first, 4-7 the second);
+// warp 8 TMA producer, warp 9 MMA issuer (one thread); warp 1 owns TMEM.
 #include <algorithm>
 
 #include "fa_common.cuh"
@@ -38,7 +39,8 @@ namespace {
 
 constexpr int kWD = 256;                          // head-dimension build
 constexpr int kWTile = kWD / 64 * kBoxBytes;      // [128, 256] bf16: 64 KB
-constexpr int kWThreads = 192;
+constexpr int kWThreads = 320;
+constexpr int kWProd = 8, kWIss = 9;           // producer and issuer warps
 constexpr uint32_t kWColAcc = 0;                  // TMEM: the dK, dV or dQ accumulator in columns 0-255
 
 // 64 fp32 TMEM columns of this thread's lane
@@ -63,11 +65,11 @@ __device__ __forceinline__ void store_row64(uint32_t box, int row, const float (
                  : "memory");
 }
 
-// The 256 fp32 accumulator columns of this thread's lane, times `mul`, as
-// row `row` of a [128, 256] bf16 tile (four 128-row boxes) at `stg`
-__device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int row, float mul) {
+// Accumulator columns [128 half, 128 half + 128) of this thread's lane, times
+// `mul`, into row `row` of a [128, 256] bf16 tile (four 128-row boxes) at `stg`
+__device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int row, float mul, int half) {
 #pragma unroll
-  for (int c0 = 0; c0 < kWD; c0 += 32) {
+  for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
     uint32_t t[32];
     tmem_ld_32x32b_x32(taddr + c0, t);
     tmem_wait_ld();
@@ -112,7 +114,7 @@ struct WideDkCfg {
   static_assert(kLayout <= kSmemAlloc, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kWThreads, 1)
 wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dk, const BwdParams p) {
@@ -173,13 +175,13 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
       mbar_init(bar_vec_full(i), 1);
-      mbar_init(bar_vec_empty(i), 128);
+      mbar_init(bar_vec_empty(i), 256);
     }
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_read, 128);
+    mbar_init(bar_s_read, 256);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_ready, 128);
-    mbar_init(bar_k_tmem, 128);
+    mbar_init(bar_ready, 256);
+    mbar_init(bar_k_tmem, 256);
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
     fence_mbar_init();
@@ -194,7 +196,7 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
-  if (warp == 0) {
+  if (warp == kWProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&map_q);
@@ -228,7 +230,7 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
     // S^T_0; per step t: [S^T_t read] dP^T_t into the same columns (dO_t's slot
     // free after), [dS^T_t written] dK_t (Q_t's slot free after), [Q_{t+1}] S^T_{t+1}.
@@ -299,8 +301,8 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ one thread per key row
-    const int quarter = warp & 3;
+    // ------------------------------------------------------------ one thread per key row and column half
+    const int quarter = warp & 3, g = warp >> 2;   // g: queries [64g, 64g + 64) of each step
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int key = jt * kBN + r;
@@ -310,12 +312,13 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     bool ok = true;
     if (nsteps > 0) {
       // this key row of K into TMEM as the A operand of S^T (128 columns of
-      // bf16 pairs, the tile's 16-byte units in order); slot 0 is then free
+      // bf16 pairs, the tile's 16-byte units in order; this warp's two boxes);
+      // slot 0 is then free
       ok = mbar_wait(bar_kv_full, 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
 #pragma unroll
-        for (int bx = 0; bx < kWD / 64; ++bx) {
+        for (int bx = 2 * g; bx < 2 * g + 2; ++bx) {
           uint32_t w[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -336,19 +339,19 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(vb) - base));
-      float pr[128];
+      const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(vb) - base)) + 64 * g;
+      float pr[64];
       {
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(t_sp + 32 * q4, sr[q4]);
+        uint32_t sr[2][32];
+        tmem_ld_32x32b_x32(t_sp + 64 * g, sr[0]);
+        tmem_ld_32x32b_x32(t_sp + 64 * g + 32, sr[1]);
         tmem_wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+        reg_fence_x32(sr[0]);
+        reg_fence_x32(sr[1]);
         // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
-        const int lim = key - p.causal_off - step_tile(t) * kBM;   // first visible query column
+        const int lim = key - p.causal_off - step_tile(t) * kBM - 64 * g;   // first visible column of the half
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float e = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -vec[c]));
           pr[c] = (key_pad || (p.causal && c < lim)) ? 0.f : e;
         }
@@ -360,14 +363,13 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      {
         float x[64];
-        tmem_ld64(t_sp + 64u * hh, x);
+        tmem_ld64(t_sp + 64u * g, x);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = pr[64 * hh + c] * (x[c] - vec[kBM + 64 * hh + c]);
-        // dS^T row r, queries [64 hh, 64 hh + 64): box hh
-        store_row64(s_ds + hh * kBoxBytes, r, x);
+        for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - vec[kBM + c]);
+        // dS^T row r, queries [64 g, 64 g + 64): box g
+        store_row64(s_ds + g * kBoxBytes, r, x);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -385,10 +387,10 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (ok) {
       tc_fence_after();
       if (nsteps > 0) {
-        stage_acc_row(tbase + lane_off + kWColAcc, stg, r, p.scale);
+        stage_acc_row(tbase + lane_off + kWColAcc, stg, r, p.scale, g);
       } else {
 #pragma unroll
-        for (int bx = 0; bx < kWD / 64; ++bx)
+        for (int bx = 2 * g; bx < 2 * g + 2; ++bx)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" :: "r"(swz128(stg + bx * kBoxBytes, r, u)), "r"(0u)
@@ -396,8 +398,8 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (!*abort_flag && warp == 2 && lane == 0 && jt < nkt) {
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 0 && lane == 0 && jt < nkt) {
       for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_dk, stg + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
       tma_store_commit();
       tma_store_wait_all0();
@@ -434,7 +436,7 @@ struct WideDvCfg {
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kWThreads, 1)
 wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dv,
                const BwdParams p) {
@@ -491,9 +493,9 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     mbar_init(bar_do_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_vec_full(i), 1);
-      mbar_init(bar_vec_empty(i), 128);
+      mbar_init(bar_vec_empty(i), 256);
       mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_ready(i), 128);
+      mbar_init(bar_ready(i), 256);
     }
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
@@ -509,7 +511,7 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
-  if (warp == 0) {
+  if (warp == kWProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&map_q);
@@ -536,12 +538,14 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
     // S^T_0; per step t: [P^T_t written, dO_t landed] dV_t, then [Q_{t+1}
     // landed] S^T_{t+1} into the other buffer. Each S^T frees Q's buffer once
     // it completes, each dV frees dO's. (S^T_{t+1} first put Q_{t+1}'s load in
-    // front of dV_t.)
+    // front of dV_t.) P^T of query q sits in column 64 (q / 64) + (q % 64) / 2
+    // of the buffer: each column half's warps write over the S^T columns they
+    // read themselves.
     if (lane == 0) {
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || mbar_wait(bar_k_full, 0, abort_flag, deadline));
@@ -570,11 +574,12 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         if (!(ok = mbar_wait(bar_ready(t & 1), (t >> 1) & 1, abort_flag, deadline))) break;
         if (!(ok = mbar_wait(bar_do_full, t & 1, abort_flag, deadline))) break;
         tc_fence_after();
-        // dV += P^T dO (K = 128 queries; P^T of queries 2c, 2c+1 in column c of the buffer)
+        // dV += P^T dO (K = 128 queries)
         const uint32_t a = tbase + C::kColS + 128u * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_bf16_ts(tbase + kWColAcc, a + kk * 8, desc_add(dod, kk * 16 * 128), id_v, t > 0 || kk > 0);
+          mma_bf16_ts(tbase + kWColAcc, a + 64 * (kk >> 2) + (kk & 3) * 8, desc_add(dod, kk * 16 * 128), id_v,
+                      t > 0 || kk > 0);
         mma_commit(bar_do_empty);
         if (t + 1 < nsteps) {
           // S^T_{t+1} into the other buffer, whose P^T_{t-1} dV_{t-1} (issued
@@ -588,8 +593,8 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ one thread per key row
-    const int quarter = warp & 3;
+    // ------------------------------------------------------------ one thread per key row and column half
+    const int quarter = warp & 3, g = warp >> 2;   // g: queries [64g, 64g + 64) of each step
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int key = jt * kBN + r;
@@ -603,34 +608,32 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base));
-      const uint32_t ts = tbase + lane_off + C::kColS + 128u * sb;
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(ts + 32 * q4, sr[q4]);
+      const float* lse2 = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base)) + 64 * g;
+      const uint32_t ts = tbase + lane_off + C::kColS + 128u * sb + 64u * g;
+      uint32_t sr[2][32];
+      tmem_ld_32x32b_x32(ts, sr[0]);
+      tmem_ld_32x32b_x32(ts + 32, sr[1]);
       tmem_wait_ld();
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
+      reg_fence_x32(sr[0]);
+      reg_fence_x32(sr[1]);
       // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key;
       // query rows past N have LSE = +inf, so P = 0
-      const int lim = key - p.causal_off - step_tile(t) * kBM;   // first visible query column
+      const int lim = key - p.causal_off - step_tile(t) * kBM - 64 * g;   // first visible column of the half
+      uint32_t pp[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pp[32];
+      for (int c2 = 0; c2 < 32; ++c2) {
+        float e[2];
 #pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2) {
-          float e[2];
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int c = 64 * h + 2 * c2 + e2;
-            const float pe = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
-            e[e2] = (key_pad || (p.causal && c < lim)) ? 0.f : pe;
-          }
-          pp[c2] = pack_bf16x2(e[0], e[1]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int c = 2 * c2 + e2;
+          const float pe = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
+          e[e2] = (key_pad || (p.causal && c < lim)) ? 0.f : pe;
         }
-        // P^T over the S^T columns this thread has read: queries 64h + 2c2, +1 in column 32h + c2
-        tmem_st_32x32b_x32(ts + 32 * h, pp);
+        pp[c2] = pack_bf16x2(e[0], e[1]);
       }
+      // P^T over the first 32 of the S^T columns this thread has read: queries
+      // 64g + 2c2, +1 in column 64g + c2
+      tmem_st_32x32b_x32(ts, pp);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ready(sb));
@@ -646,10 +649,10 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (ok) {
       tc_fence_after();
       if (nsteps > 0) {
-        stage_acc_row(tbase + lane_off + kWColAcc, s_k, r, 1.0f);
+        stage_acc_row(tbase + lane_off + kWColAcc, s_k, r, 1.0f, g);
       } else {
 #pragma unroll
-        for (int bx = 0; bx < kWD / 64; ++bx)
+        for (int bx = 2 * g; bx < 2 * g + 2; ++bx)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" :: "r"(swz128(s_k + bx * kBoxBytes, r, u)), "r"(0u)
@@ -657,8 +660,8 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (!*abort_flag && warp == 2 && lane == 0) {
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 0 && lane == 0) {
       for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_dv, s_k + bx * kBoxBytes, bx * 64, jt * kBN, bhkv);
       tma_store_commit();
       tma_store_wait_all0();
@@ -697,7 +700,7 @@ struct WideDqCfg {
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kWThreads, 1)
 wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
@@ -754,10 +757,10 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_init(bar_empty(i), 1);
     }
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_read, 128);
+    mbar_init(bar_s_read, 256);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_ready, 128);
-    mbar_init(bar_q_tmem, 128);
+    mbar_init(bar_ready, 256);
+    mbar_init(bar_q_tmem, 256);
     mbar_init(bar_o_final, 1);
     mbar_init(bar_stall, 1);
     fence_mbar_init();
@@ -772,7 +775,7 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t tbase = *tmem_slot;
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
-  if (warp == 0) {
+  if (warp == kWProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nsteps > 0) {
       tma_prefetch_map(&map_k);
@@ -799,7 +802,7 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
     // S_0; per step j: [S_j read] dP_j into the same columns (V_j's slot free
     // after), [dS_j written] dQ_j (K_j's slot free after), [K_{j+1}] S_{j+1}.
@@ -870,8 +873,8 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ one thread per query row
-    const int quarter = warp & 3;
+    // ------------------------------------------------------------ one thread per query row and column half
+    const int quarter = warp & 3, g = warp >> 2;   // g: keys [64g, 64g + 64) of each step
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int q = qt * kBM + r;
@@ -885,12 +888,12 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (nsteps > 0) {
       // this row of Q into TMEM as the A operand of S: 128 columns of bf16
       // pairs, the lower dimension in the low half (the tile's 16-byte units
-      // in order); slot 0 is then free for K and V
+      // in order; this warp's two boxes); slot 0 is then free for K and V
       ok = mbar_wait(bar_q_full, 0, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
 #pragma unroll
-        for (int bx = 0; bx < kWD / 64; ++bx) {
+        for (int bx = 2 * g; bx < 2 * g + 2; ++bx) {
           uint32_t w[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -909,17 +912,17 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float pr[128];
+      float pr[64];
       {
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_32x32b_x32(t_sp + 32 * q4, sr[q4]);
+        uint32_t sr[2][32];
+        tmem_ld_32x32b_x32(t_sp + 64 * g, sr[0]);
+        tmem_ld_32x32b_x32(t_sp + 64 * g + 32, sr[1]);
         tmem_wait_ld();
+        reg_fence_x32(sr[0]);
+        reg_fence_x32(sr[1]);
+        const int lim = key_lim - j * kBN - 64 * g;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) reg_fence_x32(sr[q4]);
-        const int lim = key_lim - j * kBN;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float pe = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
           pr[c] = (c < lim) ? pe : 0.f;
         }
@@ -931,14 +934,13 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      {
         float x[64];
-        tmem_ld64(t_sp + 64u * hh, x);
+        tmem_ld64(t_sp + 64u * g, x);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = pr[64 * hh + c] * (x[c] - dsub);
-        // dS row r, keys [64 hh, 64 hh + 64): box hh
-        store_row64(s_ds + hh * kBoxBytes, r, x);
+        for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dsub);
+        // dS row r, keys [64 g, 64 g + 64): box g
+        store_row64(s_ds + g * kBoxBytes, r, x);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -953,10 +955,10 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tc_fence_after();
       // staging: the Q tile, idle once every MMA has completed
       if (nsteps > 0) {
-        stage_acc_row(tbase + lane_off + kWColAcc, s_q, r, p.scale);
+        stage_acc_row(tbase + lane_off + kWColAcc, s_q, r, p.scale, g);
       } else {
 #pragma unroll
-        for (int bx = 0; bx < kWD / 64; ++bx)
+        for (int bx = 2 * g; bx < 2 * g + 2; ++bx)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" :: "r"(swz128(s_q + bx * kBoxBytes, r, u)), "r"(0u)
@@ -964,8 +966,8 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (!*abort_flag && warp == 2 && lane == 0) {
+    named_bar_sync(1, 256);
+    if (!*abort_flag && warp == 0 && lane == 0) {
       for (int bx = 0; bx < kWD / 64; ++bx) tma_store_3d(&map_dq, s_q + bx * kBoxBytes, bx * 64, qt * kBM, bh);
       tma_store_commit();
       tma_store_wait_all0();

@@ -12,8 +12,8 @@ other loads. S and dP share one 128-column TMEM region: one thread issues
 S_0, then per step [every warp has read S_s] dP_s, which frees B's slot,
 [dS_s written] the accumulate, which frees A's slot, and [A_{s+1} landed]
 S_{s+1}. dS has one shared-memory buffer; the dK pass double-buffers the
-step's LSE and D. Four warps, one per TMEM lane quarter, read S, form P,
-wait for dP, and write dS.
+step's LSE and D. Eight warps, two per TMEM lane quarter (one per half of
+the score columns), read S, form P, wait for dP, and write dS.
 
 As for the other kernels, the roles run as coroutines with random latencies
 over barriers with the hardware's parity rule. The model checks that every
@@ -32,7 +32,7 @@ import pytest
 
 from test_wide_schedule import Barrier
 
-WARPS = 4
+WARPS = 8
 
 
 def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=True, vec_release_last=True,
