@@ -418,18 +418,27 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ dV per key tile, 128-query steps
-// Shared memory: K | Q | dO (one [128, 256] bf16 tile each) | LSE x2 | barriers.
+// Shared memory: K (one [128, 256] bf16 tile) | a ring of five 32 KB slots |
+// LSE x3 | barriers. Every Q and dO tile travels through the ring as two
+// pieces of 128 columns (two 64-column boxes each), in the order the products
+// read them: Q_0, Q_1, then per step t dO_t and Q_{t+2}. A slot goes back to
+// the producer when the products that read its piece complete, so loads run
+// up to five pieces (over one step) ahead of the tensor core.
 // TMEM: dV accumulator | S^T buffer 0 | S^T buffer 1 (128 columns each).
-// With 128 queries per step S^T = K Q^T is an N = 128 product (an N = 64
-// product takes about as long); Q and dO have one buffer each, so step t+1's
-// Q loads once S^T_t has read step t's.
+// Products: S^T_0 and S^T_1, then per step t [P^T_t written] dV_t (two
+// N = 128 halves, one per dO piece) and S^T_{t+2} into the buffer dV_t has
+// just read, so the warps form P^T_{t+1} while the tensor core runs dV_t and
+// S^T_{t+2}. With 128 queries per step S^T = K Q^T is an N = 128 product (an
+// N = 64 product takes about as long).
 struct WideDvCfg {
   static constexpr int kOffK = 0;
-  static constexpr int kOffQ = kWTile;
-  static constexpr int kOffDo = 2 * kWTile;
-  static constexpr int kOffVec = 3 * kWTile;
+  static constexpr int kSlots = 5;
+  static constexpr int kSlotBytes = 2 * kBoxBytes;     // [128, 128] bf16: half of a Q or dO tile
+  static constexpr int kOffRing = kWTile;
+  static constexpr int kNVec = 3;                      // LSE buffers: step t in buffer t % 3
   static constexpr int kVecBytes = 512;                // LSE log2(e) of 128 queries
-  static constexpr int kOffBar = kOffVec + 2 * kVecBytes;
+  static constexpr int kOffVec = kOffRing + kSlots * kSlotBytes;
+  static constexpr int kOffBar = kOffVec + kNVec * kVecBytes;
   static constexpr int kLayout = kOffBar + 256;
   static constexpr int kSmemAlloc = kLayout + 1024;
   static constexpr uint32_t kColS = 256;               // buffers at 256 and 384
@@ -449,18 +458,20 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
   }
-  const uint32_t s_k = base + C::kOffK, s_q = base + C::kOffQ, s_do = base + C::kOffDo;
+  const uint32_t s_k = base + C::kOffK;
+  auto s_slot = [&](int i) { return base + C::kOffRing + i * C::kSlotBytes; };
   auto s_vec = [&](int i) { return base + C::kOffVec + i * C::kVecBytes; };
   const uint32_t bars = base + C::kOffBar;
-  const uint32_t bar_k_full = bars, bar_q_full = bars + 8, bar_q_empty = bars + 16;
-  const uint32_t bar_do_full = bars + 24, bar_do_empty = bars + 32;
-  auto bar_vec_full = [&](int i) { return bars + 40u + 8u * i; };
-  auto bar_vec_empty = [&](int i) { return bars + 56u + 8u * i; };
-  auto bar_s_full = [&](int i) { return bars + 72u + 8u * i; };
-  auto bar_ready = [&](int i) { return bars + 88u + 8u * i; };      // P^T written over S^T
-  const uint32_t bar_o_final = bars + 104, bar_stall = bars + 112;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 120);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 124);
+  const uint32_t bar_k_full = bars;
+  auto bar_full = [&](int i) { return bars + 8u + 8u * i; };           // ring slot i landed
+  auto bar_empty = [&](int i) { return bars + 48u + 8u * i; };         // ring slot i read
+  auto bar_vec_full = [&](int i) { return bars + 88u + 8u * i; };
+  auto bar_vec_empty = [&](int i) { return bars + 112u + 8u * i; };
+  auto bar_s_full = [&](int i) { return bars + 136u + 8u * i; };
+  auto bar_ready = [&](int i) { return bars + 152u + 8u * i; };      // P^T written over S^T
+  const uint32_t bar_o_final = bars + 168, bar_stall = bars + 176;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 184);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 188);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -487,13 +498,15 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar_k_full, 1);
-    mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
-    mbar_init(bar_do_full, 1);
-    mbar_init(bar_do_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    for (int i = 0; i < C::kNVec; ++i) {
       mbar_init(bar_vec_full(i), 1);
       mbar_init(bar_vec_empty(i), 256);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s_full(i), 1);
       mbar_init(bar_ready(i), 256);
     }
@@ -519,75 +532,96 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_arrive_expect_tx(bar_k_full, kWTile);
       for (int bx = 0; bx < kWD / 64; ++bx)
         tma_load_3d(s_k + bx * kBoxBytes, &map_k, bar_k_full, bx * 64, jt * kBN, bhkv);
-      for (int t = 0; t < nsteps; ++t) {
-        const int bh = step_head(t), it = step_tile(t);
-        const uint32_t par = (t & 1) ^ 1;                // one buffer: phase t - 1 released it
-        if (!mbar_wait(bar_q_empty, par, abort_flag, deadline)) break;
-        mbar_arrive_expect_tx(bar_q_full, kWTile);
-        for (int bx = 0; bx < kWD / 64; ++bx)
-          tma_load_3d(s_q + bx * kBoxBytes, &map_q, bar_q_full, bx * 64, it * kBM, bh);
-        const int vb = t & 1;
-        if (!mbar_wait(bar_vec_empty(vb), ((t >> 1) & 1) ^ 1, abort_flag, deadline)) break;
+      int k = 0;                                       // ring pieces issued
+      // columns [128 half, 128 half + 128) of rows [row0, row0 + 128) of head bh
+      auto piece = [&](const CUtensorMap* m, int row0, int bh, int half) -> bool {
+        const int slot = k % C::kSlots, use = k / C::kSlots;
+        ++k;
+        if (!mbar_wait(bar_empty(slot), (use & 1) ^ 1, abort_flag, deadline)) return false;
+        mbar_arrive_expect_tx(bar_full(slot), C::kSlotBytes);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_3d(s_slot(slot) + bx * kBoxBytes, m, bar_full(slot), (2 * half + bx) * 64, row0, bh);
+        return true;
+      };
+      auto load_q = [&](int t) -> bool {              // Q_t and the LSE of step t
+        const int bh = step_head(t), it = step_tile(t), vb = t % C::kNVec;
+        if (!mbar_wait(bar_vec_empty(vb), ((t / C::kNVec) & 1) ^ 1, abort_flag, deadline)) return false;
         mbar_arrive_expect_tx(bar_vec_full(vb), C::kVecBytes);
         bulk_load(s_vec(vb), p.ws_lse2 + static_cast<size_t>(bh) * p.NQP + static_cast<size_t>(it) * kBM, C::kVecBytes,
                   bar_vec_full(vb));
-        if (!mbar_wait(bar_do_empty, par, abort_flag, deadline)) break;
-        mbar_arrive_expect_tx(bar_do_full, kWTile);
-        for (int bx = 0; bx < kWD / 64; ++bx)
-          tma_load_3d(s_do + bx * kBoxBytes, &map_do, bar_do_full, bx * 64, it * kBM, bh);
+        return piece(&map_q, it * kBM, bh, 0) && piece(&map_q, it * kBM, bh, 1);
+      };
+      bool ok = (nsteps < 1 || load_q(0)) && (nsteps < 2 || load_q(1));
+      for (int t = 0; t < nsteps && ok; ++t) {
+        const int bh = step_head(t), row0 = step_tile(t) * kBM;
+        ok = piece(&map_do, row0, bh, 0) && piece(&map_do, row0, bh, 1);
+        if (ok && t + 2 < nsteps) ok = load_q(t + 2);
       }
     }
     __syncwarp();
   } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
-    // S^T_0; per step t: [P^T_t written, dO_t landed] dV_t, then [Q_{t+1}
-    // landed] S^T_{t+1} into the other buffer. Each S^T frees Q's buffer once
-    // it completes, each dV frees dO's. (S^T_{t+1} first put Q_{t+1}'s load in
-    // front of dV_t.) P^T of query q sits in column 64 (q / 64) + (q % 64) / 2
-    // of the buffer: each column half's warps write over the S^T columns they
-    // read themselves.
+    // S^T_0, S^T_1; per step t: [P^T_t written] dV_t, then S^T_{t+2} into the
+    // buffer dV_t has read. Each piece is taken from the ring in the order the
+    // producer loads it and handed back by a commit after its products.
     if (lane == 0) {
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || mbar_wait(bar_k_full, 0, abort_flag, deadline));
       const uint32_t id_s = make_idesc(1, 128, 128, 0, 0);     // S^T: K and Q both K-major
-      const uint32_t id_v = make_idesc(1, 128, kWD, 0, 1);     // dV: A = P^T from TMEM, B = dO MN-major
-      const uint64_t kd = smem_desc_sw128(s_k, 16, 1024), qd = smem_desc_sw128(s_q, 16, 1024);
-      const uint64_t dod = smem_desc_sw128(s_do, kBoxBytes, 1024);
-      auto scores = [&](int t) {
+      const uint32_t id_v = make_idesc(1, 128, 128, 0, 1);     // dV half: A = P^T from TMEM, B = dO MN-major
+      const uint64_t kd = smem_desc_sw128(s_k, 16, 1024);
+      const uint64_t ring_k = smem_desc_sw128(s_slot(0), 16, 1024);           // K-major view of slot 0
+      const uint64_t ring_mn = smem_desc_sw128(s_slot(0), kBoxBytes, 1024);   // MN-major view of slot 0
+      int k = 0;                                       // ring pieces taken
+      auto take = [&](int& slot) -> bool {
+        slot = k % C::kSlots;
+        const int use = k / C::kSlots;
+        ++k;
+        if (!mbar_wait(bar_full(slot), use & 1, abort_flag, deadline)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto scores = [&](int t) -> bool {              // S^T_t = K Q_t^T, the two halves of d in turn
         const uint32_t d = tbase + C::kColS + 128u * (t & 1);
 #pragma unroll
-        for (int kk = 0; kk < kWD / 16; ++kk) {
-          const uint32_t off = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
-          mma_bf16_ss(d, desc_add(kd, off), desc_add(qd, off), id_s, kk > 0);
+        for (int h = 0; h < 2; ++h) {
+          int slot;
+          if (!take(slot)) return false;
+          const uint64_t qd = desc_add(ring_k, static_cast<uint32_t>(slot * C::kSlotBytes));
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const int kk = 8 * h + k8;
+            const uint32_t off_k = (kk * 32 / 128) * kBoxBytes + (kk * 32) % 128;
+            const uint32_t off_q = (k8 * 32 / 128) * kBoxBytes + (k8 * 32) % 128;
+            mma_bf16_ss(d, desc_add(kd, off_k), desc_add(qd, off_q), id_s, kk > 0);
+          }
+          mma_commit(bar_empty(slot));
         }
         mma_commit(bar_s_full(t & 1));
-        mma_commit(bar_q_empty);
+        return true;
       };
-      if (ok && nsteps > 0) {
-        ok = mbar_wait(bar_q_full, 0, abort_flag, deadline);
-        if (ok) {
-          tc_fence_after();
-          scores(0);
-        }
-      }
-      for (int t = 0; t < nsteps && ok; ++t) {
-        if (!(ok = mbar_wait(bar_ready(t & 1), (t >> 1) & 1, abort_flag, deadline))) break;
-        if (!(ok = mbar_wait(bar_do_full, t & 1, abort_flag, deadline))) break;
-        tc_fence_after();
-        // dV += P^T dO (K = 128 queries)
+      auto dv = [&](int t) -> bool {                  // dV += P^T dO_t (K = 128 queries), d in two halves
         const uint32_t a = tbase + C::kColS + 128u * (t & 1);
 #pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_bf16_ts(tbase + kWColAcc, a + 64 * (kk >> 2) + (kk & 3) * 8, desc_add(dod, kk * 16 * 128), id_v,
-                      t > 0 || kk > 0);
-        mma_commit(bar_do_empty);
-        if (t + 1 < nsteps) {
-          // S^T_{t+1} into the other buffer, whose P^T_{t-1} dV_{t-1} (issued
-          // before) has read
-          if (!(ok = mbar_wait(bar_q_full, (t + 1) & 1, abort_flag, deadline))) break;
-          tc_fence_after();
-          scores(t + 1);
+        for (int h = 0; h < 2; ++h) {
+          int slot;
+          if (!take(slot)) return false;
+          const uint64_t dod = desc_add(ring_mn, static_cast<uint32_t>(slot * C::kSlotBytes));
+#pragma unroll
+          for (int kk = 0; kk < kBM / 16; ++kk)
+            mma_bf16_ts(tbase + kWColAcc + 128u * h, a + 64 * (kk >> 2) + (kk & 3) * 8, desc_add(dod, kk * 16 * 128),
+                        id_v, t > 0 || kk > 0);
+          mma_commit(bar_empty(slot));
         }
+        return true;
+      };
+      ok = ok && (nsteps < 1 || scores(0)) && (nsteps < 2 || scores(1));
+      for (int t = 0; t < nsteps && ok; ++t) {
+        if (!(ok = mbar_wait(bar_ready(t & 1), (t >> 1) & 1, abort_flag, deadline))) break;
+        tc_fence_after();
+        ok = dv(t);
+        // S^T_{t+2} goes into the buffer whose P^T_t dV_t (issued before) reads
+        if (ok && t + 2 < nsteps) ok = scores(t + 2);
       }
       if (ok) mma_commit(bar_o_final);
     }
@@ -602,13 +636,13 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
-      const int sb = t & 1;
+      const int sb = t & 1, vb = t % C::kNVec;
       ok = mbar_wait(bar_s_full(sb), (t >> 1) & 1, abort_flag, deadline) &&
-           mbar_wait(bar_vec_full(sb), (t >> 1) & 1, abort_flag, deadline);
+           mbar_wait(bar_vec_full(vb), (t / C::kNVec) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(gbase + (s_vec(sb) - base)) + 64 * g;
+      const float* lse2 = reinterpret_cast<const float*>(gbase + (s_vec(vb) - base)) + 64 * g;
       const uint32_t ts = tbase + lane_off + C::kColS + 128u * sb + 64u * g;
       uint32_t sr[2][32];
       tmem_ld_32x32b_x32(ts, sr[0]);
@@ -637,7 +671,7 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ready(sb));
-      mbar_arrive(bar_vec_empty(sb));
+      mbar_arrive(bar_vec_empty(vb));
     }
     // ---------------------------------------------------------- epilogue
     if (ok) {
