@@ -418,21 +418,23 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ dV per key tile, 128-query steps
-// Shared memory: K (one [128, 256] bf16 tile) | a ring of five 32 KB slots |
+// Shared memory: K (one [128, 256] bf16 tile) | a ring of four 32 KB slots |
 // LSE x3 | barriers. Every Q and dO tile travels through the ring as two
 // pieces of 128 columns (two 64-column boxes each), in the order the products
-// read them: Q_0, Q_1, then per step t dO_t and Q_{t+2}. A slot goes back to
-// the producer when the products that read its piece complete, so loads run
-// up to five pieces (over one step) ahead of the tensor core.
+// read them: Q_0, Q_1, then per step t dO_t and Q_{t+2}. A tile's two pieces
+// always take slots 0-1 or 2-3, so one N = 256 product group can read dO_t
+// across both. A slot goes back to the producer when the products that read
+// its piece complete, so loads run up to four pieces (one step) ahead of the
+// tensor core.
 // TMEM: dV accumulator | S^T buffer 0 | S^T buffer 1 (128 columns each).
-// Products: S^T_0 and S^T_1, then per step t [P^T_t written] dV_t (two
-// N = 128 halves, one per dO piece) and S^T_{t+2} into the buffer dV_t has
+// Products: S^T_0 and S^T_1, then per step t [P^T_t written] dV_t (N = 256
+// over both dO pieces) and S^T_{t+2} into the buffer dV_t has
 // just read, so the warps form P^T_{t+1} while the tensor core runs dV_t and
 // S^T_{t+2}. With 128 queries per step S^T = K Q^T is an N = 128 product (an
 // N = 64 product takes about as long).
 struct WideDvCfg {
   static constexpr int kOffK = 0;
-  static constexpr int kSlots = 5;
+  static constexpr int kSlots = 4;
   static constexpr int kSlotBytes = 2 * kBoxBytes;     // [128, 128] bf16: half of a Q or dO tile
   static constexpr int kOffRing = kWTile;
   static constexpr int kNVec = 3;                      // LSE buffers: step t in buffer t % 3
@@ -568,7 +570,7 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       bool ok = !p.test_stall || mbar_wait(bar_stall, 0, abort_flag, deadline);   // runs out by design
       ok = ok && (nsteps == 0 || mbar_wait(bar_k_full, 0, abort_flag, deadline));
       const uint32_t id_s = make_idesc(1, 128, 128, 0, 0);     // S^T: K and Q both K-major
-      const uint32_t id_v = make_idesc(1, 128, 128, 0, 1);     // dV half: A = P^T from TMEM, B = dO MN-major
+      const uint32_t id_v = make_idesc(1, 128, kWD, 0, 1);     // dV: A = P^T from TMEM, B = dO MN-major
       const uint64_t kd = smem_desc_sw128(s_k, 16, 1024);
       const uint64_t ring_k = smem_desc_sw128(s_slot(0), 16, 1024);           // K-major view of slot 0
       const uint64_t ring_mn = smem_desc_sw128(s_slot(0), kBoxBytes, 1024);   // MN-major view of slot 0
@@ -602,17 +604,15 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       };
       auto dv = [&](int t) -> bool {                  // dV += P^T dO_t (K = 128 queries), d in two halves
         const uint32_t a = tbase + C::kColS + 128u * (t & 1);
+        int s0, s1;                                    // adjacent slots: pieces come in pairs from an even slot
+        if (!take(s0) || !take(s1)) return false;
+        const uint64_t dod = desc_add(ring_mn, static_cast<uint32_t>(s0 * C::kSlotBytes));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          int slot;
-          if (!take(slot)) return false;
-          const uint64_t dod = desc_add(ring_mn, static_cast<uint32_t>(slot * C::kSlotBytes));
-#pragma unroll
-          for (int kk = 0; kk < kBM / 16; ++kk)
-            mma_bf16_ts(tbase + kWColAcc + 128u * h, a + 64 * (kk >> 2) + (kk & 3) * 8, desc_add(dod, kk * 16 * 128),
-                        id_v, t > 0 || kk > 0);
-          mma_commit(bar_empty(slot));
-        }
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_bf16_ts(tbase + kWColAcc, a + 64 * (kk >> 2) + (kk & 3) * 8, desc_add(dod, kk * 16 * 128), id_v,
+                      t > 0 || kk > 0);
+        mma_commit(bar_empty(s0));
+        mma_commit(bar_empty(s1));
         return true;
       };
       ok = ok && (nsteps < 1 || scores(0)) && (nsteps < 2 || scores(1));

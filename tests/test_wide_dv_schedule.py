@@ -2,11 +2,13 @@
 wide_dv_kernel), run on the CPU.
 
 Per 128-key tile the pass walks 128-query steps t. Q_t and dO_t each travel
-through a ring of five shared-memory slots as two pieces (columns 0-127 and
+through a ring of four shared-memory slots as two pieces (columns 0-127 and
 128-255), in the order the products read them: Q_0, Q_1, then per step dO_t
-and Q_{t+2}. One thread issues S^T_0 and S^T_1 into two TMEM buffers, then per
-step [every warp has written P^T_t over S^T_t] dV_t (one product group per dO
-piece) and S^T_{t+2} into the buffer dV_t has just read. Each piece's slot
+and Q_{t+2}; a tile's pieces always take slots 0-1 or 2-3. One thread issues
+S^T_0 and S^T_1 into two TMEM buffers (each half of the contraction once its
+piece has landed), then per step [every warp has written P^T_t over S^T_t]
+dV_t (one N = 256 product group over both dO pieces) and S^T_{t+2} into the
+buffer dV_t has just read. Each piece's slot
 goes back to the producer by a commit after the products that read it; the
 step's LSE sits in one of three buffers (t % 3), loaded with Q_t. Eight warps
 read S^T_t, write P^T_t and hand the LSE buffer back.
@@ -15,9 +17,10 @@ As for the other kernels, the roles run as coroutines with random latencies
 over barriers with the hardware's parity rule. The model checks that every
 product reads the piece and TMEM buffer of its own step, that no slot, TMEM
 buffer or LSE buffer is overwritten while a reader still needs it, that no
-parity wait passes on an older phase, and that nothing deadlocks. Planted
-changes show what the slot hand-back after the products, the issuer's wait
-for P^T and the order of dV_t before S^T_{t+2} guard.
+parity wait passes on an older phase, that both pieces of dO_t sit in
+adjacent slots, and that nothing deadlocks. Planted changes show what the
+slot hand-back after the products, the issuer's wait for P^T, the order of
+dV_t before S^T_{t+2} and the ring's four slots guard.
 """
 import heapq
 import random
@@ -27,7 +30,7 @@ import pytest
 from test_wide_schedule import Barrier
 
 WARPS = 8
-SLOTS = 5
+SLOTS = 4
 NVEC = 3
 
 
@@ -44,18 +47,18 @@ def piece_order(n):
 
 
 def simulate(n, seed, *, release_after_products=True, issuer_waits_ready=True, dv_before_next_scores=True,
-             warp_cycles=(100, 1500)):
+             warp_cycles=(100, 1500), slots=SLOTS):
     rng = random.Random(seed)
     errors = []
-    full = [Barrier(1) for _ in range(SLOTS)]
-    empty = [Barrier(1) for _ in range(SLOTS)]
+    full = [Barrier(1) for _ in range(slots)]
+    empty = [Barrier(1) for _ in range(slots)]
     vec_full = [Barrier(1) for _ in range(NVEC)]
     vec_empty = [Barrier(WARPS) for _ in range(NVEC)]
     s_full = [Barrier(1), Barrier(1)]
     ready = [Barrier(WARPS), Barrier(WARPS)]
     o_final = Barrier(1)
-    slot = [None] * SLOTS            # piece held; None while a load is in flight
-    inflight = [False] * SLOTS
+    slot = [None] * slots            # piece held; None while a load is in flight
+    inflight = [False] * slots
     vec = [None] * NVEC
     # TMEM buffer b, per warp's region (its 32 lanes, its half of the columns): ("S" | "P", step)
     buf = [[None] * WARPS, [None] * WARPS]
@@ -81,20 +84,23 @@ def simulate(n, seed, *, release_after_products=True, issuer_waits_ready=True, d
                 op[1].arrive()
                 continue
             kind, t, h, i = op
-            want = ("Q" if kind == "S" else "dO", t, h)
-            if slot[i] != want:
-                errors.append(f"{kind}({t}) half {h} read slot {i} holding {slot[i]}")
+            # S reads one piece (half h of Q_t); dV reads both pieces of dO_t, from slot i and i + 1
+            reads = [(i, ("Q", t, h))] if kind == "S" else [(i, ("dO", t, 0)), (i + 1, ("dO", t, 1))]
+            for j, want in reads:
+                if j >= slots or slot[j] != want:
+                    errors.append(f"{kind}({t}) read slot {j} holding {slot[j] if j < slots else None}, not {want}")
             b = t & 1
             if kind == "S" and h == 0 and t >= 2 and (dv_done[0] < t - 2 or buf[b] != [("P", t - 2)] * WARPS):
                 errors.append(f"S({t}) overwrote buffer {b} holding {buf[b]} before dV({t - 2}) read it")
             if kind == "dV" and buf[b] != [("P", t)] * WARPS:
                 errors.append(f"dV({t}) read buffer {b} holding {buf[b]}")
-            yield ("delay", rng.uniform(100, 600))
-            if slot[i] != want:
-                errors.append(f"{kind}({t}) half {h}: slot {i} changed under the product ({slot[i]})")
+            yield ("delay", rng.uniform(100, 600) * len(reads))
+            for j, want in reads:
+                if j < slots and slot[j] != want:
+                    errors.append(f"{kind}({t}): slot {j} changed under the product ({slot[j]})")
             if kind == "S" and h == 1:
                 buf[b] = [("S", t)] * WARPS
-            if kind == "dV" and h == 1:
+            if kind == "dV":
                 dv_done[0] = t
 
     # ------------------------------------------------------------ producer
@@ -120,8 +126,8 @@ def simulate(n, seed, *, release_after_products=True, issuer_waits_ready=True, d
                 vec_full[x].arrive()
                 vec[x] = None
                 later(rng.uniform(200, 2000), land_vec(x, t))
-            i = k % SLOTS
-            yield from wait(empty[i], ((k // SLOTS) & 1) ^ 1, "producer empty")
+            i = k % slots
+            yield from wait(empty[i], ((k // slots) & 1) ^ 1, "producer empty")
             if inflight[i]:
                 errors.append(f"{what} loaded into slot {i} while a load was in flight")
             full[i].expect_tx(1)
@@ -134,8 +140,8 @@ def simulate(n, seed, *, release_after_products=True, issuer_waits_ready=True, d
         k = [0]
 
         def take():
-            i = k[0] % SLOTS
-            par = (k[0] // SLOTS) & 1
+            i = k[0] % slots
+            par = (k[0] // slots) & 1
             k[0] += 1
             yield from wait(full[i], par, "issuer full")
             return i
@@ -150,9 +156,11 @@ def simulate(n, seed, *, release_after_products=True, issuer_waits_ready=True, d
             pipe.append(("commit", s_full[t & 1]))
 
         def dv(t):
-            for h in (0, 1):
-                i = yield from take()
-                pipe.extend([("dV", t, h, i), ("commit", empty[i])])
+            i0 = yield from take()
+            i1 = yield from take()
+            if i1 != i0 + 1:
+                errors.append(f"dO({t}) pieces in slots {i0} and {i1}: not adjacent")
+            pipe.extend([("dV", t, 0, i0), ("commit", empty[i0]), ("commit", empty[i1])])
 
         for t in range(min(n, 2)):
             yield from scores(t)
@@ -269,3 +277,11 @@ def test_dv_must_precede_the_scores_two_steps_ahead():
     """S^T_{t+2} goes into the buffer that holds P^T_t: dV_t has to be queued
     first."""
     assert bad_runs(dv_before_next_scores=False) > 0
+
+
+def test_pieces_of_a_tile_share_an_even_slot_pair():
+    """One product group reads both pieces of dO_t through one descriptor, so
+    they must sit in adjacent slots. Four slots keep every tile's pair in slots
+    0-1 or 2-3; five would split some."""
+    assert bad_runs() == 0
+    assert sum(bool(simulate(n, seed, slots=5)) for n in (3, 7, 12) for seed in range(4)) > 0
