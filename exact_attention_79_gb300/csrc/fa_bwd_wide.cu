@@ -93,12 +93,12 @@ __device__ __forceinline__ void stage_acc_row(uint32_t taddr, uint32_t stg, int 
 // ------------------------------------------------------------------ dK per key tile, 128-query steps
 // Shared memory: V | two 64 KB slots | dS^T | LSE, D x2 | barriers. K lands in
 // slot 0 and the warps copy it into TMEM as the A operand of S^T; Q_t then
-// goes to slot (t + 1) & 1 and dO_t to slot t & 1, so Q_{t+1} takes the slot
-// dO_t leaves after dP^T_t and dO_{t+1} the one Q_t leaves after dK_t.
-// TMEM: dK accumulator | S^T, then dP^T, of the step (128 columns) | K.
-// Per step S^T_t (N = 128 queries) goes into the score columns; once every
-// warp has read it, dP^T_t goes into the same columns; once every warp has
-// written dS^T_t, dK += dS^T_t Q_t.
+// always goes to slot 0 and dO_t to slot 1, so dO_{t+1} loads as soon as
+// dP^T_t has read dO_t, early in step t, and Q_{t+1} once dK_t has read Q_t.
+// TMEM: dK accumulator | dP^T, then S^T, of the step (128 columns) | K.
+// Per step dP^T_t (N = 128 queries) goes into the score columns; once every
+// warp has read it into registers, S^T_t goes into the same columns; once
+// every warp has written dS^T_t, dK += dS^T_t Q_t, and dP^T_{t+1} follows.
 struct WideDkCfg {
   static constexpr int kOffV = 0;
   static constexpr int kOffSlot = kWTile;              // two 64 KB slots; slot 0 first holds K
@@ -165,8 +165,10 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const int nsteps = G * per_head;
   auto step_head = [&](int t) { return b * p.Hq + hk * G + t / per_head; };
   auto step_tile = [&](int t) { return it0 + t % per_head; };
-  auto q_slot = [&](int t) { return (t + 1) & 1; };
-  auto do_slot = [&](int t) { return t & 1; };
+  // Q_t always in slot 0 (after K has gone from it into TMEM), dO_t in slot 1:
+  // dO_{t+1} loads as soon as dP^T_t has read dO_t, early in step t
+  auto q_slot = [](int) { return 0; };
+  auto do_slot = [](int) { return 1; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -219,6 +221,7 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       };
       for (int t = 0; t < nsteps; ++t) {
         const int bh = step_head(t), row0 = step_tile(t) * kBM;
+        if (!load(&map_do, do_slot(t), row0, bh)) break;
         if (!load(&map_q, q_slot(t), row0, bh)) break;
         const int vb = t & 1;
         if (!mbar_wait(bar_vec_empty(vb), ((t >> 1) & 1) ^ 1, abort_flag, deadline)) break;
@@ -226,14 +229,14 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         const size_t voff = static_cast<size_t>(bh) * p.NQP + row0;
         bulk_load(s_vec(vb), p.ws_lse2 + voff, kBM * 4, bar_vec_full(vb));
         bulk_load(s_vec(vb) + kBM * 4, p.ws_d + voff, kBM * 4, bar_vec_full(vb));
-        if (!load(&map_do, do_slot(t), row0, bh)) break;
       }
     }
     __syncwarp();
   } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
-    // S^T_0; per step t: [S^T_t read] dP^T_t into the same columns (dO_t's slot
-    // free after), [dS^T_t written] dK_t (Q_t's slot free after), [Q_{t+1}] S^T_{t+1}.
+    // dP^T_0; per step t: [dP^T_t read] S^T_t into the same columns, [dS^T_t
+    // written] dK_t (Q_t's slot free after), [dO_{t+1}] dP^T_{t+1} (dO_t's slot
+    // was free once dP^T_t completed).
     if (lane == 0) {
       int fulls[2] = {0, 0};
       auto wait_full = [&](int slot) -> bool {
@@ -274,27 +277,27 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         mma_commit(bar_empty(q_slot(t)));
       };
       if (ok && nsteps > 0) {
-        ok = wait_full(q_slot(0));
+        ok = wait_full(do_slot(0));
         if (ok) {
           tc_fence_after();
-          scores(0);
+          dp(0);
         }
       }
       for (int t = 0; t < nsteps && ok; ++t) {
-        if (!(ok = mbar_wait(bar_s_read, t & 1, abort_flag, deadline))) break;
-        if (!(ok = wait_full(do_slot(t)))) break;
+        if (!(ok = mbar_wait(bar_s_read, t & 1, abort_flag, deadline))) break;   // every warp read dP^T_t
+        if (!(ok = wait_full(q_slot(t)))) break;
         tc_fence_after();
-        dp(t);
-        // the single dS^T buffer: dS^T_t is written after dP^T_t completes, so
-        // after dK_{t-1} (issued before dP^T_t) has read dS^T_{t-1}
+        scores(t);
+        // the single dS^T buffer: dS^T_t is written after S^T_t completes, so
+        // after dK_{t-1} (issued before S^T_t) has read dS^T_{t-1}
         if (!(ok = mbar_wait(bar_ready, t & 1, abort_flag, deadline))) break;
         tc_fence_after();
         dk(t);
         if (t + 1 < nsteps) {
-          // the score columns: every warp read dP^T_t before its dS^T_t
-          if (!(ok = wait_full(q_slot(t + 1)))) break;
+          // the score columns: every warp read S^T_t before its dS^T_t
+          if (!(ok = wait_full(do_slot(t + 1)))) break;
           tc_fence_after();
-          scores(t + 1);
+          dp(t + 1);
         }
       }
       if (ok) mma_commit(bar_o_final);
@@ -334,42 +337,40 @@ wide_dk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     for (int t = 0; t < nsteps && ok; ++t) {
       const int vb = t & 1;
+      ok = mbar_wait(bar_dp_full, t & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float dpv[64];
+      tmem_ld64(t_sp + 64u * g, dpv);
+      // dP^T_t is in registers: its columns may take S^T_t
+      tc_fence_before();
+      mbar_arrive(bar_s_read);
       ok = mbar_wait(bar_s_full, t & 1, abort_flag, deadline) &&
            mbar_wait(bar_vec_full(vb), (t >> 1) & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(gbase + (s_vec(vb) - base)) + 64 * g;
-      float pr[64];
       {
-        uint32_t sr[2][32];
-        tmem_ld_32x32b_x32(t_sp + 64 * g, sr[0]);
-        tmem_ld_32x32b_x32(t_sp + 64 * g + 32, sr[1]);
-        tmem_wait_ld();
-        reg_fence_x32(sr[0]);
-        reg_fence_x32(sr[1]);
-        // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key
+        // P^T[key, q] = 2^(S^T s log2e - LSE_q log2e); causal: q + (Nk - N) >= key;
+        // dS^T = P^T (dP^T - D), formed in dpv in place, 32 columns of S^T at a time
         const int lim = key - p.causal_off - step_tile(t) * kBM - 64 * g;   // first visible column of the half
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float e = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -vec[c]));
-          pr[c] = (key_pad || (p.causal && c < lim)) ? 0.f : e;
-        }
-      }
-      // S^T_t is in registers: its columns may take dP^T_t
-      tc_fence_before();
-      mbar_arrive(bar_s_read);
-      ok = mbar_wait(bar_dp_full, t & 1, abort_flag, deadline);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        float x[64];
-        tmem_ld64(t_sp + 64u * g, x);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[32];
+          tmem_ld_32x32b_x32(t_sp + 64 * g + 32 * h, sr);
+          tmem_wait_ld();
+          reg_fence_x32(sr);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - vec[kBM + c]);
+          for (int c = 32 * h; c < 32 * h + 32; ++c) {
+            const float e = ex2_approx(fmaf(__uint_as_float(sr[c & 31]), sl2, -vec[c]));
+            const float pr = (key_pad || (p.causal && c < lim)) ? 0.f : e;
+            dpv[c] = pr * (dpv[c] - vec[kBM + c]);
+          }
+        }
         // dS^T row r, queries [64 g, 64 g + 64): box g
-        store_row64(s_ds + g * kBoxBytes, r, x);
+        store_row64(s_ds + g * kBoxBytes, r, dpv);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -715,14 +716,15 @@ wide_dv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 
 // ------------------------------------------------------------------ dQ per query tile, 128-key steps
 // Shared memory: dO | two 64 KB slots | dS | barriers. Q lands in slot 0 and
-// the warps copy it into TMEM as the A operand of S; K_j then goes to slot
-// (j + 1) & 1 and V_j to slot j & 1, so K_{j+1} takes the slot V_j leaves
-// after dP_j and V_{j+1} the one K_j leaves after dQ_j.
-// TMEM: dQ accumulator | S, then dP, of the step (128 columns) | Q.
-// Per step S_j (N = 128 keys) goes into the score columns; once every warp
-// has read it, dP_j goes into the same columns; once every warp has written
-// dS_j, dQ_j += dS_j K_j. With 128 keys per step every score product is
-// N = 128 (an N = 64 product takes about as long).
+// the warps copy it into TMEM as the A operand of S; K_j then always goes to
+// slot 0 and V_j to slot 1, so V_{j+1} loads as soon as dP_j has read V_j,
+// early in step j, and K_{j+1} once dQ_j has read K_j.
+// TMEM: dQ accumulator | dP, then S, of the step (128 columns) | Q.
+// Per step dP_j (N = 128 keys) goes into the score columns; once every warp
+// has read it into registers, S_j goes into the same columns; once every
+// warp has written dS_j, dQ_j += dS_j K_j, and dP_{j+1} follows. With 128
+// keys per step every score product is N = 128 (an N = 64 product takes
+// about as long).
 struct WideDqCfg {
   static constexpr int kOffDo = 0;
   static constexpr int kOffSlot = kWTile;              // two 64 KB slots; slot 0 first holds Q
@@ -780,8 +782,10 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const int last = qt * kBM + kBM - 1 + p.causal_off;   // the tile's last row sees keys up to here
     nsteps = last < 0 ? 0 : min(nkt, last / kBN + 1);
   }
-  auto k_slot = [&](int j) { return (j + 1) & 1; };
-  auto v_slot = [&](int j) { return j & 1; };
+  // K_j always in slot 0 (after Q has gone from it into TMEM), V_j in slot 1:
+  // V_{j+1} loads as soon as dP_j has read V_j, early in step j
+  auto k_slot = [](int) { return 0; };
+  auto v_slot = [](int) { return 1; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -831,15 +835,16 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         return true;
       };
       for (int j = 0; j < nsteps; ++j) {
-        if (!load(&map_k, k_slot(j), j * kBN)) break;
         if (!load(&map_v, v_slot(j), j * kBN)) break;
+        if (!load(&map_k, k_slot(j), j * kBN)) break;
       }
     }
     __syncwarp();
   } else if (warp == kWIss) {
     // ------------------------------------------------------------ MMA issuer
-    // S_0; per step j: [S_j read] dP_j into the same columns (V_j's slot free
-    // after), [dS_j written] dQ_j (K_j's slot free after), [K_{j+1}] S_{j+1}.
+    // dP_0; per step j: [dP_j read] S_j into the same columns, [dS_j written]
+    // dQ_j (K_j's slot free after), [V_{j+1}] dP_{j+1} (V_j's slot was free
+    // once dP_j completed).
     if (lane == 0) {
       int fulls[2] = {0, 0};
       auto wait_full = [&](int slot) -> bool {
@@ -880,27 +885,27 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         mma_commit(bar_empty(k_slot(j)));
       };
       if (ok && nsteps > 0) {
-        ok = wait_full(k_slot(0));
+        ok = wait_full(v_slot(0));
         if (ok) {
           tc_fence_after();
-          scores(0);
+          dp(0);
         }
       }
       for (int j = 0; j < nsteps && ok; ++j) {
-        if (!(ok = mbar_wait(bar_s_read, j & 1, abort_flag, deadline))) break;
-        if (!(ok = wait_full(v_slot(j)))) break;
+        if (!(ok = mbar_wait(bar_s_read, j & 1, abort_flag, deadline))) break;   // every warp read dP_j
+        if (!(ok = wait_full(k_slot(j)))) break;
         tc_fence_after();
-        dp(j);
-        // the single dS buffer: dS_j is written after dP_j completes, so after
-        // dQ_{j-1} (issued before dP_j) has read dS_{j-1}
+        scores(j);
+        // the single dS buffer: dS_j is written after S_j completes, so after
+        // dQ_{j-1} (issued before S_j) has read dS_{j-1}
         if (!(ok = mbar_wait(bar_ready, j & 1, abort_flag, deadline))) break;
         tc_fence_after();
         dq(j);
         if (j + 1 < nsteps) {
-          // the score columns: every warp read dP_j before its dS_j
-          if (!(ok = wait_full(k_slot(j + 1)))) break;
+          // the score columns: every warp read S_j before its dS_j
+          if (!(ok = wait_full(v_slot(j + 1)))) break;
           tc_fence_after();
-          scores(j + 1);
+          dp(j + 1);
         }
       }
       if (ok) mma_commit(bar_o_final);
@@ -942,11 +947,19 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     for (int j = 0; j < nsteps && ok; ++j) {
+      ok = mbar_wait(bar_dp_full, j & 1, abort_flag, deadline);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float dpv[64];
+      tmem_ld64(t_sp + 64u * g, dpv);
+      // dP_j is in registers: its columns may take S_j
+      tc_fence_before();
+      mbar_arrive(bar_s_read);
       ok = mbar_wait(bar_s_full, j & 1, abort_flag, deadline);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float pr[64];
       {
         uint32_t sr[2][32];
         tmem_ld_32x32b_x32(t_sp + 64 * g, sr[0]);
@@ -954,27 +967,16 @@ wide_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         tmem_wait_ld();
         reg_fence_x32(sr[0]);
         reg_fence_x32(sr[1]);
+        // P = 2^(S s log2e - LSE log2e), dS = P (dP - D)
         const int lim = key_lim - j * kBN - 64 * g;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 64; ++c) {                  // dpv becomes dS in place
           const float pe = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
-          pr[c] = (c < lim) ? pe : 0.f;
+          const float pr = (c < lim) ? pe : 0.f;
+          dpv[c] = pr * (dpv[c] - dsub);
         }
-      }
-      // S_j is in registers: its columns may take dP_j
-      tc_fence_before();
-      mbar_arrive(bar_s_read);
-      ok = mbar_wait(bar_dp_full, j & 1, abort_flag, deadline);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        float x[64];
-        tmem_ld64(t_sp + 64u * g, x);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dsub);
         // dS row r, keys [64 g, 64 g + 64): box g
-        store_row64(s_ds + g * kBoxBytes, r, x);
+        store_row64(s_ds + g * kBoxBytes, r, dpv);
       }
       fence_proxy_async_smem();
       tc_fence_before();

@@ -4,16 +4,16 @@ The kernels (csrc/fa_bwd_wide.cu, wide_dk_kernel and wide_dq_kernel) walk
 128-row steps s over two 64 KB shared-memory slots. Each step has an operand
 A (Q_s in the dK pass, K_s in the dQ pass), read by the scores S_s and by the
 accumulate (dK += dS^T Q_s, dQ += dS K_s), and an operand B (dO_s or V_s),
-read only by dP_s. A_s lands in slot (s + 1) & 1 and B_s in slot s & 1, so B
-takes the slot A left and the other way round. Each pass keeps one operand in
-TMEM as the A operand of the scores (K in the dK pass, Q in the dQ pass): it
-lands in slot 0, every warp copies its rows, and only then does slot 0 take
-other loads. S and dP share one 128-column TMEM region: one thread issues
-S_0, then per step [every warp has read S_s] dP_s, which frees B's slot,
-[dS_s written] the accumulate, which frees A's slot, and [A_{s+1} landed]
-S_{s+1}. dS has one shared-memory buffer; the dK pass double-buffers the
-step's LSE and D. Eight warps, two per TMEM lane quarter (one per half of
-the score columns), read S, form P, wait for dP, and write dS.
+read only by dP_s. A always lands in slot 0 and B in slot 1. Each pass keeps
+one operand in TMEM as the A operand of the scores (K in the dK pass, Q in
+the dQ pass): it lands in slot 0, every warp copies its rows, and only then
+does slot 0 take A. dP and S share one 128-column TMEM region: one thread
+issues dP_0, then per step [every warp has read dP_s, A_s landed] S_s,
+[dS_s written] the accumulate, which frees A's slot, and [B_{s+1} landed]
+dP_{s+1}; B's slot is free once dP_s completes, early in the step. dS has
+one shared-memory buffer; the dK pass double-buffers the step's LSE and D.
+Eight warps, two per TMEM lane quarter (one per half of the score columns),
+read dP into registers, then read S, form P and write dS.
 
 As for the other kernels, the roles run as coroutines with random latencies
 over barriers with the hardware's parity rule. The model checks that every
@@ -21,7 +21,7 @@ product and every warp reads the data of its own step, that no slot, TMEM
 buffer, dS buffer or vector buffer is overwritten while a reader still needs
 it, and that no parity wait passes on an older phase. Planted changes show
 what the accumulate's release of A's slot, the warps' wait for dP, the
-issuer's wait for every warp's read of S and the producer's wait for the
+issuer's wait for every warp's read of dP and the producer's wait for the
 TMEM copy guard; the vector buffer's release point turns out to be implied
 by the slot order.
 """
@@ -62,10 +62,10 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
     events = []
 
     def a_slot(s):
-        return (s + 1) & 1
+        return 0
 
     def b_slot(s):
-        return s & 1
+        return 1
 
     def wait(bar, parity, who, phase=None):
         yield ("wait", lambda: bar.passes(parity))
@@ -90,13 +90,13 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                     errors.append(f"S({s}) read slot {a_slot(s)} holding {slot[a_slot(s)]}")
                 if len(copied) < WARPS:
                     errors.append(f"S({s}) read its TMEM operand before every warp copied its rows")
-                if s > 0 and len(read_dp.get(s - 1, ())) < WARPS:
-                    errors.append(f"S({s}) overwrote dP({s - 1}) before every warp read it")
+                if len(read_dp.get(s, ())) < WARPS:
+                    errors.append(f"S({s}) overwrote dP({s}) before every warp read it")
             elif kind == "dP":
                 if slot[b_slot(s)] != ("B", s):
                     errors.append(f"dP({s}) read slot {b_slot(s)} holding {slot[b_slot(s)]}")
-                if len(read_s.get(s, ())) < WARPS:
-                    errors.append(f"dP({s}) overwrote S({s}) before every warp read it")
+                if s > 0 and len(read_s.get(s - 1, ())) < WARPS:
+                    errors.append(f"dP({s}) overwrote S({s - 1}) before every warp read it")
             elif kind == "acc":
                 if ds_buf[0] is None or ds_buf[0][0] != s or len(ds_buf[0][1]) < WARPS:
                     errors.append(f"accumulate({s}) read dS holding {ds_buf[0]}")
@@ -147,6 +147,7 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             later(rng.uniform(300, 4000), land(i, what))
 
         for s in range(n):
+            yield from load(b_slot(s), ("B", s))
             yield from load(a_slot(s), ("A", s))
             if dk_pass:
                 x = s & 1
@@ -155,7 +156,6 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 vec_full[x].arrive()
                 vec[x] = None
                 later(rng.uniform(200, 2000), land_vec(x, s))
-            yield from load(b_slot(s), ("B", s))
 
     # ------------------------------------------------------------ issuer
     def issuer():
@@ -171,24 +171,22 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             return
         yield from wait(t_full, 0, "issuer t_full", 0)
         yield from wait(t_copied, 0, "issuer copied", 0)
-        yield from wait_full(a_slot(0))
-        pipe.extend([("S", 0), ("commit", s_full)])
-        if not release_a_after_acc:
-            pipe.append(("commit", empty[a_slot(0)]))
+        yield from wait_full(b_slot(0))
+        pipe.extend([("dP", 0), ("commit", dp_full), ("commit", empty[b_slot(0)])])
         for s in range(n):
-            if issuer_waits_s_read:
-                yield from wait(s_read, s & 1, "issuer s_read", s)
-            yield from wait_full(b_slot(s))
-            pipe.extend([("dP", s), ("commit", dp_full), ("commit", empty[b_slot(s)])])
+            if issuer_waits_s_read:                                 # every warp read dP_s
+                yield from wait(s_read, s & 1, "issuer dp read", s)
+            yield from wait_full(a_slot(s))
+            pipe.extend([("S", s), ("commit", s_full)])
+            if not release_a_after_acc:
+                pipe.append(("commit", empty[a_slot(s)]))
             yield from wait(ready, s & 1, "issuer ready", s)
             pipe.append(("acc", s))
             if release_a_after_acc:
                 pipe.append(("commit", empty[a_slot(s)]))
             if s + 1 < n:
-                yield from wait_full(a_slot(s + 1))
-                pipe.extend([("S", s + 1), ("commit", s_full)])
-                if not release_a_after_acc:
-                    pipe.append(("commit", empty[a_slot(s + 1)]))
+                yield from wait_full(b_slot(s + 1))
+                pipe.extend([("dP", s + 1), ("commit", dp_full), ("commit", empty[b_slot(s + 1)])])
         pipe.append(("commit", o_final))
 
     # ------------------------------------------------------------ warps
@@ -202,6 +200,13 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
             t_copied.arrive()
         for s in range(n):
             v = s & 1
+            if warps_wait_dp:
+                yield from wait(dp_full, s & 1, f"warp {w} dp_full", s)
+            if sp[0] != ("dP", s):
+                errors.append(f"warp {w} read dP({s}) from score columns holding {sp[0]}")
+            yield ("delay", rng.uniform(20, 300))                # dP into registers
+            read_dp.setdefault(s, set()).add(w)
+            s_read.arrive()
             yield from wait(s_full, s & 1, f"warp {w} s_full", s)
             if dk_pass:
                 yield from wait(vec_full[v], (s >> 1) & 1, f"warp {w} vec_full", s >> 1)
@@ -211,12 +216,6 @@ def simulate(n, seed, *, dk_pass=True, release_a_after_acc=True, warps_wait_dp=T
                 errors.append(f"warp {w} read S({s}) from score columns holding {sp[0]}")
             yield ("delay", rng.uniform(*warp_cycles))          # S read, P formed
             read_s.setdefault(s, set()).add(w)
-            s_read.arrive()
-            if warps_wait_dp:
-                yield from wait(dp_full, s & 1, f"warp {w} dp_full", s)
-            if sp[0] != ("dP", s):
-                errors.append(f"warp {w} read dP({s}) from score columns holding {sp[0]}")
-            read_dp.setdefault(s, set()).add(w)
             if dk_pass and not vec_release_last:
                 vec_empty[v].arrive()
                 yield ("delay", rng.uniform(0, 400))
@@ -288,34 +287,35 @@ def bad_runs(dk_pass=True, **kw):
 @pytest.mark.parametrize("dk_pass", [True, False])
 def test_a_slot_must_wait_for_the_accumulate(dk_pass):
     """A_s is read by S_s and by the accumulate; releasing its slot after S_s
-    lets B_{s+1} land over it before the accumulate has read it."""
+    lets A_{s+1} land over it before the accumulate has read it."""
     assert bad_runs(dk_pass, release_a_after_acc=False) > 0
 
 
 @pytest.mark.parametrize("dk_pass", [True, False])
 def test_warps_must_wait_for_dp(dk_pass):
-    """P is formed before dP arrives; the dP read still needs its own wait."""
+    """The warps read dP first, into registers; that read needs its own wait."""
     assert bad_runs(dk_pass, warps_wait_dp=False) > 0
 
 
 @pytest.mark.parametrize("dk_pass", [True, False])
-def test_slots_0_1_must_wait_for_the_tmem_copy(dk_pass):
-    """K (dK pass) or Q (dQ pass) lands in slots 0 and 1 and each warp copies
-    its rows into TMEM; a load into those slots before every warp has copied
-    would overwrite the operand under a warp still reading it."""
+def test_slot_0_must_wait_for_the_tmem_copy(dk_pass):
+    """K (dK pass) or Q (dQ pass) lands in slot 0 and each warp copies its
+    rows into TMEM; a load into that slot before every warp has copied would
+    overwrite the operand under a warp still reading it."""
     assert bad_runs(dk_pass, producer_waits_copy=False) > 0
 
 
 @pytest.mark.parametrize("dk_pass", [True, False])
-def test_dp_must_wait_until_every_warp_read_s(dk_pass):
-    """S and dP share the score columns: dP_s may go in only once every warp
-    has read S_s."""
+def test_scores_must_wait_until_every_warp_read_dp(dk_pass):
+    """dP and S share the score columns: S_s may go in only once every warp
+    has read dP_s."""
     assert bad_runs(dk_pass, issuer_waits_s_read=False) > 0
 
 
 def test_vector_release_is_implied_by_the_slot_order():
     """Not load-bearing: the producer loads step s + 2's LSE and D only after
-    A_{s+2}, whose slot the accumulate of step s frees, and that accumulate
-    waits for every warp's dS of step s, written after its D read. So handing
-    the vector buffer back early is still safe."""
+    A_{s+2}, whose slot the accumulate of step s + 1 frees, and that
+    accumulate waits for every warp's dS of step s + 1, written after the
+    warp finished step s. So handing the vector buffer back early is still
+    safe."""
     assert bad_runs(True, vec_release_last=False) == 0
